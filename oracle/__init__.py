@@ -1,0 +1,215 @@
+"""CSA2 oracle (test infrastructure only).
+
+A plain single-threaded CPU definition of the CSA2 sparse-attention hot path
+in fp64 (``csa2_oracle.c``), bound with ctypes.  Only the test suite, the
+package's smoke check and the benchmark's CPU-baseline leg may import it.  It
+imports nothing from the CUDA package and shares no code with it.
+
+Every function cites the passage of the DeepSeek-V4.1-Flash pages it follows;
+the readings taken where the pages are silent are listed in the header of
+``csa2_oracle.c``.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+from typing import Optional, Sequence
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "csa2_oracle.c")
+_LIB_PATH = os.path.join(_HERE, "_libcsa2_oracle.so")
+_lock = threading.Lock()
+_lib = None
+
+FULL, REINDEX, REUSE = 0, 1, 2
+
+
+def build(force: bool = False) -> str:
+    """Compile the oracle (gcc, no fast-math, no FMA contraction)."""
+    if (not force and os.path.exists(_LIB_PATH)
+            and os.path.getmtime(_LIB_PATH) >= os.path.getmtime(_SRC)):
+        return _LIB_PATH
+    tmp = _LIB_PATH + f".tmp{os.getpid()}"
+    subprocess.run(["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-ffp-contract=off",
+                    "-o", tmp, _SRC, "-lm"], check=True)
+    os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            build()
+            lib = ctypes.CDLL(_LIB_PATH)
+            vp, i32, i64, dbl = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_double
+            sig = {
+                "orc_e2m1_value": (dbl, [i32]),
+                "orc_e4m3_value": (dbl, [i32]),
+                "orc_e4m3_encode": (i32, [dbl]),
+                "orc_e2m1_encode_magnitude": (i32, [dbl]),
+                "orc_fp4_row_bytes": (i64, [i32]),
+                "orc_quantize_kv_fp4": (None, [vp, i64, i32, vp]),
+                "orc_dequantize_kv_fp4": (None, [vp, i64, i32, vp]),
+                "orc_n_visible": (i64, [vp, i32, i32, i64]),
+                "orc_index_scores": (None, [vp, vp, i32, i32, i32, i64, i64, i32, vp, i32, vp]),
+                "orc_topk": (None, [vp, i32, i64, i32, vp, i32, vp]),
+                "orc_hier_pool_index": (None, [vp, vp, i32, i32, i32, i64, i64, i32, vp, i32, i32,
+                                               vp]),
+                "orc_sparse_attn": (None, [vp, vp, i32, i32, i32, i64, i64, i32, vp, i32, dbl,
+                                           vp, vp]),
+                "orc_layer_group": (i32, [i32, vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32,
+                                          i32, i64, i64, i32, vp, i32, i32, i32, vp, dbl]),
+            }
+            for name, (res, args) in sig.items():
+                f = getattr(lib, name)
+                f.restype = res
+                f.argtypes = args
+            _lib = lib
+    return _lib
+
+
+def _ptr(a: Optional[np.ndarray]):
+    return None if a is None else a.ctypes.data
+
+
+def _c(a, dtype) -> np.ndarray:
+    return np.ascontiguousarray(a, dtype=dtype)
+
+
+# --- formats (DeepSeek-V4.1-Flash pages: release summary "CSA2"; walkthrough 1.(5).4) ---
+
+def e2m1_value(code: int) -> float:
+    return _load().orc_e2m1_value(code)
+
+
+def e4m3_value(byte: int) -> float:
+    return _load().orc_e4m3_value(byte)
+
+
+def e4m3_encode(v: float) -> int:
+    return _load().orc_e4m3_encode(float(v))
+
+
+def e2m1_encode_magnitude(q: float) -> int:
+    return _load().orc_e2m1_encode_magnitude(float(q))
+
+
+def fp4_row_bytes(d: int) -> int:
+    return int(_load().orc_fp4_row_bytes(d))
+
+
+def quantize_kv_fp4(x: np.ndarray) -> np.ndarray:
+    """fp32 [n][d] -> uint8 [n][d/2 + d/16] (walkthrough 1.(5).4 "FP4 Main KV Cache")."""
+    x = _c(x, np.float32)
+    n, d = x.shape
+    out = np.empty((n, fp4_row_bytes(d)), dtype=np.uint8)
+    _load().orc_quantize_kv_fp4(_ptr(x), n, d, _ptr(out))
+    return out
+
+
+def dequantize_kv_fp4(rows: np.ndarray, d: int) -> np.ndarray:
+    rows = _c(rows, np.uint8)
+    n = rows.shape[0]
+    out = np.empty((n, d), dtype=np.float64)
+    _load().orc_dequantize_kv_fp4(_ptr(rows), n, d, _ptr(out))
+    return out
+
+
+def n_visible(q_pos: Optional[np.ndarray], q: int, ratio: int, N: int) -> int:
+    qp = None if q_pos is None else _c(q_pos, np.int32)
+    return int(_load().orc_n_visible(_ptr(qp), q, ratio, N))
+
+
+# --- indexer, top-k, pool (walkthrough 1.(4), 1.(4).1, 1.(4).2) ---
+
+def index_scores(q_fp8, k_fp8, N: int, kv_seq_stride: int, q_per_seq: int, q_pos, ratio: int):
+    """q_fp8 [B][H_I][D_I], k_fp8 [S*stride][D_I] -> fp64 scores [B][N] (-inf if invisible)."""
+    q_fp8 = _c(q_fp8, np.uint8)
+    k_fp8 = _c(k_fp8, np.uint8)
+    B, H_I, D_I = q_fp8.shape
+    qp = None if q_pos is None else _c(q_pos, np.int32)
+    out = np.empty((B, N), dtype=np.float64)
+    _load().orc_index_scores(_ptr(q_fp8), _ptr(k_fp8), B, H_I, D_I, N, kv_seq_stride, q_per_seq,
+                             _ptr(qp), ratio, _ptr(out))
+    return out
+
+
+def topk(scores, k: int, q_pos=None, ratio: int = 1) -> np.ndarray:
+    """scores [B][N] (any float type, compared as fp64) -> int32 idx [B][k]."""
+    scores = _c(scores, np.float64)
+    B, N = scores.shape
+    qp = None if q_pos is None else _c(q_pos, np.int32)
+    out = np.empty((B, k), dtype=np.int32)
+    _load().orc_topk(_ptr(scores), B, N, k, _ptr(qp), ratio, _ptr(out))
+    return out
+
+
+def hier_pool_index(q_fp8, k_fp8, N: int, kv_seq_stride: int, q_per_seq: int, pool, k: int):
+    q_fp8 = _c(q_fp8, np.uint8)
+    k_fp8 = _c(k_fp8, np.uint8)
+    pool = _c(pool, np.int32)
+    B, H_I, D_I = q_fp8.shape
+    P = pool.shape[1]
+    out = np.empty((B, k), dtype=np.int32)
+    _load().orc_hier_pool_index(_ptr(q_fp8), _ptr(k_fp8), B, H_I, D_I, N, kv_seq_stride,
+                                q_per_seq, _ptr(pool), P, k, _ptr(out))
+    return out
+
+
+# --- attention (walkthrough 1.(4), 1.(5).4, 2.(2).1) ---
+
+def sparse_attn(q_bf16, kv_fp4, N: int, kv_seq_stride: int, q_per_seq: int, idx, scale: float):
+    """q_bf16 [B][H][D] (uint16 bits), kv_fp4 [S*stride][9D/16], idx [B][k] -> (out, lse) fp64."""
+    q_bf16 = _c(q_bf16, np.uint16)
+    kv_fp4 = _c(kv_fp4, np.uint8)
+    idx = _c(idx, np.int32)
+    B, H, D = q_bf16.shape
+    k = idx.shape[1]
+    out = np.empty((B, H, D), dtype=np.float64)
+    lse = np.empty((B, H), dtype=np.float64)
+    _load().orc_sparse_attn(_ptr(q_bf16), _ptr(kv_fp4), B, H, D, N, kv_seq_stride, q_per_seq,
+                            _ptr(idx), k, float(scale), _ptr(out), _ptr(lse))
+    return out, lse
+
+
+def layer_group(modes: Sequence[int], q_bf16: Sequence[np.ndarray], qi_fp8: Sequence[np.ndarray],
+                kv_fp4, ki_fp8, N: int, kv_seq_stride: int, q_per_seq: int, q_pos, ratio: int,
+                k: int, pool_size: int, scale: float):
+    """Runs the layer schedule (walkthrough 1.(4).1 and 1.(4).2).
+
+    Returns (outs, lses, idxs, pool) with one array per layer."""
+    L = len(modes)
+    q_bf16 = [_c(q, np.uint16) for q in q_bf16]
+    B, H, D = q_bf16[0].shape
+    H_I, D_I = None, None
+    qis = []
+    for l in range(L):
+        qi = qi_fp8[l]
+        if qi is None:
+            qis.append(None)
+        else:
+            qi = _c(qi, np.uint8)
+            H_I, D_I = qi.shape[1], qi.shape[2]
+            qis.append(qi)
+    kv_fp4 = _c(kv_fp4, np.uint8)
+    ki_fp8 = _c(ki_fp8, np.uint8)
+    qp = None if q_pos is None else _c(q_pos, np.int32)
+    outs = [np.empty((B, H, D), np.float64) for _ in range(L)]
+    lses = [np.empty((B, H), np.float64) for _ in range(L)]
+    idxs = [np.empty((B, k), np.int32) for _ in range(L)]
+    pool = np.empty((B, max(pool_size, 1)), np.int32)
+    P = ctypes.c_void_p
+    arr = lambda xs: (P * L)(*[_ptr(x) for x in xs])
+    modes_c = (ctypes.c_int * L)(*modes)
+    rc = _load().orc_layer_group(L, modes_c, arr(q_bf16), arr(qis), arr(outs), arr(lses),
+                                 arr(idxs), _ptr(kv_fp4), _ptr(ki_fp8), B, H, H_I, D, D_I, N,
+                                 kv_seq_stride, q_per_seq, _ptr(qp), ratio, k, pool_size,
+                                 _ptr(pool), float(scale))
+    if rc != 0:
+        raise ValueError("invalid layer schedule")
+    return outs, lses, idxs, (pool if pool_size > 0 else None)

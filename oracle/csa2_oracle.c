@@ -1,0 +1,414 @@
+/*
+ * CSA2 oracle: a plain, slow, single-threaded CPU definition of the CSA2
+ * sparse-attention hot path, in fp64.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Only the test suite, the package's smoke check
+ * and the benchmark's CPU-baseline leg may load this code.  It shares no
+ * code, header, table or helper with the CUDA library; the two meet only in
+ * the seeded input bytes.
+ *
+ * Sources (web pages on DeepSeek-V4.1-Flash; citations name the page and its
+ * section):
+ *  [P2]  modelscope.csdn.net release summary, section "CSA2": three static
+ *        layer modes Full / Reindex / Reuse that share main KV and indexer K
+ *        and reuse top-k indices; FP4 main-KV cache in E2M1 with one E4M3
+ *        scale per 16 channels.
+ *  [P4a] wkq9411.github.io paper walkthrough, section 1.(4) "CSA2": a
+ *        lightweight indexer scores main-KV entries with indexer Q and K and
+ *        keeps the top-k entries per query; each query attends the selected
+ *        entries; ratio-m compression without overlap.
+ *  [P4b] same page, 1.(4).1 "Cross-Layer KV and Index Reuse": what each mode
+ *        computes and what it takes from earlier layers.
+ *  [P4c] same page, 1.(4).2 "Hierarchical Sparse Indexer": the first Full
+ *        layer builds a candidate pool, later Reindex layers score only pool
+ *        positions and take their own top-k there.
+ *  [P4d] same page, 1.(5).4 "FP4 Main KV Cache": E2M1 values, one E4M3 scale
+ *        per 16 channels, no second-level global scale, largest magnitude
+ *        448 x 6 = 2688, quantised after RoPE, dequantised before attention.
+ *  [P4e] same page, 2.(2).1 "Model settings": 64 main query heads of 512 dims.
+ *
+ * Readings where the pages are silent (each is also listed in the design doc):
+ *  R1  scale byte = E4M3(absmax/6) rounded to nearest even, saturating at 448;
+ *      code = E2M1 value nearest to the exact quotient |x|/scale, ties to the
+ *      even code; sign bit = sign bit of x; scale 0 gives magnitude code 0.
+ *  R2  row layout: D/2 code bytes (channel 2j in the low nibble of byte j),
+ *      then D/16 scale bytes (byte b covers channels 16b..16b+15).
+ *  R3  indexer score = sum over indexer heads of the dot product of that
+ *      head's q with the entry's single (head-shared) indexer K vector.
+ *  R4  entry j of a ratio-r context is visible to the query at token
+ *      position pos iff r*j + r - 1 <= pos (the entry's last token is not
+ *      in the future).  No position array means every entry is visible.
+ *  R5  top-k = the min(k, visible) visible entries ranked by score
+ *      descending then index ascending; returned in ascending index order,
+ *      padded with -1.
+ *  R6  hierarchical pool = the top-P of the Full layer's scores (flat pool of
+ *      positions); a Reindex layer scores only pool entries and ranks them by
+ *      (score desc, entry index asc).
+ *  R7  attention: K = V = the dequantised 512-channel latent shared by all
+ *      heads (MQA over the latent); logits = scale * <q_h, v_j>; softmax over
+ *      the selected entries; -1 slots are skipped; no valid slot gives
+ *      o = 0 and lse = -inf.  No RoPE is applied (the cache is quantised
+ *      after RoPE).
+ *  R8  a Reuse layer takes the indices of the nearest preceding Full or
+ *      Reindex layer.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+/* ---------------------------------------------------------------------- */
+/* Formats [P2], [P4d]                                                     */
+/* ---------------------------------------------------------------------- */
+
+/* E2M1: sign bit, 2 exponent bits (bias 1), 1 mantissa bit.  Magnitudes of
+ * codes 0..7: 0, 0.5, 1, 1.5, 2, 3, 4, 6. */
+double orc_e2m1_value(int code) {
+  int s = (code >> 3) & 1, e = (code >> 1) & 3, m = code & 1;
+  double mag = (e == 0) ? 0.5 * m : (1.0 + 0.5 * m) * ldexp(1.0, e - 1);
+  return s ? -mag : mag;
+}
+
+/* E4M3 (OCP 8-bit floating point, "e4m3fn"): sign, 4 exponent bits (bias 7),
+ * 3 mantissa bits, no infinities, S.1111.111 is NaN. */
+double orc_e4m3_value(int byte) {
+  int s = (byte >> 7) & 1, e = (byte >> 3) & 15, m = byte & 7;
+  double mag;
+  if (e == 15 && m == 7) return NAN;
+  if (e == 0) mag = (m / 8.0) * ldexp(1.0, -6);
+  else mag = (1.0 + m / 8.0) * ldexp(1.0, e - 7);
+  return s ? -mag : mag;
+}
+
+/* Nearest E4M3 byte to v, ties to the even mantissa (even byte), saturating
+ * to the largest finite magnitude 448.  Exhaustive search over the 127
+ * non-negative finite codes. */
+int orc_e4m3_encode(double v) {
+  if (isnan(v)) return 0x7F;
+  int sign = signbit(v) ? 0x80 : 0;
+  double a = fabs(v);
+  if (a >= 448.0) return sign | 0x7E;
+  int best = 0;
+  double best_d = INFINITY;
+  for (int c = 0; c <= 0x7E; ++c) {
+    double d = fabs(orc_e4m3_value(c) - a);
+    if (d < best_d || (d == best_d && (c & 1) == 0)) {
+      best = c;
+      best_d = d;
+    }
+  }
+  return sign | best;
+}
+
+/* Nearest of the 8 E2M1 magnitudes to q >= 0, ties to the even code. */
+int orc_e2m1_encode_magnitude(double q) {
+  int best = 0;
+  double best_d = INFINITY;
+  for (int c = 0; c < 8; ++c) {
+    double d = fabs(orc_e2m1_value(c) - q);
+    if (d < best_d || (d == best_d && (c & 1) == 0)) {
+      best = c;
+      best_d = d;
+    }
+  }
+  return best;
+}
+
+static double bf16_value(uint16_t bits) {
+  uint32_t u = (uint32_t)bits << 16;
+  float f;
+  memcpy(&f, &u, 4);
+  return (double)f;
+}
+
+/* ---------------------------------------------------------------------- */
+/* FP4 main-KV quantise / dequantise [P4d], readings R1, R2                */
+/* ---------------------------------------------------------------------- */
+
+int64_t orc_fp4_row_bytes(int d) { return d / 2 + d / 16; }
+
+/* x: fp32 [n_rows][d] -> out: [n_rows][d/2 + d/16] bytes.  d % 16 == 0. */
+void orc_quantize_kv_fp4(const float* x, int64_t n_rows, int d, uint8_t* out) {
+  int64_t rb = orc_fp4_row_bytes(d);
+  for (int64_t r = 0; r < n_rows; ++r) {
+    const float* xr = x + r * d;
+    uint8_t* codes = out + r * rb;
+    uint8_t* scales = codes + d / 2;
+    memset(codes, 0, (size_t)(d / 2));
+    for (int b = 0; b < d / 16; ++b) {
+      double amax = 0.0;
+      for (int i = 0; i < 16; ++i) amax = fmax(amax, fabs((double)xr[16 * b + i]));
+      /* amax/6 and |x|/s below are fp64 quotients of an fp32 value by a
+       * number of at most 4 significant bits.  Such a quotient can equal a
+       * rounding midpoint (at most 5 significant bits) only if the exact
+       * quotient equals it, because an fp32 dividend next to 6 x midpoint
+       * (resp. s x midpoint) differs from it by at least 2^-24 relative,
+       * far above fp64's 2^-53; so rounding the fp64 quotient is rounding
+       * the exact quotient. */
+      int sbyte = orc_e4m3_encode(amax / 6.0);
+      double s = orc_e4m3_value(sbyte);
+      scales[b] = (uint8_t)sbyte;
+      for (int i = 0; i < 16; ++i) {
+        int ch = 16 * b + i;
+        double xv = (double)xr[ch];
+        int mag = (s == 0.0) ? 0 : orc_e2m1_encode_magnitude(fabs(xv) / s);
+        int code = (signbit(xv) ? 8 : 0) | mag;
+        codes[ch / 2] |= (uint8_t)((ch & 1) ? (code << 4) : code);
+      }
+    }
+  }
+}
+
+/* One row of [d/2 + d/16] bytes -> d values: code value x scale. */
+void orc_dequantize_row(const uint8_t* row, int d, double* out) {
+  const uint8_t* scales = row + d / 2;
+  for (int ch = 0; ch < d; ++ch) {
+    int code = (ch & 1) ? (row[ch / 2] >> 4) : (row[ch / 2] & 15);
+    out[ch] = orc_e2m1_value(code) * orc_e4m3_value(scales[ch / 16]);
+  }
+}
+
+void orc_dequantize_kv_fp4(const uint8_t* rows, int64_t n_rows, int d, double* out) {
+  int64_t rb = orc_fp4_row_bytes(d);
+  for (int64_t r = 0; r < n_rows; ++r) orc_dequantize_row(rows + r * rb, d, out + r * d);
+}
+
+/* ---------------------------------------------------------------------- */
+/* Causal visibility [P4a], reading R4                                     */
+/* ---------------------------------------------------------------------- */
+
+int64_t orc_n_visible(const int32_t* q_pos, int q, int ratio, int64_t N) {
+  if (!q_pos) return N;
+  /* visibility is monotone in j, so the visible entries form a prefix;
+   * count it straight from the definition */
+  int64_t pos = q_pos[q], n = 0;
+  while (n < N && (int64_t)ratio * n + ratio - 1 <= pos) ++n;
+  return n;
+}
+
+/* ---------------------------------------------------------------------- */
+/* Indexer scores [P4a], [P4b], reading R3                                 */
+/* ---------------------------------------------------------------------- */
+
+/* scores[q][j] = sum_h sum_d qI[q][h][d] * KI[seq(q)][j][d] for visible j,
+ * -inf otherwise.  q_fp8 [B][H_I][D_I], k_fp8 [S][N][D_I] (sequence s at
+ * offset s * kv_seq_stride entries), scores [B][N]. */
+void orc_index_scores(const uint8_t* q_fp8, const uint8_t* k_fp8, int B, int H_I, int D_I,
+                      int64_t N, int64_t kv_seq_stride, int q_per_seq, const int32_t* q_pos,
+                      int ratio, double* scores) {
+  double* kj = (double*)malloc(sizeof(double) * D_I);
+  double* qv = (double*)malloc(sizeof(double) * H_I * D_I);
+  for (int q = 0; q < B; ++q) {
+    const uint8_t* kseq = k_fp8 + (int64_t)(q / q_per_seq) * kv_seq_stride * D_I;
+    int64_t nv = orc_n_visible(q_pos, q, ratio, N);
+    for (int i = 0; i < H_I * D_I; ++i) qv[i] = orc_e4m3_value(q_fp8[(int64_t)q * H_I * D_I + i]);
+    for (int64_t j = 0; j < N; ++j) {
+      if (j >= nv) {
+        scores[(int64_t)q * N + j] = -INFINITY;
+        continue;
+      }
+      for (int d = 0; d < D_I; ++d) kj[d] = orc_e4m3_value(kseq[j * D_I + d]);
+      double s = 0.0;
+      for (int h = 0; h < H_I; ++h) {
+        double dot = 0.0;
+        for (int d = 0; d < D_I; ++d) dot += qv[h * D_I + d] * kj[d];
+        s += dot;
+      }
+      scores[(int64_t)q * N + j] = s;
+    }
+  }
+  free(kj);
+  free(qv);
+}
+
+/* ---------------------------------------------------------------------- */
+/* Top-k [P4a], reading R5                                                 */
+/* ---------------------------------------------------------------------- */
+
+typedef struct {
+  double s;
+  int64_t j;
+} cand_t;
+
+static int cmp_rank(const void* a, const void* b) {
+  const cand_t* x = (const cand_t*)a;
+  const cand_t* y = (const cand_t*)b;
+  if (x->s > y->s) return -1;
+  if (x->s < y->s) return 1;
+  return (x->j < y->j) ? -1 : (x->j > y->j);
+}
+
+static int cmp_i32(const void* a, const void* b) {
+  int32_t x = *(const int32_t*)a, y = *(const int32_t*)b;
+  return (x > y) - (x < y);
+}
+
+/* Rank n candidates, write the first min(k, n) entry ids in ascending order
+ * to out[0..k), pad with -1. */
+static void select_topk(cand_t* c, int64_t n, int k, int32_t* out) {
+  qsort(c, (size_t)n, sizeof(cand_t), cmp_rank);
+  int64_t take = n < k ? n : k;
+  for (int64_t t = 0; t < take; ++t) out[t] = (int32_t)c[t].j;
+  qsort(out, (size_t)take, sizeof(int32_t), cmp_i32);
+  for (int64_t t = take; t < k; ++t) out[t] = -1;
+}
+
+/* scores [B][N] -> idx [B][k]; only visible entries (R4) are candidates. */
+void orc_topk(const double* scores, int B, int64_t N, int k, const int32_t* q_pos, int ratio,
+              int32_t* idx) {
+  cand_t* c = (cand_t*)malloc(sizeof(cand_t) * (N > 0 ? N : 1));
+  for (int q = 0; q < B; ++q) {
+    int64_t nv = orc_n_visible(q_pos, q, ratio, N);
+    for (int64_t j = 0; j < nv; ++j) {
+      c[j].s = scores[(int64_t)q * N + j];
+      c[j].j = j;
+    }
+    select_topk(c, nv, k, idx + (int64_t)q * k);
+  }
+  free(c);
+}
+
+/* ---------------------------------------------------------------------- */
+/* Hierarchical Sparse Indexer, Reindex-in-pool [P4c], reading R6          */
+/* ---------------------------------------------------------------------- */
+
+/* For each query, score only the entries listed in pool[q][0..P) (-1 slots
+ * skipped) and keep the top-k of them by (score desc, entry id asc). */
+void orc_hier_pool_index(const uint8_t* q_fp8, const uint8_t* k_fp8, int B, int H_I, int D_I,
+                         int64_t N, int64_t kv_seq_stride, int q_per_seq, const int32_t* pool,
+                         int P, int k, int32_t* idx) {
+  cand_t* c = (cand_t*)malloc(sizeof(cand_t) * (P > 0 ? P : 1));
+  double* qv = (double*)malloc(sizeof(double) * H_I * D_I);
+  for (int q = 0; q < B; ++q) {
+    const uint8_t* kseq = k_fp8 + (int64_t)(q / q_per_seq) * kv_seq_stride * D_I;
+    for (int i = 0; i < H_I * D_I; ++i) qv[i] = orc_e4m3_value(q_fp8[(int64_t)q * H_I * D_I + i]);
+    int64_t n = 0;
+    for (int p = 0; p < P; ++p) {
+      int32_t j = pool[(int64_t)q * P + p];
+      if (j < 0 || j >= N) continue;
+      double s = 0.0;
+      for (int h = 0; h < H_I; ++h) {
+        double dot = 0.0;
+        for (int d = 0; d < D_I; ++d)
+          dot += qv[h * D_I + d] * orc_e4m3_value(kseq[(int64_t)j * D_I + d]);
+        s += dot;
+      }
+      c[n].s = s;
+      c[n].j = j;
+      ++n;
+    }
+    select_topk(c, n, k, idx + (int64_t)q * k);
+  }
+  free(c);
+  free(qv);
+}
+
+/* ---------------------------------------------------------------------- */
+/* Sparse MQA attention over the selected FP4 entries [P4a], [P4d], R7     */
+/* ---------------------------------------------------------------------- */
+
+/* q_bf16 [B][H][D] (bf16 bits), kv_fp4 [S][N][D/2 + D/16], idx [B][k]
+ * -> out [B][H][D] (fp64), lse [B][H] (fp64, may be NULL). */
+void orc_sparse_attn(const uint16_t* q_bf16, const uint8_t* kv_fp4, int B, int H, int D, int64_t N,
+                     int64_t kv_seq_stride, int q_per_seq, const int32_t* idx, int k,
+                     double scale, double* out, double* lse) {
+  int64_t rb = orc_fp4_row_bytes(D);
+  double* v = (double*)malloc(sizeof(double) * (size_t)(k > 0 ? k : 1) * D);
+  double* logit = (double*)malloc(sizeof(double) * (size_t)(k > 0 ? k : 1));
+  double* qh = (double*)malloc(sizeof(double) * D);
+  for (int q = 0; q < B; ++q) {
+    const uint8_t* kvseq = kv_fp4 + (int64_t)(q / q_per_seq) * kv_seq_stride * rb;
+    /* gather and dequantise the selected rows */
+    int n = 0;
+    for (int t = 0; t < k; ++t) {
+      int32_t j = idx[(int64_t)q * k + t];
+      if (j < 0 || j >= N) continue;
+      orc_dequantize_row(kvseq + (int64_t)j * rb, D, v + (int64_t)n * D);
+      ++n;
+    }
+    for (int h = 0; h < H; ++h) {
+      double* o = out + ((int64_t)q * H + h) * D;
+      for (int c = 0; c < D; ++c) qh[c] = bf16_value(q_bf16[((int64_t)q * H + h) * D + c]);
+      if (n == 0) {
+        for (int c = 0; c < D; ++c) o[c] = 0.0;
+        if (lse) lse[(int64_t)q * H + h] = -INFINITY;
+        continue;
+      }
+      double m = -INFINITY;
+      for (int t = 0; t < n; ++t) {
+        double dot = 0.0;
+        for (int c = 0; c < D; ++c) dot += qh[c] * v[(int64_t)t * D + c];
+        logit[t] = scale * dot;
+        if (logit[t] > m) m = logit[t];
+      }
+      double l = 0.0;
+      for (int t = 0; t < n; ++t) {
+        logit[t] = exp(logit[t] - m); /* now the unnormalised weight */
+        l += logit[t];
+      }
+      for (int c = 0; c < D; ++c) o[c] = 0.0;
+      for (int t = 0; t < n; ++t) {
+        double p = logit[t] / l;
+        for (int c = 0; c < D; ++c) o[c] += p * v[(int64_t)t * D + c];
+      }
+      if (lse) lse[(int64_t)q * H + h] = m + log(l);
+    }
+  }
+  free(v);
+  free(logit);
+  free(qh);
+}
+
+/* ---------------------------------------------------------------------- */
+/* Layer modes Full / Reindex / Reuse [P4b], [P4c], reading R8             */
+/* ---------------------------------------------------------------------- */
+
+enum { ORC_FULL = 0, ORC_REINDEX = 1, ORC_REUSE = 2 };
+
+/* Runs n_layers layers over one shared FP4 main KV and indexer K.
+ *   modes[l]          FULL / REINDEX / REUSE; layer 0 must be FULL
+ *   q_bf16[l]         [B][H][D] main query of layer l
+ *   qi_fp8[l]         [B][H_I][D_I] indexer query (ignored for REUSE)
+ *   out[l], lse[l]    [B][H][D], [B][H] outputs (lse may be NULL)
+ *   idx_out[l]        [B][k] indices layer l attended (written for every layer)
+ *   pool_out          [B][pool_size] when pool_size > 0 (built by FULL layers)
+ * Returns 0, or -1 for an invalid schedule. */
+int orc_layer_group(int n_layers, const int* modes, const uint16_t* const* q_bf16,
+                    const uint8_t* const* qi_fp8, double* const* out, double* const* lse,
+                    int32_t* const* idx_out, const uint8_t* kv_fp4, const uint8_t* ki_fp8, int B,
+                    int H, int H_I, int D, int D_I, int64_t N, int64_t kv_seq_stride,
+                    int q_per_seq, const int32_t* q_pos, int ratio, int k, int pool_size,
+                    int32_t* pool_out, double scale) {
+  if (n_layers < 1 || modes[0] != ORC_FULL) return -1;
+  double* scores = (double*)malloc(sizeof(double) * (size_t)B * (size_t)(N > 0 ? N : 1));
+  const int32_t* latest = NULL;
+  for (int l = 0; l < n_layers; ++l) {
+    int32_t* idx = idx_out[l];
+    if (modes[l] == ORC_FULL) {
+      orc_index_scores(qi_fp8[l], ki_fp8, B, H_I, D_I, N, kv_seq_stride, q_per_seq, q_pos, ratio,
+                       scores);
+      orc_topk(scores, B, N, k, q_pos, ratio, idx);
+      if (pool_size > 0) orc_topk(scores, B, N, pool_size, q_pos, ratio, pool_out);
+      latest = idx;
+    } else if (modes[l] == ORC_REINDEX) {
+      if (pool_size > 0) {
+        orc_hier_pool_index(qi_fp8[l], ki_fp8, B, H_I, D_I, N, kv_seq_stride, q_per_seq, pool_out,
+                            pool_size, k, idx);
+      } else {
+        orc_index_scores(qi_fp8[l], ki_fp8, B, H_I, D_I, N, kv_seq_stride, q_per_seq, q_pos,
+                         ratio, scores);
+        orc_topk(scores, B, N, k, q_pos, ratio, idx);
+      }
+      latest = idx;
+    } else if (modes[l] == ORC_REUSE) {
+      memcpy(idx, latest, sizeof(int32_t) * (size_t)B * (size_t)k);
+    } else {
+      free(scores);
+      return -1;
+    }
+    orc_sparse_attn(q_bf16[l], kv_fp4, B, H, D, N, kv_seq_stride, q_per_seq, idx, k, scale, out[l],
+                    lse ? lse[l] : NULL);
+  }
+  free(scores);
+  return 0;
+}
