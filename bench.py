@@ -1,0 +1,485 @@
+#!/usr/bin/env python
+"""CSA2 sparse-attention decode benchmark.
+
+One step = one pass of the whole hot path over one batch: the Full-mode CSA2
+layer of the 32-query, 64K-token-context decode workload (indexer scores over
+16384 FP4/FP8 entries per query, top-2048, gather + dequantise + 64-head MQA
+attention, split combine), replayed as one CUDA graph of csa2_layer_group.
+Inputs are resident in HBM; L2 is flushed (512 MiB write) before every timed
+step and each step is timed with its own CUDA events.
+
+Prints one JSON line (rank 0).  `--impl reference` times the CPU oracle on a
+bounded sample of the same workload instead.  Under torchrun every rank runs
+an independent replica (the path has no data exchange); the reported value is
+the queries of all ranks over the slowest rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "CSA2 query-tokens/s per layer at 64K ctx; % of GB300 HBM roofline"
+UNIT = "query-tokens/s"
+DEFAULT_WORKLOAD = "decode_b32_ctx64k"
+FLUSH_BYTES = 512 << 20
+
+
+def parse_args():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=20)
+    p.add_argument("--warmup", type=int, default=5)
+    p.add_argument("--impl", default="csa2", choices=["csa2", "reference"])
+    p.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--kernel-loop", default="",
+                   help="run only this many launches of the layer group (for profilers)")
+    return p.parse_args()
+
+
+def dist_setup(args):
+    import torch
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if backend == "nccl":
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend=backend)
+    elif torch.cuda.is_available():
+        torch.cuda.set_device(local)
+    return rank, world, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def allreduce_max(x: float, world: int) -> float:
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64,
+                     device="cuda" if dist.get_backend() == "nccl" else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), float(d.get("bf16_tflops", 1900.0)), "measured"
+    except Exception:
+        return 6800.0, 1900.0, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clock/throttle samples every 200 ms while running."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.proc = None
+        self.dev = device_index
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200", "-i", str(self.dev)],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except Exception:
+            self.proc.kill()
+            out = ""
+        sm, smax, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.strip().splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                smax = float(f[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        busy = [x for x in sm if smax and x > 0.5 * smax] or sm
+        return {"sm_mhz": statistics.median(busy) if busy else None, "sm_max_mhz": smax,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------
+# GPU arm
+# ---------------------------------------------------------------------------
+
+def algorithmic_bytes(w):
+    """Per step: indexer K of every scored entry, indexer q, selected FP4 rows,
+    main queries (bf16) and outputs (fp32), as the workload's layers read them."""
+    from sparse_attention_decode_csa2_gb300.synthetic import FULL, REINDEX, REUSE
+    B, N, k = w.B, w.N, w.k
+    total = 0
+    per_layer = []
+    for l, m in enumerate(w.modes):
+        b = B * k * w.row_bytes + B * w.H * w.D * 2 + B * w.H * w.D * 4
+        if m == FULL or (m == REINDEX and not w.pool):
+            n_scored = sum(min(N, (int(p) + 1) // w.ratio) for p in w.q_pos())
+            b += n_scored * w.D_I + B * w.H_I * w.D_I
+            if w.q_per_seq > 1:   # one shared context: its K is read once
+                b -= n_scored * w.D_I
+                b += w.n_seq * N * w.D_I
+        elif m == REINDEX:
+            b += B * w.pool * (w.D_I + 4) + B * w.H_I * w.D_I
+        per_layer.append(b)
+        total += b
+    return total, per_layer
+
+
+def kernel_bytes(w):
+    """Algorithmic bytes of each timed component op (one launch over the batch)."""
+    B, N, k = w.B, w.N, w.k
+    n_scored = sum(min(N, (int(p) + 1) // w.ratio) for p in w.q_pos())
+    return {
+        "index_scores": n_scored * w.D_I + B * w.H_I * w.D_I + B * N * 4,
+        "topk": n_scored * 4 + B * k * 4,
+        "sparse_attn_fp4": B * k * (w.row_bytes + 4) + B * w.H * w.D * (2 + 4) + B * w.H * 4,
+    }
+
+
+def attn_flops(w):
+    return 4.0 * w.B * w.H * w.k * w.D
+
+
+def run_gpu(args, rank, world, local):
+    import numpy as np
+    import torch
+    from sparse_attention_decode_csa2_gb300 import build
+    if rank == 0 or not os.path.exists(build.LIB_PATH):
+        build.build()
+    barrier(world)
+    from sparse_attention_decode_csa2_gb300 import csa2, workload
+    from sparse_attention_decode_csa2_gb300.synthetic import FULL, REINDEX, REUSE, WORKLOADS
+
+    w = WORKLOADS[args.workload]
+    dev = torch.device("cuda", torch.cuda.current_device())
+    inp = workload.prepare(w, device=dev)
+    lg = inp.layer_group(reuse_idx_copy=False)
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+
+    stream = torch.cuda.Stream(device=dev)
+    with torch.cuda.stream(stream):
+        for _ in range(2):
+            lg()
+    stream.synchronize()
+    code, bits = csa2.read_status(lg.ws)
+    if code != 0:
+        raise RuntimeError(f"device status {bits} after warm-up")
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        lg()
+    torch.cuda.synchronize()
+
+    if args.kernel_loop:
+        for _ in range(int(args.kernel_loop)):
+            flush.zero_()
+            graph.replay()
+        torch.cuda.synchronize()
+        return None
+
+    K, W = args.steps, args.warmup
+    for _ in range(W):
+        flush.zero_()
+        graph.replay()
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(K)]
+    sampler = ClockSampler(local)
+    sampler.start()
+    time.sleep(0.3)
+    barrier(world)
+    torch.cuda.synchronize()
+    t_wall = time.perf_counter()
+    cur = torch.cuda.current_stream()
+    for i in range(K):
+        flush.zero_()
+        ev[i][0].record(cur)
+        graph.replay()
+        ev[i][1].record(cur)
+    torch.cuda.synchronize()
+    barrier(world)
+    t_wall = time.perf_counter() - t_wall
+    step_ms = [a.elapsed_time(b) for a, b in ev]
+
+    # component ops, each timed alone over the same batch (L2 flushed before each)
+    comp = {}
+    scores = torch.empty((w.B, w.N), dtype=torch.float32, device=dev)
+    idx = torch.empty((w.B, w.k), dtype=torch.int32, device=dev)
+    out = torch.empty((w.B, w.H, w.D), dtype=torch.float32, device=dev)
+    lse = torch.empty((w.B, w.H), dtype=torch.float32, device=dev)
+    ws = csa2.make_workspace(w.B, w.N, w.k, w.H, w.pool, dev)
+    ops = {
+        "index_scores": lambda: csa2.index_scores(inp.qi[0], inp.ki_fp8, w.N, w.kv_seq_stride,
+                                                  w.q_per_seq, inp.q_pos, w.ratio, out=scores),
+        "topk": lambda: csa2.topk(scores, w.k, inp.q_pos, w.ratio, ws, out=idx),
+        "sparse_attn_fp4": lambda: csa2.sparse_attn_fp4(inp.q[0], inp.kv_fp4, w.N,
+                                                        w.kv_seq_stride, w.q_per_seq, idx,
+                                                        inp.scale, out=out, lse=lse, ws=ws),
+    }
+    for name, fn in ops.items():
+        fn()
+        torch.cuda.synchronize()
+        e = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+             for _ in range(K)]
+        for i in range(K):
+            flush.zero_()
+            e[i][0].record(cur)
+            fn()
+            e[i][1].record(cur)
+        torch.cuda.synchronize()
+        comp[name] = statistics.mean(a.elapsed_time(b) for a, b in e)
+    clocks = sampler.stop()
+
+    # end to end through the public API with host buffers
+    e2e = None
+    if not args.no_e2e:
+        host_in = {
+            "kv_fp4": inp.kv_fp4.cpu().pin_memory(), "ki_fp8": inp.ki_fp8.cpu().pin_memory(),
+            "q": [t.cpu().pin_memory() for t in inp.q],
+            "qi": [None if t is None else t.cpu().pin_memory() for t in inp.qi],
+            "q_pos": inp.q_pos.cpu().pin_memory(),
+        }
+        host_out = [torch.empty_like(o, device="cpu").pin_memory() for o in lg.out]
+        h2d = (host_in["kv_fp4"].numel() + host_in["ki_fp8"].numel() + host_in["q_pos"].numel() * 4
+               + sum(t.numel() * 2 for t in host_in["q"])
+               + sum(t.numel() for t in host_in["qi"] if t is not None))
+        d2h = sum(o.numel() * 4 for o in host_out)
+
+        def e2e_step():
+            inp.kv_fp4.copy_(host_in["kv_fp4"], non_blocking=True)
+            inp.ki_fp8.copy_(host_in["ki_fp8"], non_blocking=True)
+            inp.q_pos.copy_(host_in["q_pos"], non_blocking=True)
+            for d, h in zip(inp.q, host_in["q"]):
+                d.copy_(h, non_blocking=True)
+            for d, h in zip(inp.qi, host_in["qi"]):
+                if d is not None:
+                    d.copy_(h, non_blocking=True)
+            outs, _, _, _ = lg()
+            for h, o in zip(host_out, outs):
+                h.copy_(o, non_blocking=True)
+
+        for _ in range(max(1, min(W, 3))):
+            e2e_step()
+        torch.cuda.synchronize()
+        Ke = max(3, min(K, 10))
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        barrier(world)
+        e0.record(cur)
+        for _ in range(Ke):
+            e2e_step()
+        e1.record(cur)
+        torch.cuda.synchronize()
+        e2e_s = allreduce_max(e0.elapsed_time(e1) / 1e3, world)
+        e2e = {"value": w.B * Ke * world / e2e_s, "unit": UNIT, "h2d_bytes_per_step": int(h2d),
+               "d2h_bytes_per_step": int(d2h)}
+
+    total_s = allreduce_max(sum(step_ms) / 1e3, world)
+    ms_per_step = total_s * 1e3 / K
+    value = w.B * K * world / total_s   # query tokens through one layer
+    if len(w.modes) > 1:
+        value = value * len(w.modes)    # per layer: every layer processes the batch
+
+    hbm_peak, bf16_peak, peak_src = measured_peaks()
+    step_bytes, _ = algorithmic_bytes(w)
+    kb = kernel_bytes(w)
+    dom = max(comp, key=comp.get)
+    achieved = kb[dom] / (comp[dom] / 1e3) / 1e9
+    traffic = None
+    tpath = os.path.join(ROOT, "profiles", "traffic.json")
+    if os.path.exists(tpath):
+        try:
+            with open(tpath) as f:
+                t = json.load(f)
+            rec = t.get(args.workload, {}).get(dom)
+            if rec and rec.get("kernel_rev") == kernel_revision():
+                traffic = rec.get("bytes_per_launch")
+        except Exception:
+            traffic = None
+    n_launch = csa2.group_launches(lg)
+    res = {
+        "metric": METRIC,
+        "value": value,
+        "unit": UNIT,
+        "n_gpus": world,
+        "steps": K,
+        "warmup": W,
+        "ms_per_step": ms_per_step,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "fp16-mma/fp32-acc (fp4 KV, e4m3 indexer)",
+        "data": "synthetic (seeded SplitMix64: N(0,1) latent -> FP4, integer E4M3 indexer, "
+                "bf16 N(0,1) queries)",
+        "config": {"workload": w.name, "queries": w.B, "entries_per_seq": w.N,
+                   "ctx_tokens": w.N * w.ratio, "heads": w.H, "indexer_heads": w.H_I,
+                   "top_k": w.k, "modes": [["FULL", "REINDEX", "REUSE"][m] for m in w.modes],
+                   "l2": "flushed before every timed step (512 MiB write)",
+                   "cuda_graph": True, "parallelism": f"replicas x{world}"},
+        "step_bytes": step_bytes,
+        "hbm_frac_step": (step_bytes / (ms_per_step / 1e3) / 1e9) / hbm_peak,
+        "roofline": {"bound": "hbm", "kernel": dom, "achieved": achieved, "peak": hbm_peak,
+                     "unit": "GB/s", "frac": achieved / hbm_peak, "traffic": traffic,
+                     "peak_source": peak_src},
+        "kernels_ms": comp,
+        "attn_tflops": attn_flops(w) / (comp["sparse_attn_fp4"] / 1e3) / 1e12,
+        "gpu_launches": n_launch * K,
+        "clocks": clocks,
+        "e2e": e2e,
+        "wall_s": t_wall,
+    }
+    return res
+
+
+def kernel_revision() -> str:
+    import hashlib
+    h = hashlib.sha1()
+    d = os.path.join(ROOT, "sparse_attention_decode_csa2_gb300", "csrc")
+    for n in sorted(os.listdir(d)):
+        with open(os.path.join(d, n), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:12]
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle (baseline and reference arm)
+# ---------------------------------------------------------------------------
+
+class OracleSample:
+    """The oracle's inputs for queries of a workload, prepared outside any timing."""
+
+    def __init__(self, w, queries):
+        import oracle
+        self.oracle = oracle
+        self.w = w
+        self.items = []
+        cache = {}
+        for q in queries:
+            s = q // w.q_per_seq
+            if s not in cache:
+                cache[s] = (oracle.quantize_kv_fp4(w.kv_latent(s)), w.ki_fp8(s))
+            kv, ki = cache[s]
+            L = len(w.modes)
+            self.items.append(dict(q=q, kv=kv, ki=ki, qpos=w.q_pos()[q:q + 1],
+                                   qb=[w.q_bf16(l, [q]) for l in range(L)],
+                                   qi=[w.qi_fp8(l, [q]) if w.modes[l] != 2 else None
+                                       for l in range(L)]))
+
+    def run(self, item):
+        w, o = self.w, self.oracle
+        o.layer_group(w.modes, item["qb"], item["qi"], item["kv"], item["ki"], w.N, 0, 1,
+                      item["qpos"], w.ratio, w.k, w.pool, 1.0 / math.sqrt(w.D))
+
+
+def cpu_baseline(w, budget_s=12.0):
+    n_setup = 2
+    smp = OracleSample(w, list(range(min(n_setup, w.B))))
+    done, t0 = 0, time.perf_counter()
+    while True:
+        smp.run(smp.items[done % len(smp.items)])
+        done += 1
+        el = time.perf_counter() - t0
+        if el >= budget_s or done >= 64:
+            break
+    value = done * len(w.modes) / el if len(w.modes) > 1 else done / el
+    return {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": f"{done} query passes of {w.name} (queries 0..{len(smp.items) - 1} of "
+                      f"sequence 0..), single-threaded fp64 C oracle, cache quantised by the "
+                      f"oracle before timing", "seconds": el}
+
+
+def run_reference(args, rank, world):
+    from sparse_attention_decode_csa2_gb300.synthetic import WORKLOADS
+    import oracle
+    oracle.build()
+    w = WORKLOADS[args.workload]
+    smp = OracleSample(w, [0])
+    for _ in range(args.warmup):
+        smp.run(smp.items[0])
+    t = []
+    for _ in range(args.steps):
+        t0 = time.perf_counter()
+        smp.run(smp.items[0])
+        t.append(time.perf_counter() - t0)
+    total = sum(t)
+    L = len(w.modes)
+    value = args.steps * L / total if L > 1 else args.steps / total
+    base = {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": f"1 query of {w.name} per step (the full layer path for that query), "
+                      f"single-threaded fp64 C oracle"}
+    return {
+        "metric": METRIC, "value": value, "unit": UNIT, "impl": "reference", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": total * 1e3 / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded SplitMix64)",
+        "config": {"workload": w.name, "queries_per_step": 1, "entries_per_seq": w.N,
+                   "top_k": w.k, "heads": w.H},
+        "cpu_baseline": base,
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    args = parse_args()
+    if args.impl == "reference":
+        rank = int(os.environ.get("RANK", "0"))
+        world = int(os.environ.get("WORLD_SIZE", "1"))
+        if rank != 0:
+            return 0
+        print(json.dumps(run_reference(args, rank, world)), flush=True)
+        return 0
+    rank, world, local = dist_setup(args)
+    res = run_gpu(args, rank, world, local)
+    if res is None:
+        return 0
+    if rank == 0:
+        if world == 1 and not args.no_cpu_baseline:
+            from sparse_attention_decode_csa2_gb300.synthetic import WORKLOADS
+            res["cpu_baseline"] = cpu_baseline(WORKLOADS[args.workload])
+        print(json.dumps(res), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,226 @@
+/*
+ * csa2.h -- C ABI of libcsa2.so, the GB300 (sm_103a) implementation of the
+ * CSA2 compressed-sparse-attention hot path of DeepSeek-V4.1-Flash.
+ *
+ * The operations follow the method as described on these pages:
+ *  - modelscope.csdn.net DeepSeek-V4.1-Flash release summary, section "CSA2"
+ *    (three static layer modes sharing main KV and indexer K; FP4 E2M1 main
+ *    KV with one E4M3 scale per 16 channels);
+ *  - wkq9411.github.io DeepSeek-V4.1-Flash paper walkthrough, sections
+ *    1.(4) "CSA2" (indexer scores entries, per-query top-k, each query attends
+ *    its selected entries), 1.(4).1 "Cross-Layer KV and Index Reuse",
+ *    1.(4).2 "Hierarchical Sparse Indexer", 1.(5).4 "FP4 Main KV Cache",
+ *    2.(2).1 "Model settings" (64 query heads x 512).
+ *
+ * Conventions for every call:
+ *  - All tensor pointers are DEVICE pointers, allocated and owned by the
+ *    caller; the library never allocates device memory and keeps no state.
+ *  - Layouts are dense row-major, innermost dimension last.
+ *  - Every call is asynchronous on `stream` and never synchronises, except
+ *    csa2_read_status.  Arguments are validated on the host before any
+ *    launch; an invalid call returns an error and launches nothing.
+ *  - Sequences: query q reads sequence s = q / q_per_seq, whose entries start
+ *    at entry offset s * kv_seq_stride of the KV and indexer-K arrays
+ *    (kv_seq_stride = 0: every query shares one context).
+ *  - Causal visibility: with q_pos non-NULL, entry j is visible to query q
+ *    iff ratio * j + ratio - 1 <= q_pos[q] (the entry's last token is not in
+ *    the query's future); q_pos NULL makes every entry visible.
+ *  - Scratch memory is passed as (ws, ws_bytes).  Its first 256 bytes hold a
+ *    device status word that kernels set when they meet a bad index or give
+ *    up a bounded wait; csa2_workspace_init clears it and csa2_read_status
+ *    reads and clears it.  Calls that overlap on the GPU must not share a
+ *    workspace.
+ *  - Supported shapes on the GPU path: D = 512, D_I in {32, 64, 128},
+ *    H in {16, 32, 48, 64}, 1 <= H_I <= 32, 1 <= k <= 16384,
+ *    N < 2^31.  Other shapes return CSA2_ERR_UNSUPPORTED.
+ */
+#ifndef CSA2_H_
+#define CSA2_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum csa2_status {
+  CSA2_OK = 0,
+  CSA2_ERR_INVALID_ARG = 1,   /* null pointer, bad size, bad schedule */
+  CSA2_ERR_UNSUPPORTED = 2,   /* shape outside what the kernels are built for */
+  CSA2_ERR_WORKSPACE = 3,     /* ws NULL or ws_bytes too small */
+  CSA2_ERR_CUDA = 4,          /* a CUDA runtime call or launch failed */
+  CSA2_ERR_BAD_INDEX = 5,     /* (device status) an index was outside [-1, N) */
+  CSA2_ERR_TIMEOUT = 6        /* (device status) a bounded device wait gave up */
+} csa2_status;
+
+typedef enum csa2_mode {
+  CSA2_FULL = 0,     /* own indexer q; scores every visible entry; new top-k */
+  CSA2_REINDEX = 1,  /* own indexer q; re-scores the shared indexer K (or the pool) */
+  CSA2_REUSE = 2     /* no indexer; reuses the latest FULL/REINDEX indices */
+} csa2_mode;
+
+/* Bytes of one FP4 main-KV row of d channels: d/2 code bytes then d/16 scale bytes. */
+#define CSA2_FP4_ROW_BYTES(d) ((d) / 2 + (d) / 16)
+
+/* Human-readable name of a status code (static string). */
+const char* csa2_status_string(csa2_status s);
+
+/* Library version: major * 10000 + minor * 100 + patch. */
+int csa2_version(void);
+
+/*
+ * csa2_quantize_kv_fp4 -- writes FP4 main-KV rows (walkthrough 1.(5).4
+ * "FP4 Main KV Cache": E2M1 codes, one E4M3 scale per 16 channels, no global
+ * scale; release summary "CSA2").
+ *   x      fp32 [n_rows][d], finite values
+ *   out    uint8 [n_rows][d/2 + d/16]; byte j of a row holds channel 2j in its
+ *          low nibble and channel 2j+1 in its high nibble; then one E4M3 byte
+ *          per 16-channel block b (channels 16b..16b+15)
+ *   Per block: scale = E4M3(absmax / 6) rounded to nearest even, saturating
+ *   at 448; each code = the E2M1 value nearest to the exact |x| / scale (ties
+ *   to the even code), sign bit = sign bit of x; a zero scale gives zero
+ *   magnitudes.  Bit-exact.  d must be 512; x and out 16-byte aligned.
+ */
+csa2_status csa2_quantize_kv_fp4(const float* x, int64_t n_rows, int d, uint8_t* out,
+                                 cudaStream_t stream);
+
+/*
+ * csa2_index_scores -- the lightweight indexer (walkthrough 1.(4) "CSA2":
+ * indexer Q and indexer K score main-KV entries).
+ *   q_fp8    E4M3 [B][H_I][D_I] indexer queries
+ *   k_fp8    E4M3 [S][N][D_I] indexer keys, one per entry, shared by all
+ *            indexer heads (sequence s at entry offset s * kv_seq_stride)
+ *   scores   fp32 [B][N]: scores[q][j] = sum_h sum_d q[q][h][d] * k[s][j][d]
+ *            for visible j, -inf for invisible j
+ *   For E4M3 inputs the head sum is formed first (exact in fp32 for
+ *   H_I <= 32); the dot product then accumulates in fp32, which is exact
+ *   whenever every partial sum is an fp32-representable value (e.g. integer
+ *   inputs).  k_fp8 must be 16-byte aligned.
+ */
+csa2_status csa2_index_scores(const uint8_t* q_fp8, const uint8_t* k_fp8, int B, int H_I, int D_I,
+                              int64_t N, int64_t kv_seq_stride, int q_per_seq,
+                              const int32_t* q_pos, int ratio, float* scores,
+                              cudaStream_t stream);
+
+/*
+ * csa2_topk -- per-query top-k selection (walkthrough 1.(4) "CSA2": the top-k
+ * entries per query).
+ *   scores   fp32 [B][N] (NaN not allowed; -0 and +0 compare equal)
+ *   idx      int32 [B][k]: the min(k, visible) visible entries with the
+ *            largest scores, ties broken towards the lower index, written in
+ *            ascending index order and padded with -1.  Bit-exact.
+ *   ws       at least csa2_workspace_size(B, N, k, 0, 0) bytes.
+ */
+csa2_status csa2_topk(const float* scores, int B, int64_t N, int k, const int32_t* q_pos,
+                      int ratio, int32_t* idx, void* ws, size_t ws_bytes, cudaStream_t stream);
+
+/*
+ * csa2_hier_pool_index -- a Reindex layer of the Hierarchical Sparse Indexer
+ * (walkthrough 1.(4).2): scores only the candidate-pool entries with this
+ * layer's indexer q and keeps its own top-k inside the pool.
+ *   pool     int32 [B][P] entry ids, strictly ascending, -1 padding only at
+ *            the end (the layout csa2_topk writes); a violation sets the
+ *            CSA2_ERR_BAD_INDEX status and the row's result is unspecified
+ *   idx      int32 [B][k] selected entry ids, ascending, -1 padded; ranking
+ *            by (score desc, entry id asc).  Bit-exact given exact scores.
+ *   ws       at least csa2_workspace_size(B, N, k, 0, P) bytes.
+ */
+csa2_status csa2_hier_pool_index(const uint8_t* q_fp8, const uint8_t* k_fp8, int B, int H_I,
+                                 int D_I, int64_t N, int64_t kv_seq_stride, int q_per_seq,
+                                 const int32_t* pool, int P, int k, int32_t* idx, void* ws,
+                                 size_t ws_bytes, cudaStream_t stream);
+
+/*
+ * csa2_sparse_attn_fp4 -- gathers the selected FP4 entries, dequantises them
+ * and runs MQA softmax attention over them (walkthrough 1.(4) "CSA2";
+ * 1.(5).4: the cache is dequantised before attention; 2.(2).1: 64 heads x
+ * 512).  K = V = the dequantised latent, shared by all heads.
+ *   q_bf16   bf16 [B][H][D] main queries (16-byte aligned)
+ *   kv_fp4   uint8 [S][N][D/2 + D/16] FP4 rows (16-byte aligned)
+ *   idx      int32 [B][k] entry ids; -1 slots are skipped; ids outside
+ *            [-1, N) are skipped and set CSA2_ERR_BAD_INDEX in the status
+ *   out      fp32 [B][H][D]: softmax(softmax_scale * q . v_j) weighted sum of v_j
+ *   lse      fp32 [B][H] log-sum-exp of the scaled logits, or NULL
+ *   A row with no valid slot yields out = 0 and lse = -inf.
+ *   ws       at least csa2_workspace_size(B, 0, k, H, 0) bytes.
+ */
+csa2_status csa2_sparse_attn_fp4(const uint16_t* q_bf16, const uint8_t* kv_fp4, int B, int H,
+                                 int D, int64_t N, int64_t kv_seq_stride, int q_per_seq,
+                                 const int32_t* idx, int k, float softmax_scale, float* out,
+                                 float* lse, void* ws, size_t ws_bytes, cudaStream_t stream);
+
+/* One layer of a CSA2 layer group. */
+typedef struct csa2_layer {
+  int mode;                /* csa2_mode */
+  const uint16_t* q_bf16;  /* bf16 [B][H][D] this layer's main query */
+  const uint8_t* qi_fp8;   /* E4M3 [B][H_I][D_I] indexer query; NULL for REUSE */
+  float* out;              /* fp32 [B][H][D] */
+  float* lse;              /* fp32 [B][H] or NULL */
+  int32_t* idx_out;        /* int32 [B][k]: indices this layer attended.  Required for
+                              FULL and REINDEX; for REUSE, NULL or a buffer that
+                              receives a copy of the reused indices */
+} csa2_layer;
+
+/* What the layers of one group share (walkthrough 1.(4).1). */
+typedef struct csa2_group_args {
+  const uint8_t* kv_fp4;   /* [S][N][D/2 + D/16] shared FP4 main KV */
+  const uint8_t* ki_fp8;   /* [S][N][D_I] shared indexer K */
+  int B, H, H_I, D, D_I;
+  int64_t N, kv_seq_stride;
+  int q_per_seq;
+  const int32_t* q_pos;    /* [B] or NULL */
+  int ratio;
+  int k;
+  int pool_size;           /* 0: flat indexer; P > 0: FULL layers build a top-P pool and
+                              REINDEX layers select inside it (walkthrough 1.(4).2) */
+  int32_t* pool_out;       /* int32 [B][pool_size] when pool_size > 0 */
+  float softmax_scale;
+} csa2_group_args;
+
+/*
+ * csa2_layer_group -- runs a static schedule of CSA2 layers over one shared
+ * FP4 main KV and indexer K (walkthrough 1.(4).1, 1.(4).2):
+ *   FULL    scores all visible entries with its own indexer q, takes top-k
+ *           (and the top-pool_size pool when pool_size > 0), attends;
+ *   REINDEX re-scores the shared indexer K (only the pool when pool_size > 0)
+ *           with its own indexer q, takes top-k, attends;
+ *   REUSE   attends with the indices of the nearest preceding FULL/REINDEX.
+ * Every layer attends with its own main query.  layers[0] must be FULL.
+ *   ws   at least csa2_workspace_size(B, N, k, H, pool_size) bytes.
+ */
+csa2_status csa2_layer_group(const csa2_layer* layers, int n_layers, const csa2_group_args* g,
+                             void* ws, size_t ws_bytes, cudaStream_t stream);
+
+/*
+ * Number of kernel launches csa2_layer_group enqueues for these arguments
+ * (-1 if they are invalid).  Host-only; useful to size CUDA-graph captures
+ * and to account for launches.
+ */
+int csa2_layer_group_launches(const csa2_layer* layers, int n_layers, const csa2_group_args* g);
+
+/*
+ * Scratch bytes for csa2_layer_group with these dimensions (pass 0 for
+ * dimensions a call does not use).  The same number is enough for every
+ * individual call made with the same or smaller dimensions.  Depends on the
+ * current device's SM count.
+ */
+size_t csa2_workspace_size(int B, int64_t N, int k, int H, int P);
+
+/* Clears the workspace's device status word (asynchronous, on `stream`). */
+csa2_status csa2_workspace_init(void* ws, size_t ws_bytes, cudaStream_t stream);
+
+/*
+ * Synchronises `stream`, reads and clears the device status word.  Writes
+ * the raw bits to *device_bits (if non-NULL): bit 0 bad index, bit 1 bounded
+ * wait timed out.  Returns CSA2_OK, CSA2_ERR_BAD_INDEX or CSA2_ERR_TIMEOUT.
+ */
+csa2_status csa2_read_status(void* ws, cudaStream_t stream, int32_t* device_bits);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* CSA2_H_ */

@@ -1,0 +1,299 @@
+"""Thin Python binding of libcsa2.so (declared in include/csa2.h).
+
+Argument marshalling only: every function checks tensor devices, dtypes and
+shapes, passes raw device pointers and the current CUDA stream to the C ABI,
+and raises ``Csa2Error`` on a non-OK status.  There is no CPU path: importing
+this module loads the shared library and raises if it has not been built
+(``python -m sparse_attention_decode_csa2_gb300.build``), and every call
+requires CUDA tensors.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+from typing import Optional, Sequence
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libcsa2.so")
+
+FULL, REINDEX, REUSE = 0, 1, 2
+D_LATENT = 512
+ROW_BYTES = D_LATENT // 2 + D_LATENT // 16
+
+STATUS_NAMES = {0: "CSA2_OK", 1: "CSA2_ERR_INVALID_ARG", 2: "CSA2_ERR_UNSUPPORTED",
+                3: "CSA2_ERR_WORKSPACE", 4: "CSA2_ERR_CUDA", 5: "CSA2_ERR_BAD_INDEX",
+                6: "CSA2_ERR_TIMEOUT"}
+
+
+class Csa2Error(RuntimeError):
+    def __init__(self, code: int, where: str):
+        super().__init__(f"{where}: {STATUS_NAMES.get(code, code)}")
+        self.code = code
+
+
+if not os.path.exists(LIB_PATH):
+    raise ImportError(f"{LIB_PATH} is missing: build it with "
+                      "`python -m sparse_attention_decode_csa2_gb300.build` (needs nvcc)")
+
+lib = ctypes.CDLL(LIB_PATH)
+
+_vp, _i32, _i64, _sz, _f32 = (ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_size_t,
+                              ctypes.c_float)
+
+
+class Csa2Layer(ctypes.Structure):
+    _fields_ = [("mode", ctypes.c_int), ("q_bf16", _vp), ("qi_fp8", _vp), ("out", _vp),
+                ("lse", _vp), ("idx_out", _vp)]
+
+
+class Csa2GroupArgs(ctypes.Structure):
+    _fields_ = [("kv_fp4", _vp), ("ki_fp8", _vp), ("B", ctypes.c_int), ("H", ctypes.c_int),
+                ("H_I", ctypes.c_int), ("D", ctypes.c_int), ("D_I", ctypes.c_int),
+                ("N", ctypes.c_int64), ("kv_seq_stride", ctypes.c_int64),
+                ("q_per_seq", ctypes.c_int), ("q_pos", _vp), ("ratio", ctypes.c_int),
+                ("k", ctypes.c_int), ("pool_size", ctypes.c_int), ("pool_out", _vp),
+                ("softmax_scale", ctypes.c_float)]
+
+
+_SIGS = {
+    "csa2_status_string": (ctypes.c_char_p, [_i32]),
+    "csa2_version": (_i32, []),
+    "csa2_quantize_kv_fp4": (_i32, [_vp, _i64, _i32, _vp, _vp]),
+    "csa2_index_scores": (_i32, [_vp, _vp, _i32, _i32, _i32, _i64, _i64, _i32, _vp, _i32, _vp,
+                                 _vp]),
+    "csa2_topk": (_i32, [_vp, _i32, _i64, _i32, _vp, _i32, _vp, _vp, _sz, _vp]),
+    "csa2_hier_pool_index": (_i32, [_vp, _vp, _i32, _i32, _i32, _i64, _i64, _i32, _vp, _i32,
+                                    _i32, _vp, _vp, _sz, _vp]),
+    "csa2_sparse_attn_fp4": (_i32, [_vp, _vp, _i32, _i32, _i32, _i64, _i64, _i32, _vp, _i32,
+                                    _f32, _vp, _vp, _vp, _sz, _vp]),
+    "csa2_layer_group": (_i32, [ctypes.POINTER(Csa2Layer), _i32, ctypes.POINTER(Csa2GroupArgs),
+                                _vp, _sz, _vp]),
+    "csa2_layer_group_launches": (_i32, [ctypes.POINTER(Csa2Layer), _i32,
+                                         ctypes.POINTER(Csa2GroupArgs)]),
+    "csa2_workspace_size": (_sz, [_i32, _i64, _i32, _i32, _i32]),
+    "csa2_workspace_init": (_i32, [_vp, _sz, _vp]),
+    "csa2_read_status": (_i32, [_vp, _vp, ctypes.POINTER(ctypes.c_int32)]),
+}
+for _name, (_res, _args) in _SIGS.items():
+    _f = getattr(lib, _name)
+    _f.restype = _res
+    _f.argtypes = _args
+
+EXPORTED = tuple(_SIGS)
+
+
+def _check(code: int, where: str) -> None:
+    if code != 0:
+        raise Csa2Error(code, where)
+
+
+def _stream() -> int:
+    return torch.cuda.current_stream().cuda_stream
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return None if t is None else t.data_ptr()
+
+
+def _dev(t: torch.Tensor, dtype, name: str) -> torch.Tensor:
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor (there is no CPU path)")
+    if t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    return t
+
+
+def _bits16(t: torch.Tensor, name: str) -> torch.Tensor:
+    """bf16 tensor (or its int16/uint16 bit view) -> same storage as int16."""
+    if t.dtype == torch.bfloat16:
+        t = t.view(torch.int16)
+    elif t.dtype == torch.uint16:
+        t = t.view(torch.int16)
+    return _dev(t, torch.int16, name)
+
+
+def _opt_pos(q_pos: Optional[torch.Tensor]) -> Optional[torch.Tensor]:
+    return None if q_pos is None else _dev(q_pos, torch.int32, "q_pos")
+
+
+# ---------------------------------------------------------------------------
+# workspace
+# ---------------------------------------------------------------------------
+
+def workspace_size(B: int, N: int = 0, k: int = 0, H: int = 0, P: int = 0) -> int:
+    return int(lib.csa2_workspace_size(B, N, k, H, P))
+
+
+def make_workspace(B: int, N: int = 0, k: int = 0, H: int = 0, P: int = 0,
+                   device=None) -> torch.Tensor:
+    n = workspace_size(B, N, k, H, P)
+    ws = torch.empty(n, dtype=torch.uint8, device=device or "cuda")
+    _check(lib.csa2_workspace_init(ws.data_ptr(), n, _stream()), "csa2_workspace_init")
+    return ws
+
+
+def read_status(ws: torch.Tensor):
+    """Synchronises the current stream; returns (status_code, raw_bits) and clears the word."""
+    bits = ctypes.c_int32(0)
+    code = lib.csa2_read_status(ws.data_ptr(), _stream(), ctypes.byref(bits))
+    return int(code), int(bits.value)
+
+
+# ---------------------------------------------------------------------------
+# operations (same names as the C ABI without the csa2_ prefix)
+# ---------------------------------------------------------------------------
+
+def quantize_kv_fp4(x: torch.Tensor, out: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """fp32 [n][512] -> uint8 [n][288] FP4 rows."""
+    x = _dev(x, torch.float32, "x")
+    n, d = x.reshape(-1, x.shape[-1]).shape
+    if out is None:
+        out = torch.empty((n, d // 2 + d // 16), dtype=torch.uint8, device=x.device)
+    _dev(out, torch.uint8, "out")
+    _check(lib.csa2_quantize_kv_fp4(_ptr(x), n, d, _ptr(out), _stream()), "csa2_quantize_kv_fp4")
+    return out
+
+
+def index_scores(q_fp8: torch.Tensor, k_fp8: torch.Tensor, N: int, kv_seq_stride: int,
+                 q_per_seq: int, q_pos: Optional[torch.Tensor], ratio: int,
+                 out: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """E4M3 q [B][H_I][D_I], E4M3 K [S*stride][D_I] -> fp32 scores [B][N]."""
+    q_fp8 = _dev(q_fp8, torch.uint8, "q_fp8")
+    k_fp8 = _dev(k_fp8, torch.uint8, "k_fp8")
+    B, H_I, D_I = q_fp8.shape
+    if out is None:
+        out = torch.empty((B, N), dtype=torch.float32, device=q_fp8.device)
+    _dev(out, torch.float32, "scores")
+    qp = _opt_pos(q_pos)
+    _check(lib.csa2_index_scores(_ptr(q_fp8), _ptr(k_fp8), B, H_I, D_I, N, kv_seq_stride,
+                                 q_per_seq, _ptr(qp), ratio, _ptr(out), _stream()),
+           "csa2_index_scores")
+    return out
+
+
+def topk(scores: torch.Tensor, k: int, q_pos: Optional[torch.Tensor] = None, ratio: int = 1,
+         ws: Optional[torch.Tensor] = None, out: Optional[torch.Tensor] = None) -> torch.Tensor:
+    scores = _dev(scores, torch.float32, "scores")
+    B, N = scores.shape
+    if ws is None:
+        ws = make_workspace(B, N, k, 0, 0, scores.device)
+    if out is None:
+        out = torch.empty((B, k), dtype=torch.int32, device=scores.device)
+    _dev(out, torch.int32, "idx")
+    qp = _opt_pos(q_pos)
+    _check(lib.csa2_topk(_ptr(scores), B, N, k, _ptr(qp), ratio, _ptr(out), _ptr(ws),
+                         ws.numel(), _stream()), "csa2_topk")
+    return out
+
+
+def hier_pool_index(q_fp8: torch.Tensor, k_fp8: torch.Tensor, N: int, kv_seq_stride: int,
+                    q_per_seq: int, pool: torch.Tensor, k: int, ws: Optional[torch.Tensor] = None,
+                    out: Optional[torch.Tensor] = None) -> torch.Tensor:
+    q_fp8 = _dev(q_fp8, torch.uint8, "q_fp8")
+    k_fp8 = _dev(k_fp8, torch.uint8, "k_fp8")
+    pool = _dev(pool, torch.int32, "pool")
+    B, H_I, D_I = q_fp8.shape
+    P = pool.shape[1]
+    if ws is None:
+        ws = make_workspace(B, 0, k, 0, P, q_fp8.device)
+    if out is None:
+        out = torch.empty((B, k), dtype=torch.int32, device=q_fp8.device)
+    _dev(out, torch.int32, "idx")
+    _check(lib.csa2_hier_pool_index(_ptr(q_fp8), _ptr(k_fp8), B, H_I, D_I, N, kv_seq_stride,
+                                    q_per_seq, _ptr(pool), P, k, _ptr(out), _ptr(ws), ws.numel(),
+                                    _stream()), "csa2_hier_pool_index")
+    return out
+
+
+def sparse_attn_fp4(q_bf16: torch.Tensor, kv_fp4: torch.Tensor, N: int, kv_seq_stride: int,
+                    q_per_seq: int, idx: torch.Tensor, softmax_scale: Optional[float] = None,
+                    out: Optional[torch.Tensor] = None, lse: Optional[torch.Tensor] = None,
+                    ws: Optional[torch.Tensor] = None, want_lse: bool = True):
+    """bf16 q [B][H][512], FP4 rows [S*stride][288], idx [B][k] -> (out fp32 [B][H][512], lse)."""
+    q = _bits16(q_bf16, "q_bf16")
+    kv_fp4 = _dev(kv_fp4, torch.uint8, "kv_fp4")
+    idx = _dev(idx, torch.int32, "idx")
+    B, H, D = q.shape
+    k = idx.shape[1]
+    if softmax_scale is None:
+        softmax_scale = 1.0 / math.sqrt(D)
+    if ws is None:
+        ws = make_workspace(B, 0, k, H, 0, q.device)
+    if out is None:
+        out = torch.empty((B, H, D), dtype=torch.float32, device=q.device)
+    if lse is None and want_lse:
+        lse = torch.empty((B, H), dtype=torch.float32, device=q.device)
+    _dev(out, torch.float32, "out")
+    _check(lib.csa2_sparse_attn_fp4(_ptr(q), _ptr(kv_fp4), B, H, D, N, kv_seq_stride, q_per_seq,
+                                    _ptr(idx), k, softmax_scale, _ptr(out), _ptr(lse), _ptr(ws),
+                                    ws.numel(), _stream()), "csa2_sparse_attn_fp4")
+    return out, lse
+
+
+class LayerGroup:
+    """Prepared arguments of csa2_layer_group: tensors are kept alive and the
+    ctypes structs are built once, so repeated calls (and CUDA-graph capture)
+    only cross the C ABI."""
+
+    def __init__(self, modes: Sequence[int], q_bf16: Sequence[torch.Tensor],
+                 qi_fp8: Sequence[Optional[torch.Tensor]], kv_fp4: torch.Tensor,
+                 ki_fp8: torch.Tensor, N: int, kv_seq_stride: int, q_per_seq: int,
+                 q_pos: Optional[torch.Tensor], ratio: int, k: int, pool_size: int = 0,
+                 softmax_scale: Optional[float] = None, want_lse: bool = True,
+                 reuse_idx_copy: bool = True):
+        L = len(modes)
+        self.modes = list(modes)
+        self.q = [_bits16(q, f"q_bf16[{l}]") for l, q in enumerate(q_bf16)]
+        self.qi = [None if qi is None else _dev(qi, torch.uint8, f"qi_fp8[{l}]")
+                   for l, qi in enumerate(qi_fp8)]
+        self.kv = _dev(kv_fp4, torch.uint8, "kv_fp4")
+        self.ki = _dev(ki_fp8, torch.uint8, "ki_fp8")
+        self.q_pos = _opt_pos(q_pos)
+        dev = self.kv.device
+        B, H, D = self.q[0].shape
+        H_I = D_I = 0
+        for qi in self.qi:
+            if qi is not None:
+                _, H_I, D_I = qi.shape
+        if softmax_scale is None:
+            softmax_scale = 1.0 / math.sqrt(D)
+        self.B, self.H, self.D, self.k, self.N = B, H, D, k, N
+        self.out = [torch.empty((B, H, D), dtype=torch.float32, device=dev) for _ in range(L)]
+        self.lse = [torch.empty((B, H), dtype=torch.float32, device=dev) if want_lse else None
+                    for _ in range(L)]
+        self.idx = [torch.empty((B, k), dtype=torch.int32, device=dev)
+                    if (m != REUSE or reuse_idx_copy) else None for m in self.modes]
+        self.pool = (torch.empty((B, pool_size), dtype=torch.int32, device=dev)
+                     if pool_size > 0 else None)
+        self.ws = make_workspace(B, N, k, H, pool_size, dev)
+        self._layers = (Csa2Layer * L)()
+        for l in range(L):
+            self._layers[l] = Csa2Layer(self.modes[l], _ptr(self.q[l]), _ptr(self.qi[l]),
+                                        _ptr(self.out[l]), _ptr(self.lse[l]), _ptr(self.idx[l]))
+        self._args = Csa2GroupArgs(_ptr(self.kv), _ptr(self.ki), B, H, H_I, D, D_I, N,
+                                   kv_seq_stride, q_per_seq, _ptr(self.q_pos), ratio, k,
+                                   pool_size, _ptr(self.pool), softmax_scale)
+
+    def __call__(self):
+        _check(lib.csa2_layer_group(self._layers, len(self.modes), ctypes.byref(self._args),
+                                    _ptr(self.ws), self.ws.numel(), _stream()),
+               "csa2_layer_group")
+        return self.out, self.lse, self.idx, self.pool
+
+
+def group_launches(group: LayerGroup) -> int:
+    """Kernel launches one call of `group` enqueues."""
+    return int(lib.csa2_layer_group_launches(group._layers, len(group.modes),
+                                             ctypes.byref(group._args)))
+
+
+def layer_group(modes, q_bf16, qi_fp8, kv_fp4, ki_fp8, N, kv_seq_stride, q_per_seq, q_pos, ratio,
+                k, pool_size=0, softmax_scale=None):
+    """One-shot csa2_layer_group; returns (outs, lses, idxs, pool)."""
+    return LayerGroup(modes, q_bf16, qi_fp8, kv_fp4, ki_fp8, N, kv_seq_stride, q_per_seq, q_pos,
+                      ratio, k, pool_size, softmax_scale)()

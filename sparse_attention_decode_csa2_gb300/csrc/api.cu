@@ -1,0 +1,269 @@
+// C ABI of libcsa2.so: argument validation, workspace layout and the
+// Full / Reindex / Reuse layer schedule (DeepSeek-V4.1-Flash paper
+// walkthrough, 1.(4).1 "Cross-Layer KV and Index Reuse" and 1.(4).2
+// "Hierarchical Sparse Indexer").  Every compute step runs in the kernels of
+// the other translation units; this file only checks arguments, carves the
+// caller's workspace and enqueues launches.
+#include <stdio.h>
+
+#include "csa2_internal.cuh"
+
+namespace csa2 {
+
+int device_sm_count() {
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 148;
+  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 148;
+  return sms > 0 ? sms : 148;
+}
+
+namespace {
+
+struct WsLayout {
+  size_t status = 0;       // 256 B
+  size_t scores = 0;       // [B][N] fp32
+  size_t pool_scores = 0;  // [B][P] fp32
+  size_t attn = 0;         // attention partials
+  size_t total = 0;
+};
+
+WsLayout layout(int B, int64_t N, int k, int H, int P) {
+  WsLayout w;
+  size_t off = kStatusBytes;
+  w.scores = off;
+  off += align_up((size_t)(B > 0 ? B : 0) * (size_t)(N > 0 ? N : 0) * 4, 256);
+  w.pool_scores = off;
+  off += align_up((size_t)(B > 0 ? B : 0) * (size_t)(P > 0 ? P : 0) * 4, 256);
+  w.attn = off;
+  off += attn_scratch_bytes(B, H, k);
+  w.total = off;
+  return w;
+}
+
+inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+csa2_status check_launch(cudaError_t e) { return e == cudaSuccess ? CSA2_OK : CSA2_ERR_CUDA; }
+
+csa2_status check_seq(int B, int64_t N, int64_t kv_seq_stride, int q_per_seq) {
+  if (B < 0 || N < 0 || N > INT32_MAX - 1) return CSA2_ERR_INVALID_ARG;
+  if (q_per_seq < 1 || kv_seq_stride < 0) return CSA2_ERR_INVALID_ARG;
+  if (kv_seq_stride > 0 && kv_seq_stride < N) return CSA2_ERR_INVALID_ARG;
+  return CSA2_OK;
+}
+
+csa2_status check_indexer(const uint8_t* q, const uint8_t* k, int B, int H_I, int D_I, int ratio) {
+  if (B > 0 && (!q || !k)) return CSA2_ERR_INVALID_ARG;
+  if (ratio < 1 || H_I < 1) return CSA2_ERR_INVALID_ARG;
+  if (D_I != 32 && D_I != 64 && D_I != 128) return CSA2_ERR_UNSUPPORTED;
+  if (H_I > 32) return CSA2_ERR_UNSUPPORTED;
+  if (!aligned16(k)) return CSA2_ERR_INVALID_ARG;
+  return CSA2_OK;
+}
+
+csa2_status check_attn(const uint16_t* q, const uint8_t* kv, int B, int H, int D, int k,
+                       float scale, const float* out) {
+  if (B > 0 && (!q || !kv || !out)) return CSA2_ERR_INVALID_ARG;
+  if (D != kD) return CSA2_ERR_UNSUPPORTED;
+  if (H != 16 && H != 32 && H != 64) return CSA2_ERR_UNSUPPORTED;
+  if (k < 1) return CSA2_ERR_INVALID_ARG;
+  if (k > 16384) return CSA2_ERR_UNSUPPORTED;
+  if (!(scale > 0.0f) || !(scale < INFINITY)) return CSA2_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(kv) || ((uintptr_t)out & 15u)) return CSA2_ERR_INVALID_ARG;
+  return CSA2_OK;
+}
+
+int32_t* status_ptr(void* ws) { return reinterpret_cast<int32_t*>(ws); }
+
+}  // namespace
+}  // namespace csa2
+
+using namespace csa2;
+
+extern "C" {
+
+const char* csa2_status_string(csa2_status s) {
+  switch (s) {
+    case CSA2_OK: return "CSA2_OK";
+    case CSA2_ERR_INVALID_ARG: return "CSA2_ERR_INVALID_ARG";
+    case CSA2_ERR_UNSUPPORTED: return "CSA2_ERR_UNSUPPORTED";
+    case CSA2_ERR_WORKSPACE: return "CSA2_ERR_WORKSPACE";
+    case CSA2_ERR_CUDA: return "CSA2_ERR_CUDA";
+    case CSA2_ERR_BAD_INDEX: return "CSA2_ERR_BAD_INDEX";
+    case CSA2_ERR_TIMEOUT: return "CSA2_ERR_TIMEOUT";
+  }
+  return "CSA2_ERR_UNKNOWN";
+}
+
+int csa2_version(void) { return 100; }
+
+size_t csa2_workspace_size(int B, int64_t N, int k, int H, int P) {
+  return layout(B, N, k, H, P).total;
+}
+
+csa2_status csa2_workspace_init(void* ws, size_t ws_bytes, cudaStream_t stream) {
+  if (!ws || ws_bytes < kStatusBytes) return CSA2_ERR_WORKSPACE;
+  return check_launch(cudaMemsetAsync(ws, 0, kStatusBytes, stream));
+}
+
+csa2_status csa2_read_status(void* ws, cudaStream_t stream, int32_t* device_bits) {
+  if (!ws) return CSA2_ERR_WORKSPACE;
+  int32_t bits = 0;
+  if (cudaMemcpyAsync(&bits, ws, 4, cudaMemcpyDeviceToHost, stream) != cudaSuccess)
+    return CSA2_ERR_CUDA;
+  if (cudaMemsetAsync(ws, 0, 4, stream) != cudaSuccess) return CSA2_ERR_CUDA;
+  if (cudaStreamSynchronize(stream) != cudaSuccess) return CSA2_ERR_CUDA;
+  if (device_bits) *device_bits = bits;
+  if (bits & kStatusBadIndex) return CSA2_ERR_BAD_INDEX;
+  if (bits & kStatusTimeout) return CSA2_ERR_TIMEOUT;
+  return CSA2_OK;
+}
+
+csa2_status csa2_quantize_kv_fp4(const float* x, int64_t n_rows, int d, uint8_t* out,
+                                 cudaStream_t stream) {
+  if (n_rows < 0) return CSA2_ERR_INVALID_ARG;
+  if (n_rows > 0 && (!x || !out)) return CSA2_ERR_INVALID_ARG;
+  if (d != kD) return CSA2_ERR_UNSUPPORTED;
+  if (!aligned16(x) || !aligned16(out)) return CSA2_ERR_INVALID_ARG;
+  return check_launch(launch_quantize_kv_fp4(x, n_rows, out, stream));
+}
+
+csa2_status csa2_index_scores(const uint8_t* q_fp8, const uint8_t* k_fp8, int B, int H_I, int D_I,
+                              int64_t N, int64_t kv_seq_stride, int q_per_seq,
+                              const int32_t* q_pos, int ratio, float* scores,
+                              cudaStream_t stream) {
+  csa2_status s = check_seq(B, N, kv_seq_stride, q_per_seq);
+  if (s != CSA2_OK) return s;
+  if ((s = check_indexer(q_fp8, k_fp8, B, H_I, D_I, ratio)) != CSA2_OK) return s;
+  if (B > 0 && N > 0 && !scores) return CSA2_ERR_INVALID_ARG;
+  return check_launch(launch_index_scores(q_fp8, k_fp8, B, H_I, D_I, N, kv_seq_stride, q_per_seq,
+                                          q_pos, ratio, scores, stream));
+}
+
+csa2_status csa2_topk(const float* scores, int B, int64_t N, int k, const int32_t* q_pos,
+                      int ratio, int32_t* idx, void* ws, size_t ws_bytes, cudaStream_t stream) {
+  if (B < 0 || N < 0 || N > INT32_MAX - 1 || k < 1 || ratio < 1) return CSA2_ERR_INVALID_ARG;
+  if (B > 0 && (!idx || (N > 0 && !scores))) return CSA2_ERR_INVALID_ARG;
+  if (!ws || ws_bytes < kStatusBytes) return CSA2_ERR_WORKSPACE;
+  return check_launch(launch_topk(scores, B, N, k, q_pos, ratio, nullptr, nullptr, idx, stream));
+}
+
+csa2_status csa2_hier_pool_index(const uint8_t* q_fp8, const uint8_t* k_fp8, int B, int H_I,
+                                 int D_I, int64_t N, int64_t kv_seq_stride, int q_per_seq,
+                                 const int32_t* pool, int P, int k, int32_t* idx, void* ws,
+                                 size_t ws_bytes, cudaStream_t stream) {
+  csa2_status s = check_seq(B, N, kv_seq_stride, q_per_seq);
+  if (s != CSA2_OK) return s;
+  if ((s = check_indexer(q_fp8, k_fp8, B, H_I, D_I, 1)) != CSA2_OK) return s;
+  if (P < 1 || k < 1) return CSA2_ERR_INVALID_ARG;
+  if (B > 0 && (!pool || !idx)) return CSA2_ERR_INVALID_ARG;
+  WsLayout w = layout(B, 0, 0, 0, P);
+  if (!ws || ws_bytes < w.total) return CSA2_ERR_WORKSPACE;
+  uint8_t* wsb = reinterpret_cast<uint8_t*>(ws);
+  float* pscores = reinterpret_cast<float*>(wsb + w.pool_scores);
+  cudaError_t e = launch_pool_scores(q_fp8, k_fp8, B, H_I, D_I, N, kv_seq_stride, q_per_seq, pool,
+                                     P, pscores, nullptr, status_ptr(ws), stream);
+  if (e != cudaSuccess) return CSA2_ERR_CUDA;
+  return check_launch(launch_topk(pscores, B, P, k, nullptr, 1, nullptr, pool, idx, stream));
+}
+
+csa2_status csa2_sparse_attn_fp4(const uint16_t* q_bf16, const uint8_t* kv_fp4, int B, int H,
+                                 int D, int64_t N, int64_t kv_seq_stride, int q_per_seq,
+                                 const int32_t* idx, int k, float softmax_scale, float* out,
+                                 float* lse, void* ws, size_t ws_bytes, cudaStream_t stream) {
+  csa2_status s = check_seq(B, N, kv_seq_stride, q_per_seq);
+  if (s != CSA2_OK) return s;
+  if ((s = check_attn(q_bf16, kv_fp4, B, H, D, k, softmax_scale, out)) != CSA2_OK) return s;
+  if (B > 0 && !idx) return CSA2_ERR_INVALID_ARG;
+  WsLayout w = layout(B, 0, k, H, 0);
+  if (!ws || ws_bytes < w.total) return CSA2_ERR_WORKSPACE;
+  uint8_t* wsb = reinterpret_cast<uint8_t*>(ws);
+  return check_launch(launch_sparse_attn(q_bf16, kv_fp4, B, H, N, kv_seq_stride, q_per_seq, idx,
+                                         k, softmax_scale, out, lse, wsb + w.attn,
+                                         status_ptr(ws), stream));
+}
+
+int csa2_layer_group_launches(const csa2_layer* layers, int n_layers, const csa2_group_args* g) {
+  if (!layers || !g || n_layers < 1 || layers[0].mode != CSA2_FULL) return -1;
+  if (g->B == 0) return 0;
+  int n = 0;
+  for (int l = 0; l < n_layers; ++l) {
+    const int m = layers[l].mode;
+    if (m == CSA2_FULL) n += 2 + (g->pool_size > 0 ? 1 : 0);
+    else if (m == CSA2_REINDEX) n += 2;
+    else if (m != CSA2_REUSE) return -1;
+    n += attn_launches(g->B, g->k);
+  }
+  return n;
+}
+
+csa2_status csa2_layer_group(const csa2_layer* layers, int n_layers, const csa2_group_args* g,
+                             void* ws, size_t ws_bytes, cudaStream_t stream) {
+  if (!layers || !g || n_layers < 1) return CSA2_ERR_INVALID_ARG;
+  if (layers[0].mode != CSA2_FULL) return CSA2_ERR_INVALID_ARG;
+  csa2_status s = check_seq(g->B, g->N, g->kv_seq_stride, g->q_per_seq);
+  if (s != CSA2_OK) return s;
+  if (g->pool_size < 0) return CSA2_ERR_INVALID_ARG;
+  if (g->pool_size > 0 && g->B > 0 && !g->pool_out) return CSA2_ERR_INVALID_ARG;
+  if (g->pool_size > 0 && g->pool_size < g->k) return CSA2_ERR_INVALID_ARG;
+  // validate every layer before launching anything
+  for (int l = 0; l < n_layers; ++l) {
+    const csa2_layer& L = layers[l];
+    if (L.mode != CSA2_FULL && L.mode != CSA2_REINDEX && L.mode != CSA2_REUSE)
+      return CSA2_ERR_INVALID_ARG;
+    if ((s = check_attn(L.q_bf16, g->kv_fp4, g->B, g->H, g->D, g->k, g->softmax_scale, L.out)) !=
+        CSA2_OK)
+      return s;
+    if (L.mode == CSA2_REUSE) {
+      if (L.qi_fp8) return CSA2_ERR_INVALID_ARG;
+    } else {
+      if ((s = check_indexer(L.qi_fp8, g->ki_fp8, g->B, g->H_I, g->D_I, g->ratio)) != CSA2_OK)
+        return s;
+      if (g->B > 0 && !L.idx_out) return CSA2_ERR_INVALID_ARG;
+    }
+  }
+  WsLayout w = layout(g->B, g->N, g->k, g->H, g->pool_size);
+  if (!ws || ws_bytes < w.total) return CSA2_ERR_WORKSPACE;
+  if (g->B == 0) return CSA2_OK;
+  uint8_t* wsb = reinterpret_cast<uint8_t*>(ws);
+  int32_t* status = status_ptr(ws);
+  float* scores = reinterpret_cast<float*>(wsb + w.scores);
+  float* pscores = reinterpret_cast<float*>(wsb + w.pool_scores);
+  const int32_t* latest = nullptr;
+  cudaError_t e = cudaSuccess;
+  for (int l = 0; l < n_layers && e == cudaSuccess; ++l) {
+    const csa2_layer& L = layers[l];
+    const int32_t* use = nullptr;
+    if (L.mode == CSA2_FULL || (L.mode == CSA2_REINDEX && g->pool_size == 0)) {
+      e = launch_index_scores(L.qi_fp8, g->ki_fp8, g->B, g->H_I, g->D_I, g->N, g->kv_seq_stride,
+                              g->q_per_seq, g->q_pos, g->ratio, scores, stream);
+      if (e == cudaSuccess && L.mode == CSA2_FULL && g->pool_size > 0)
+        e = launch_topk(scores, g->B, g->N, g->pool_size, g->q_pos, g->ratio, nullptr, nullptr,
+                        g->pool_out, stream);
+      if (e == cudaSuccess)
+        e = launch_topk(scores, g->B, g->N, g->k, g->q_pos, g->ratio, nullptr, nullptr, L.idx_out,
+                        stream);
+      use = L.idx_out;
+    } else if (L.mode == CSA2_REINDEX) {
+      e = launch_pool_scores(L.qi_fp8, g->ki_fp8, g->B, g->H_I, g->D_I, g->N, g->kv_seq_stride,
+                             g->q_per_seq, g->pool_out, g->pool_size, pscores, nullptr, status,
+                             stream);
+      if (e == cudaSuccess)
+        e = launch_topk(pscores, g->B, g->pool_size, g->k, nullptr, 1, nullptr, g->pool_out,
+                        L.idx_out, stream);
+      use = L.idx_out;
+    } else {  // REUSE
+      use = latest;
+      if (L.idx_out)
+        e = cudaMemcpyAsync(L.idx_out, latest, (size_t)g->B * g->k * 4, cudaMemcpyDeviceToDevice,
+                            stream);
+    }
+    if (e != cudaSuccess) break;
+    latest = use;
+    e = launch_sparse_attn(L.q_bf16, g->kv_fp4, g->B, g->H, g->N, g->kv_seq_stride, g->q_per_seq,
+                           use, g->k, g->softmax_scale, L.out, L.lse, wsb + w.attn, status,
+                           stream);
+  }
+  return check_launch(e);
+}
+
+}  // extern "C"

@@ -1,0 +1,117 @@
+// Internal declarations shared by the CUDA translation units of libcsa2.so.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_fp16.h>
+#include <stdint.h>
+
+#include "csa2.h"
+
+namespace csa2 {
+
+// Device status bits (first word of the workspace).
+constexpr int32_t kStatusBadIndex = 1;
+constexpr int32_t kStatusTimeout = 2;
+constexpr size_t kStatusBytes = 256;
+
+constexpr int kD = 512;                      // latent channels
+constexpr int kRowBytes = kD / 2 + kD / 16;  // 288 bytes per FP4 row
+constexpr int kCodeBytes = kD / 2;           // 256
+
+__host__ __device__ inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+// ---------------------------------------------------------------------------
+// Device helpers
+// ---------------------------------------------------------------------------
+
+// Two E4M3 bytes (low byte = element 0) -> two fp16 values (exact).
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint16_t v) {
+  uint32_t r;
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(r) : "h"(v));
+  return r;
+}
+
+// One byte holding two E2M1 codes (low nibble = element 0) -> two fp16 values (exact).
+__device__ __forceinline__ uint32_t e2m1x2_to_f16x2(uint32_t byte) {
+  uint32_t r;
+  asm("{\n\t.reg .b8 t;\n\tcvt.u8.u32 t, %1;\n\tcvt.rn.f16x2.e2m1x2 %0, t;\n\t}"
+      : "=r"(r)
+      : "r"(byte));
+  return r;
+}
+
+// fp32 -> E4M3 byte, round to nearest even, saturating to +-448.
+__device__ __forceinline__ uint32_t f32_to_e4m3_satfinite(float x) {
+  uint16_t r;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(0.0f), "f"(x));
+  return r & 0xFFu;  // low byte holds the second source operand
+}
+
+__device__ __forceinline__ float2 half2_bits_to_float2(uint32_t h2) {
+  __half2 h = *reinterpret_cast<__half2*>(&h2);
+  return __half22float2(h);
+}
+
+__device__ __forceinline__ float bf16_bits_to_float(uint16_t b) {
+  return __uint_as_float(static_cast<uint32_t>(b) << 16);
+}
+
+// Order-preserving map of a (non-NaN) float to uint32; -0 maps like +0.
+__device__ __forceinline__ uint32_t float_to_ordered(float f) {
+  uint32_t u = __float_as_uint(f);
+  if (u == 0x80000000u) u = 0u;
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+// Number of entries visible to a query at token position pos:
+// entry j is visible iff ratio*j + ratio - 1 <= pos, i.e. j < (pos+1)/ratio.
+__device__ __forceinline__ int64_t n_visible(const int32_t* q_pos, int q, int ratio, int64_t N) {
+  if (q_pos == nullptr) return N;
+  int64_t pos = q_pos[q];
+  if (pos < 0) return 0;
+  int64_t n = (pos + 1) / ratio;
+  return n < N ? n : N;
+}
+
+__device__ __forceinline__ void set_status(int32_t* status, int32_t bits) {
+  if (status) atomicOr(status, bits);
+}
+
+// ---------------------------------------------------------------------------
+// Launchers (each returns cudaGetLastError() of its launch)
+// ---------------------------------------------------------------------------
+
+cudaError_t launch_quantize_kv_fp4(const float* x, int64_t n_rows, uint8_t* out,
+                                   cudaStream_t stream);
+
+cudaError_t launch_index_scores(const uint8_t* q_fp8, const uint8_t* k_fp8, int B, int H_I,
+                                int D_I, int64_t N, int64_t kv_seq_stride, int q_per_seq,
+                                const int32_t* q_pos, int ratio, float* scores,
+                                cudaStream_t stream);
+
+// Scores pool entries: pool_scores[b][p] for valid pool[b][p], -inf for -1 padding;
+// n_valid[b] = number of valid leading entries.  Flags a pool that is not strictly
+// ascending with -1 only at the tail.
+cudaError_t launch_pool_scores(const uint8_t* q_fp8, const uint8_t* k_fp8, int B, int H_I,
+                               int D_I, int64_t N, int64_t kv_seq_stride, int q_per_seq,
+                               const int32_t* pool, int P, float* pool_scores, int32_t* n_valid,
+                               int32_t* status, cudaStream_t stream);
+
+// Top-k over rows of `scores` [B][N].  The number of candidates of row b is
+// n_visible(q_pos, b, ratio, N) when n_valid is null, else n_valid[b].  When
+// `map` is non-null the selected position p is written as map[b*N + p].
+cudaError_t launch_topk(const float* scores, int B, int64_t N, int k, const int32_t* q_pos,
+                        int ratio, const int32_t* n_valid, const int32_t* map, int32_t* idx,
+                        cudaStream_t stream);
+
+// Sparse attention.  scratch: partial outputs when split over several CTAs.
+size_t attn_scratch_bytes(int B, int H, int k);
+int attn_launches(int B, int k);  // kernels one sparse-attention call launches
+cudaError_t launch_sparse_attn(const uint16_t* q_bf16, const uint8_t* kv_fp4, int B, int H,
+                               int64_t N, int64_t kv_seq_stride, int q_per_seq, const int32_t* idx,
+                               int k, float softmax_scale, float* out, float* lse, void* scratch,
+                               int32_t* status, cudaStream_t stream);
+
+int device_sm_count();
+
+}  // namespace csa2
