@@ -63,7 +63,9 @@ def test_quantize_midpoints_and_neighbours_bit_exact(C):
             m = np.float32(t * s)
             blk += [m, np.nextafter(m, np.float32(0)), np.nextafter(m, np.float32(1e9))]
         blk = np.array(blk[:16], np.float32)
-        blk2 = -np.array([np.float32(6 * s)] + [np.float32(t * s) for t in mids] * 2, np.float32)[:16]
+        blk2 = -np.array([np.float32(6 * s)] + [np.float32(t * s) for t in mids] * 2 + [0.0],
+                         np.float32)
+        assert blk.size == 16 and blk2.size == 16
         row = np.zeros(512, np.float32)
         for p in range(16):
             row[32 * p:32 * p + 16] = blk
