@@ -152,6 +152,37 @@ csa2_status csa2_sparse_attn_fp4(const uint16_t* q_bf16, const uint8_t* kv_fp4, 
                                  const int32_t* idx, int k, float softmax_scale, float* out,
                                  float* lse, void* ws, size_t ws_bytes, cudaStream_t stream);
 
+/*
+ * csa2_sparse_attn_fp4_noalloc -- csa2_sparse_attn_fp4 for callers that cannot
+ * allocate device memory.  The pages have no counterpart: this is a deployment
+ * variant, not part of the method.
+ *   Who needs it: code that enqueues work while its stream is being captured
+ *   into a CUDA graph (an allocation is not a stream operation and breaks the
+ *   capture), plug-ins inside a runtime that owns every device allocation, and
+ *   latency-critical loops that must never call cudaMalloc (it can synchronise
+ *   the device).  Such callers still pass their inputs and outputs, but no
+ *   workspace.
+ *   Arguments, layouts and results are those of csa2_sparse_attn_fp4 (same
+ *   kernels).  The split partials live in a fixed 24 MiB device array inside
+ *   the library, held by every GPU that loads the library until the process
+ *   exits.  A call whose partials would not fit (more than
+ *   csa2_workspace_size(B, 0, k, H, 0) - 256 bytes > 24 MiB) returns
+ *   CSA2_ERR_WORKSPACE and launches nothing.  No cudaMalloc, cudaFree or
+ *   allocating library routine is called.
+ *   The first call on a device looks up the array's device address
+ *   (cudaGetSymbolAddress, once per device, under a lock); make that first
+ *   call before any stream capture.  All calls share the array, which keeps
+ *   the last call's contents (nothing needs to start cleared): calls that
+ *   overlap on the GPU (other streams, other host threads) race on it and must
+ *   be serialised by the caller.  There is no status word: indices outside
+ *   [-1, N) are skipped as in csa2_sparse_attn_fp4 but not reported.
+ */
+csa2_status csa2_sparse_attn_fp4_noalloc(const uint16_t* q_bf16, const uint8_t* kv_fp4, int B,
+                                         int H, int D, int64_t N, int64_t kv_seq_stride,
+                                         int q_per_seq, const int32_t* idx, int k,
+                                         float softmax_scale, float* out, float* lse,
+                                         cudaStream_t stream);
+
 /* One layer of a CSA2 layer group. */
 typedef struct csa2_layer {
   int mode;                /* csa2_mode */

@@ -69,6 +69,8 @@ _SIGS = {
                                     _i32, _vp, _vp, _sz, _vp]),
     "csa2_sparse_attn_fp4": (_i32, [_vp, _vp, _i32, _i32, _i32, _i64, _i64, _i32, _vp, _i32,
                                     _f32, _vp, _vp, _vp, _sz, _vp]),
+    "csa2_sparse_attn_fp4_noalloc": (_i32, [_vp, _vp, _i32, _i32, _i32, _i64, _i64, _i32, _vp,
+                                            _i32, _f32, _vp, _vp, _vp]),
     "csa2_layer_group": (_i32, [ctypes.POINTER(Csa2Layer), _i32, ctypes.POINTER(Csa2GroupArgs),
                                 _vp, _sz, _vp]),
     "csa2_layer_group_launches": (_i32, [ctypes.POINTER(Csa2Layer), _i32,
