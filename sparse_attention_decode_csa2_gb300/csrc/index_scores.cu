@@ -23,15 +23,34 @@ namespace {
 
 constexpr int kThreads = 256;
 
-// qsum[d] = sum_h e4m3(q[h][d]) for one query, computed by the first D_I threads.
+// qsum[d] = sum_h e4m3(q[h][d]) for one query.  The H_I x D_I bytes are
+// fetched with one 16-byte load per thread (a single memory latency), decoded
+// into `qf` and summed over heads from shared memory.  Needs H_I * D_I <= 16 *
+// blockDim.x; ends with a barrier.
 __device__ __forceinline__ void load_qsum(const uint8_t* __restrict__ q, int H_I, int D_I,
-                                          float* __restrict__ qsum) {
+                                          float* __restrict__ qf, float* __restrict__ qsum) {
+  const int nchunks = H_I * D_I / 16;
+  if ((int)threadIdx.x < nchunks) {
+    const uint4 v = __ldg(reinterpret_cast<const uint4*>(q) + threadIdx.x);
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    float* dst = qf + threadIdx.x * 16;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float2 lo = half2_bits_to_float2(e4m3x2_to_f16x2((uint16_t)(w[i] & 0xFFFFu)));
+      const float2 hi = half2_bits_to_float2(e4m3x2_to_f16x2((uint16_t)(w[i] >> 16)));
+      dst[4 * i + 0] = lo.x;
+      dst[4 * i + 1] = lo.y;
+      dst[4 * i + 2] = hi.x;
+      dst[4 * i + 3] = hi.y;
+    }
+  }
+  __syncthreads();
   for (int d = threadIdx.x; d < D_I; d += blockDim.x) {
     float s = 0.0f;
-    for (int h = 0; h < H_I; ++h)
-      s += half2_bits_to_float2(e4m3x2_to_f16x2((uint16_t)q[h * D_I + d])).x;
+    for (int h = 0; h < H_I; ++h) s += qf[h * D_I + d];
     qsum[d] = s;
   }
+  __syncthreads();
 }
 
 // 16 E4M3 bytes (a uint4) dotted with 16 fp32 weights.
@@ -59,31 +78,40 @@ index_scores_decode_kernel(const uint8_t* __restrict__ q_fp8, const uint8_t* __r
   constexpr int TPE = D_I / 16;               // threads per entry
   constexpr int EPI = kThreads / TPE;         // entries per iteration
   constexpr int ITERS = 1024 / EPI;
+  constexpr int U = ITERS < 8 ? ITERS : 8;
+  __shared__ __align__(16) float qf[32 * 128];
   __shared__ float qsum[D_I];
   const int q = blockIdx.y;
-  load_qsum(q_fp8 + (int64_t)q * H_I * D_I, H_I, D_I, qsum);
-  __syncthreads();
   const int sub = threadIdx.x % TPE;
-  float w[16];
-#pragma unroll
-  for (int i = 0; i < 16; ++i) w[i] = qsum[sub * 16 + i];
   const int64_t nv = n_visible(q_pos, q, ratio, N);
   const uint8_t* kseq = k_fp8 + (int64_t)(q / q_per_seq) * kv_seq_stride * D_I;
   float* srow = scores + (int64_t)q * N;
   const int64_t base = (int64_t)blockIdx.x * 1024 + threadIdx.x / TPE;
-  constexpr int U = 4;
+  // first batch of K rows in flight before the q prologue
+  uint4 v[U];
+#pragma unroll
+  for (int u = 0; u < U; ++u) {
+    const int64_t e = base + (int64_t)u * EPI;
+    v[u] = (e < nv) ? __ldg(reinterpret_cast<const uint4*>(kseq + e * D_I) + sub)
+                    : make_uint4(0, 0, 0, 0);
+  }
+  load_qsum(q_fp8 + (int64_t)q * H_I * D_I, H_I, D_I, qf, qsum);
+  float w[16];
+#pragma unroll
+  for (int i = 0; i < 16; ++i) w[i] = qsum[sub * 16 + i];
 #pragma unroll
   for (int it0 = 0; it0 < ITERS; it0 += U) {
-    uint4 v[U];
+    if (it0 > 0) {
 #pragma unroll
-    for (int u = 0; u < U; ++u) {
-      int64_t e = base + (int64_t)(it0 + u) * EPI;
-      v[u] = (e < nv) ? __ldg(reinterpret_cast<const uint4*>(kseq + e * D_I) + sub)
-                      : make_uint4(0, 0, 0, 0);
+      for (int u = 0; u < U; ++u) {
+        const int64_t e = base + (int64_t)(it0 + u) * EPI;
+        v[u] = (e < nv) ? __ldg(reinterpret_cast<const uint4*>(kseq + e * D_I) + sub)
+                        : make_uint4(0, 0, 0, 0);
+      }
     }
 #pragma unroll
     for (int u = 0; u < U; ++u) {
-      int64_t e = base + (int64_t)(it0 + u) * EPI;
+      const int64_t e = base + (int64_t)(it0 + u) * EPI;
       float s = dot16(v[u], w);
 #pragma unroll
       for (int o = TPE / 2; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
@@ -102,15 +130,23 @@ index_scores_tiled_kernel(const uint8_t* __restrict__ q_fp8, const uint8_t* __re
                           float* __restrict__ scores) {
   constexpr int QT = 16;
   __shared__ __align__(16) float qsum[QT][D_I];
+  __shared__ __align__(16) uint8_t qbytes[QT * 32 * 128];
   const int q0 = blockIdx.y * QT;
+  const int nq = min(QT, B - q0);
+  {
+    // all queries' bytes with one 16-byte load per thread per round
+    const int chunks = nq * H_I * D_I / 16;
+    const uint4* src = reinterpret_cast<const uint4*>(q_fp8 + (int64_t)q0 * H_I * D_I);
+    for (int c = threadIdx.x; c < chunks; c += kThreads)
+      reinterpret_cast<uint4*>(qbytes)[c] = __ldg(src + c);
+  }
+  __syncthreads();
   for (int i = threadIdx.x; i < QT * D_I; i += kThreads) {
-    int qq = i / D_I, d = i % D_I;
+    const int qq = i / D_I, d = i % D_I;
     float s = 0.0f;
-    if (q0 + qq < B) {
-      const uint8_t* qp = q_fp8 + (int64_t)(q0 + qq) * H_I * D_I;
+    if (qq < nq)
       for (int h = 0; h < H_I; ++h)
-        s += half2_bits_to_float2(e4m3x2_to_f16x2((uint16_t)qp[h * D_I + d])).x;
-    }
+        s += half2_bits_to_float2(e4m3x2_to_f16x2((uint16_t)qbytes[(qq * H_I + h) * D_I + d])).x;
     qsum[qq][d] = s;
   }
   __syncthreads();
@@ -163,10 +199,10 @@ pool_scores_kernel(const uint8_t* __restrict__ q_fp8, const uint8_t* __restrict_
                    int32_t* status) {
   constexpr int TPE = D_I / 16;
   constexpr int EPI = kThreads / TPE;
+  __shared__ __align__(16) float qf[32 * 128];
   __shared__ float qsum[D_I];
   const int q = blockIdx.y;
-  load_qsum(q_fp8 + (int64_t)q * H_I * D_I, H_I, D_I, qsum);
-  __syncthreads();
+  load_qsum(q_fp8 + (int64_t)q * H_I * D_I, H_I, D_I, qf, qsum);
   const int sub = threadIdx.x % TPE;
   float w[16];
 #pragma unroll

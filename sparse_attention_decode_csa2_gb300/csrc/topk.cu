@@ -3,14 +3,19 @@
 // the lower index; the result is written in ascending index order and padded
 // with -1 when fewer than k entries are candidates.
 //
-// One 1024-thread CTA per row.  Scores map to order-preserving uint32 keys
-// (-0 folded onto +0).  A three-pass MSB radix select (11 + 11 + 10 bits,
-// shared-memory histograms with warp-aggregated atomics) finds the exact k-th
-// largest key T and how many keys equal to T are still needed.  A final
-// in-order sweep over 1024-element rounds (warp ballots for ranks) writes
-// every key > T and the first `need` keys == T, in ascending position.  Rows
-// whose candidates fit in shared memory keep their keys there; longer rows
-// re-read the scores (L2-resident) on every pass.
+// Scores map to order-preserving uint32 keys (-0 folded onto +0).  An MSB
+// radix select finds the exact k-th largest key class and how many of its
+// members are still needed; an ordered sweep then writes every larger key
+// and the first `need` members of the class, in ascending position.
+//
+// Rows of up to 32768 candidates (topk_reg_kernel, one 512-thread CTA per
+// row): each thread holds KPT consecutive keys in registers, so the ordered
+// sweep needs only two block scans.  The radix passes start at the highest
+// bit where the row's min and max keys differ and take 11-bit digits; they
+// stop as soon as the threshold bin is consumed exactly.
+// Longer rows (topk_long_kernel, 1024 threads): keys are re-read from the
+// (L2-resident) scores on every pass, three 11/11/10-bit passes, and the
+// ordered sweep runs in 1024-element rounds with warp ballots.
 #include "csa2_internal.cuh"
 
 namespace csa2 {
@@ -18,7 +23,6 @@ namespace {
 
 constexpr int kThreads = 1024;
 constexpr int kWarps = kThreads / 32;
-constexpr int kSmemKeyCap = 40960;  // 160 KiB of keys
 
 struct TopkShared {
   int32_t hist[2048];
@@ -71,9 +75,209 @@ __device__ __forceinline__ int block_exclusive_scan(int v, int32_t* warp_tot, in
   return r;
 }
 
+constexpr int kRegThreads = 512;
+constexpr int kRegWarps = kRegThreads / 32;
+constexpr int kRegMaxKeys = kRegThreads * 64;
+
+// Exclusive scan of one int per thread over a kRegThreads block.
+__device__ __forceinline__ int reg_block_scan(int v, int32_t* tot, int* total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int x = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    int y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
+  }
+  if (lane == 31) tot[warp] = x;
+  __syncthreads();
+  if (warp == 0) {
+    int t = lane < kRegWarps ? tot[lane] : 0;
+    int s = t;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      int y = __shfl_up_sync(0xffffffffu, s, o);
+      if (lane >= o) s += y;
+    }
+    if (lane < kRegWarps) tot[lane] = s - t;
+    if (lane == kRegWarps - 1) tot[kRegWarps] = s;
+  }
+  __syncthreads();
+  const int r = tot[warp] + x - v;
+  *total = tot[kRegWarps];
+  __syncthreads();
+  return r;
+}
+
+template <int KPT>
+__global__ void __launch_bounds__(kRegThreads, 1)
+topk_reg_kernel(const float* __restrict__ scores, int64_t N, int k,
+                const int32_t* __restrict__ q_pos, int ratio, const int32_t* __restrict__ n_valid,
+                const int32_t* __restrict__ map, int32_t* __restrict__ idx) {
+  __shared__ int32_t hist[2048];
+  __shared__ int32_t tot[kRegWarps + 1];
+  __shared__ uint32_t red_min[kRegWarps], red_max[kRegWarps];
+  __shared__ int32_t s_digit, s_above, s_cnt;
+
+  const int b = blockIdx.x;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const float* row = scores + (int64_t)b * N;
+  const int32_t* mrow = map ? map + (int64_t)b * N : nullptr;
+  int32_t* out = idx + (int64_t)b * k;
+
+  int n;
+  if (map) {
+    int c = 0;
+    for (int64_t j = tid; j < N; j += kRegThreads) c += (mrow[j] >= 0);
+    int t;
+    reg_block_scan(c, tot, &t);
+    n = t;
+  } else if (n_valid) {
+    n = n_valid[b];
+  } else {
+    n = (int)n_visible(q_pos, b, ratio, N);
+  }
+  if (n <= k) {
+    for (int j = tid; j < k; j += kRegThreads) out[j] = (j < n) ? (mrow ? mrow[j] : j) : -1;
+    return;
+  }
+
+  // keys of positions [tid*KPT, tid*KPT + KPT) in registers
+  const int base = tid * KPT;
+  uint32_t key[KPT];
+  const bool vec = ((N & 3) == 0) && ((reinterpret_cast<uintptr_t>(scores) & 15u) == 0);
+#pragma unroll
+  for (int i = 0; i < KPT; i += 4) {
+    const int j = base + i;
+    float v[4];
+    if (vec && j + 3 < n) {
+      const float4 f = *reinterpret_cast<const float4*>(row + j);
+      v[0] = f.x; v[1] = f.y; v[2] = f.z; v[3] = f.w;
+    } else {
+#pragma unroll
+      for (int e = 0; e < 4; ++e) v[e] = (j + e < n) ? row[j + e] : 0.0f;
+    }
+#pragma unroll
+    for (int e = 0; e < 4; ++e) key[i + e] = float_to_ordered(v[e]);
+  }
+
+  // highest bit where the row's keys differ
+  uint32_t kmin = 0xFFFFFFFFu, kmax = 0u;
+#pragma unroll
+  for (int i = 0; i < KPT; ++i) {
+    if (base + i < n) {
+      kmin = min(kmin, key[i]);
+      kmax = max(kmax, key[i]);
+    }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    kmin = min(kmin, __shfl_xor_sync(0xffffffffu, kmin, o));
+    kmax = max(kmax, __shfl_xor_sync(0xffffffffu, kmax, o));
+  }
+  if (lane == 0) {
+    red_min[warp] = kmin;
+    red_max[warp] = kmax;
+  }
+  __syncthreads();
+  kmin = red_min[0];
+  kmax = red_max[0];
+#pragma unroll
+  for (int w = 1; w < kRegWarps; ++w) {
+    kmin = min(kmin, red_min[w]);
+    kmax = max(kmax, red_max[w]);
+  }
+
+  uint32_t prefix, mask;
+  int cur_hi;
+  const uint32_t diff = kmin ^ kmax;
+  if (diff == 0u) {
+    prefix = kmax;
+    mask = 0xFFFFFFFFu;
+    cur_hi = -1;
+  } else {
+    const int hb = 31 - __clz(diff);
+    mask = ~((2u << hb) - 1u);  // hb = 31: 2u << 31 wraps to 0, mask = 0
+    prefix = kmax & mask;
+    cur_hi = hb;
+  }
+  int need = k;
+  bool done = cur_hi < 0;
+  while (!done) {
+    const int nbits = min(11, cur_hi + 1);
+    const int shift = cur_hi + 1 - nbits;
+    const int nbins = 1 << nbits;
+    for (int i = tid; i < nbins; i += kRegThreads) hist[i] = 0;
+    __syncthreads();
+#pragma unroll
+    for (int i = 0; i < KPT; ++i) {
+      if (base + i < n && (key[i] & mask) == prefix)
+        atomicAdd(&hist[(key[i] >> shift) & (uint32_t)(nbins - 1)], 1);
+    }
+    __syncthreads();
+    const int per = (nbins + kRegThreads - 1) / kRegThreads;
+    const int dtop = nbins - 1 - tid * per;
+    int cnt = 0;
+    for (int p = 0; p < per; ++p)
+      if (dtop - p >= 0) cnt += hist[dtop - p];
+    int total;
+    const int before = reg_block_scan(cnt, tot, &total);
+    if (before < need && before + cnt >= need) {
+      int acc = before;
+      for (int p = 0; p < per; ++p) {
+        const int d = dtop - p;
+        if (d < 0) break;
+        const int h = hist[d];
+        if (acc + h >= need) {
+          s_digit = d;
+          s_above = acc;
+          s_cnt = h;
+          break;
+        }
+        acc += h;
+      }
+    }
+    __syncthreads();
+    need -= s_above;
+    prefix |= (uint32_t)s_digit << shift;
+    mask |= (uint32_t)(nbins - 1) << shift;
+    cur_hi = shift - 1;
+    done = (cur_hi < 0) || (s_cnt == need);
+    __syncthreads();
+  }
+
+  // ordered write: keys above the class, then the first `need` class members
+  int gt = 0, eq = 0;
+#pragma unroll
+  for (int i = 0; i < KPT; ++i) {
+    if (base + i < n) {
+      const uint32_t km = key[i] & mask;
+      gt += km > prefix;
+      eq += km == prefix;
+    }
+  }
+  int tot_eq, tot_sel;
+  const int eq_before = reg_block_scan(eq, tot, &tot_eq);
+  const int take_eq = max(0, min(eq, need - eq_before));
+  int off = reg_block_scan(gt + take_eq, tot, &tot_sel);
+  int taken = 0;
+#pragma unroll
+  for (int i = 0; i < KPT; ++i) {
+    if (base + i < n) {
+      const uint32_t km = key[i] & mask;
+      const bool is_eq = km == prefix;
+      const bool t = (km > prefix) || (is_eq && taken < take_eq);
+      taken += (is_eq && t);
+      if (t && off < k) {
+        out[off] = mrow ? mrow[base + i] : base + i;
+        ++off;
+      }
+    }
+  }
+}
+
 template <bool kSmem>
 __global__ void __launch_bounds__(kThreads, 1)
-topk_kernel(const float* __restrict__ scores, int64_t N, int k, const int32_t* __restrict__ q_pos,
+topk_long_kernel(const float* __restrict__ scores, int64_t N, int k, const int32_t* __restrict__ q_pos,
             int ratio, const int32_t* __restrict__ n_valid, const int32_t* __restrict__ map,
             int32_t* __restrict__ idx) {
   extern __shared__ __align__(16) uint8_t smem_raw[];
@@ -217,21 +421,24 @@ cudaError_t launch_topk(const float* scores, int B, int64_t N, int k, const int3
                         int ratio, const int32_t* n_valid, const int32_t* map, int32_t* idx,
                         cudaStream_t stream) {
   if (B == 0) return cudaSuccess;
-  const size_t base = align_up(sizeof(TopkShared), 16);
-  if (N <= kSmemKeyCap) {
-    size_t smem = base + (size_t)N * 4;
-    static bool attr_set = false;
-    if (!attr_set) {
-      cudaFuncSetAttribute(topk_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           (int)(base + (size_t)kSmemKeyCap * 4));
-      attr_set = true;
-    }
-    topk_kernel<true><<<B, kThreads, smem, stream>>>(scores, N, k, q_pos, ratio, n_valid, map,
-                                                     idx);
-  } else {
-    topk_kernel<false><<<B, kThreads, base, stream>>>(scores, N, k, q_pos, ratio, n_valid, map,
-                                                      idx);
+  if (N <= kRegMaxKeys) {
+    if (N <= kRegThreads * 8)
+      topk_reg_kernel<8><<<B, kRegThreads, 0, stream>>>(scores, N, k, q_pos, ratio, n_valid, map,
+                                                        idx);
+    else if (N <= kRegThreads * 16)
+      topk_reg_kernel<16><<<B, kRegThreads, 0, stream>>>(scores, N, k, q_pos, ratio, n_valid, map,
+                                                         idx);
+    else if (N <= kRegThreads * 32)
+      topk_reg_kernel<32><<<B, kRegThreads, 0, stream>>>(scores, N, k, q_pos, ratio, n_valid, map,
+                                                         idx);
+    else
+      topk_reg_kernel<64><<<B, kRegThreads, 0, stream>>>(scores, N, k, q_pos, ratio, n_valid, map,
+                                                         idx);
+    return cudaGetLastError();
   }
+  const size_t base = align_up(sizeof(TopkShared), 16);
+  topk_long_kernel<false><<<B, kThreads, base, stream>>>(scores, N, k, q_pos, ratio, n_valid, map,
+                                                         idx);
   return cudaGetLastError();
 }
 
