@@ -31,7 +31,7 @@
  *    reads and clears it.  Calls that overlap on the GPU must not share a
  *    workspace.
  *  - Supported shapes on the GPU path: D = 512, D_I in {32, 64, 128},
- *    H in {16, 32, 48, 64}, 1 <= H_I <= 32, 1 <= k <= 16384,
+ *    H in {16, 32, 64}, 1 <= H_I <= 32, 1 <= k <= 16384,
  *    N < 2^31.  Other shapes return CSA2_ERR_UNSUPPORTED.
  */
 #ifndef CSA2_H_
@@ -70,6 +70,10 @@ const char* csa2_status_string(csa2_status s);
 
 /* Library version: major * 10000 + minor * 100 + patch. */
 int csa2_version(void);
+
+/* Message of the last CUDA error that made a call of this thread return
+ * CSA2_ERR_CUDA (static string; "no error" if none). */
+const char* csa2_last_cuda_error(void);
 
 /*
  * csa2_quantize_kv_fp4 -- writes FP4 main-KV rows (walkthrough 1.(5).4

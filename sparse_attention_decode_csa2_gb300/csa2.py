@@ -29,8 +29,9 @@ STATUS_NAMES = {0: "CSA2_OK", 1: "CSA2_ERR_INVALID_ARG", 2: "CSA2_ERR_UNSUPPORTE
 
 
 class Csa2Error(RuntimeError):
-    def __init__(self, code: int, where: str):
-        super().__init__(f"{where}: {STATUS_NAMES.get(code, code)}")
+    def __init__(self, code: int, where: str, detail: str = ""):
+        msg = f"{where}: {STATUS_NAMES.get(code, code)}"
+        super().__init__(msg + (f" ({detail})" if detail else ""))
         self.code = code
 
 
@@ -61,6 +62,7 @@ class Csa2GroupArgs(ctypes.Structure):
 _SIGS = {
     "csa2_status_string": (ctypes.c_char_p, [_i32]),
     "csa2_version": (_i32, []),
+    "csa2_last_cuda_error": (ctypes.c_char_p, []),
     "csa2_quantize_kv_fp4": (_i32, [_vp, _i64, _i32, _vp, _vp]),
     "csa2_index_scores": (_i32, [_vp, _vp, _i32, _i32, _i32, _i64, _i64, _i32, _vp, _i32, _vp,
                                  _vp]),
@@ -89,7 +91,8 @@ EXPORTED = tuple(_SIGS)
 
 def _check(code: int, where: str) -> None:
     if code != 0:
-        raise Csa2Error(code, where)
+        detail = lib.csa2_last_cuda_error().decode() if code == 4 else ""
+        raise Csa2Error(code, where, detail)
 
 
 def _stream() -> int:

@@ -42,7 +42,13 @@ WsLayout layout(int B, int64_t N, int k, int H, int P) {
 
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-csa2_status check_launch(cudaError_t e) { return e == cudaSuccess ? CSA2_OK : CSA2_ERR_CUDA; }
+thread_local const char* g_last_cuda_error = "no error";
+
+csa2_status check_launch(cudaError_t e) {
+  if (e == cudaSuccess) return CSA2_OK;
+  g_last_cuda_error = cudaGetErrorString(e);
+  return CSA2_ERR_CUDA;
+}
 
 csa2_status check_seq(int B, int64_t N, int64_t kv_seq_stride, int q_per_seq) {
   if (B < 0 || N < 0 || N > INT32_MAX - 1) return CSA2_ERR_INVALID_ARG;
@@ -96,6 +102,8 @@ const char* csa2_status_string(csa2_status s) {
 
 int csa2_version(void) { return 100; }
 
+const char* csa2_last_cuda_error(void) { return g_last_cuda_error; }
+
 size_t csa2_workspace_size(int B, int64_t N, int k, int H, int P) {
   return layout(B, N, k, H, P).total;
 }
@@ -136,7 +144,7 @@ csa2_status csa2_index_scores(const uint8_t* q_fp8, const uint8_t* k_fp8, int B,
   if ((s = check_indexer(q_fp8, k_fp8, B, H_I, D_I, ratio)) != CSA2_OK) return s;
   if (B > 0 && N > 0 && !scores) return CSA2_ERR_INVALID_ARG;
   return check_launch(launch_index_scores(q_fp8, k_fp8, B, H_I, D_I, N, kv_seq_stride, q_per_seq,
-                                          q_pos, ratio, scores, stream));
+                                          q_pos, ratio, scores, nullptr, stream));
 }
 
 csa2_status csa2_topk(const float* scores, int B, int64_t N, int k, const int32_t* q_pos,
@@ -235,7 +243,7 @@ csa2_status csa2_layer_group(const csa2_layer* layers, int n_layers, const csa2_
     const int32_t* use = nullptr;
     if (L.mode == CSA2_FULL || (L.mode == CSA2_REINDEX && g->pool_size == 0)) {
       e = launch_index_scores(L.qi_fp8, g->ki_fp8, g->B, g->H_I, g->D_I, g->N, g->kv_seq_stride,
-                              g->q_per_seq, g->q_pos, g->ratio, scores, stream);
+                              g->q_per_seq, g->q_pos, g->ratio, scores, status, stream);
       if (e == cudaSuccess && L.mode == CSA2_FULL && g->pool_size > 0)
         e = launch_topk(scores, g->B, g->N, g->pool_size, g->q_pos, g->ratio, nullptr, nullptr,
                         g->pool_out, stream);

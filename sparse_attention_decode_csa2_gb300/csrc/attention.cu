@@ -392,27 +392,25 @@ attn_combine_kernel(const float* __restrict__ part_o, const float* __restrict__ 
   if (lse && threadIdx.x == 0) lse[(int64_t)b * H + h] = (L > 0.f) ? M + logf(L) : -INFINITY;
 }
 
+constexpr int kSplitTile = 128;  // entries per tile of the tensor-core kernel
+
 int choose_splits(int B, int k) {
   const int sms = device_sm_count();
-  int max_split = (k + kTile - 1) / kTile;
+  int max_split = (k + kSplitTile - 1) / kSplitTile;
   int s = sms / (B > 0 ? B : 1);
   if (s < 1) s = 1;
   if (s > max_split) s = max_split;
   // round chunk to whole tiles, then recount
-  int chunk = ((k + s - 1) / s + kTile - 1) / kTile * kTile;
+  int chunk = ((k + s - 1) / s + kSplitTile - 1) / kSplitTile * kSplitTile;
   return (k + chunk - 1) / chunk;
 }
 
-template <int H>
-cudaError_t launch_attn_t(const uint16_t* q_bf16, const uint8_t* kv_fp4, int B, int64_t N,
-                          int64_t kv_seq_stride, int q_per_seq, const int32_t* idx, int k,
-                          float softmax_scale, float* out, float* lse, void* scratch,
-                          int32_t* status, cudaStream_t stream) {
-  using L = AttnSmem<H>;
+cudaError_t launch_attn(const uint16_t* q_bf16, const uint8_t* kv_fp4, int B, int H, int64_t N,
+                        int64_t kv_seq_stride, int q_per_seq, const int32_t* idx, int k,
+                        float softmax_scale, float* out, float* lse, void* scratch,
+                        int32_t* status, cudaStream_t stream) {
   const int nsplit = choose_splits(B, k);
-  const int chunk = ((k + nsplit - 1) / nsplit + kTile - 1) / kTile * kTile;
-  cudaFuncSetAttribute(sparse_attn_kernel<H>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                       (int)L::bytes);
+  const int chunk = ((k + nsplit - 1) / nsplit + kSplitTile - 1) / kSplitTile * kSplitTile;
   float* part_o = nullptr;
   float* part_lse = nullptr;
   if (nsplit > 1) {
@@ -420,11 +418,9 @@ cudaError_t launch_attn_t(const uint16_t* q_bf16, const uint8_t* kv_fp4, int B, 
     part_lse = part_o + (size_t)B * nsplit * H * kD;
   }
   const float scale_log2 = softmax_scale * 1.4426950408889634f;
-  dim3 grid((unsigned)nsplit, (unsigned)B);
-  sparse_attn_kernel<H><<<grid, kThreads, L::bytes, stream>>>(
-      q_bf16, kv_fp4, N, kv_seq_stride, q_per_seq, idx, k, chunk, scale_log2, out, lse, part_o,
-      part_lse, status);
-  cudaError_t e = cudaGetLastError();
+  cudaError_t e = launch_sparse_attn_tc(q_bf16, kv_fp4, B, H, N, kv_seq_stride, q_per_seq, idx, k,
+                                        nsplit, chunk, scale_log2, out, lse, part_o, part_lse,
+                                        status, stream);
   if (e != cudaSuccess || nsplit == 1) return e;
   attn_combine_kernel<<<dim3((unsigned)H, (unsigned)B), 128, 0, stream>>>(part_o, part_lse, H,
                                                                          nsplit, out, lse);
@@ -450,17 +446,8 @@ cudaError_t launch_sparse_attn(const uint16_t* q_bf16, const uint8_t* kv_fp4, in
                                int k, float softmax_scale, float* out, float* lse, void* scratch,
                                int32_t* status, cudaStream_t stream) {
   if (B == 0) return cudaSuccess;
-  switch (H) {
-    case 16:
-      return launch_attn_t<16>(q_bf16, kv_fp4, B, N, kv_seq_stride, q_per_seq, idx, k,
-                               softmax_scale, out, lse, scratch, status, stream);
-    case 32:
-      return launch_attn_t<32>(q_bf16, kv_fp4, B, N, kv_seq_stride, q_per_seq, idx, k,
-                               softmax_scale, out, lse, scratch, status, stream);
-    default:
-      return launch_attn_t<64>(q_bf16, kv_fp4, B, N, kv_seq_stride, q_per_seq, idx, k,
-                               softmax_scale, out, lse, scratch, status, stream);
-  }
+  return launch_attn(q_bf16, kv_fp4, B, H, N, kv_seq_stride, q_per_seq, idx, k, softmax_scale, out,
+                     lse, scratch, status, stream);
 }
 
 }  // namespace csa2

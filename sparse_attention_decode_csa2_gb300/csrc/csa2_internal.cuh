@@ -86,8 +86,15 @@ cudaError_t launch_quantize_kv_fp4(const float* x, int64_t n_rows, uint8_t* out,
 
 cudaError_t launch_index_scores(const uint8_t* q_fp8, const uint8_t* k_fp8, int B, int H_I,
                                 int D_I, int64_t N, int64_t kv_seq_stride, int q_per_seq,
-                                const int32_t* q_pos, int ratio, float* scores,
+                                const int32_t* q_pos, int ratio, float* scores, int32_t* status,
                                 cudaStream_t stream);
+
+// Tensor-core indexer (TMA + tcgen05 kind::f8f6f4); cudaErrorNotSupported for
+// shapes it does not cover.
+cudaError_t launch_index_scores_tc(const uint8_t* q_fp8, const uint8_t* k_fp8, int B, int H_I,
+                                   int D_I, int64_t N, int64_t kv_seq_stride, int q_per_seq,
+                                   const int32_t* q_pos, int ratio, float* scores,
+                                   int32_t* status, cudaStream_t stream);
 
 // Scores pool entries: pool_scores[b][p] for valid pool[b][p], -inf for -1 padding;
 // n_valid[b] = number of valid leading entries.  Flags a pool that is not strictly
@@ -111,6 +118,13 @@ cudaError_t launch_sparse_attn(const uint16_t* q_bf16, const uint8_t* kv_fp4, in
                                int64_t N, int64_t kv_seq_stride, int q_per_seq, const int32_t* idx,
                                int k, float softmax_scale, float* out, float* lse, void* scratch,
                                int32_t* status, cudaStream_t stream);
+
+// tcgen05 kernel of one sparse-attention call (partials when nsplit > 1).
+cudaError_t launch_sparse_attn_tc(const uint16_t* q_bf16, const uint8_t* kv_fp4, int B, int H,
+                                  int64_t N, int64_t kv_seq_stride, int q_per_seq,
+                                  const int32_t* idx, int k, int nsplit, int chunk,
+                                  float scale_log2, float* out, float* lse, float* part_o,
+                                  float* part_lse, int32_t* status, cudaStream_t stream);
 
 int device_sm_count();
 

@@ -254,20 +254,11 @@ cudaError_t launch_scores_t(const uint8_t* q_fp8, const uint8_t* k_fp8, int B, i
 
 cudaError_t launch_index_scores(const uint8_t* q_fp8, const uint8_t* k_fp8, int B, int H_I,
                                 int D_I, int64_t N, int64_t kv_seq_stride, int q_per_seq,
-                                const int32_t* q_pos, int ratio, float* scores,
+                                const int32_t* q_pos, int ratio, float* scores, int32_t* status,
                                 cudaStream_t stream) {
   if (B == 0 || N == 0) return cudaSuccess;
-  switch (D_I) {
-    case 32:
-      return launch_scores_t<32>(q_fp8, k_fp8, B, H_I, N, kv_seq_stride, q_per_seq, q_pos, ratio,
-                                 scores, stream);
-    case 64:
-      return launch_scores_t<64>(q_fp8, k_fp8, B, H_I, N, kv_seq_stride, q_per_seq, q_pos, ratio,
-                                 scores, stream);
-    default:
-      return launch_scores_t<128>(q_fp8, k_fp8, B, H_I, N, kv_seq_stride, q_per_seq, q_pos, ratio,
-                                  scores, stream);
-  }
+  return launch_index_scores_tc(q_fp8, k_fp8, B, H_I, D_I, N, kv_seq_stride, q_per_seq, q_pos,
+                                ratio, scores, status, stream);
 }
 
 cudaError_t launch_pool_scores(const uint8_t* q_fp8, const uint8_t* k_fp8, int B, int H_I,

@@ -11,8 +11,10 @@
 // Rows of up to 32768 candidates (topk_reg_kernel, one 512-thread CTA per
 // row): each thread holds KPT consecutive keys in registers, so the ordered
 // sweep needs only two block scans.  The radix passes start at the highest
-// bit where the row's min and max keys differ and take 11-bit digits; they
-// stop as soon as the threshold bin is consumed exactly.
+// bit where the row's min and max keys differ and take 8-bit digits counted
+// in per-warp private histograms (rows with few distinct scores, such as
+// integer-valued ones, would otherwise serialise on a handful of shared
+// bins); they stop as soon as the threshold bin is consumed exactly.
 // Longer rows (topk_long_kernel, 1024 threads): keys are re-read from the
 // (L2-resident) scores on every pass, three 11/11/10-bit passes, and the
 // ordered sweep runs in 1024-element rounds with warp ballots.
@@ -113,7 +115,7 @@ __global__ void __launch_bounds__(kRegThreads, 1)
 topk_reg_kernel(const float* __restrict__ scores, int64_t N, int k,
                 const int32_t* __restrict__ q_pos, int ratio, const int32_t* __restrict__ n_valid,
                 const int32_t* __restrict__ map, int32_t* __restrict__ idx) {
-  __shared__ int32_t hist[2048];
+  __shared__ int32_t whist[kRegWarps * 256];  // per-warp 8-bit digit histograms
   __shared__ int32_t tot[kRegWarps + 1];
   __shared__ uint32_t red_min[kRegWarps], red_max[kRegWarps];
   __shared__ int32_t s_digit, s_above, s_cnt;
@@ -202,44 +204,37 @@ topk_reg_kernel(const float* __restrict__ scores, int64_t N, int k,
   }
   int need = k;
   bool done = cur_hi < 0;
+  int32_t* my_hist = whist + warp * 256;  // this warp's private histogram
   while (!done) {
-    const int nbits = min(11, cur_hi + 1);
+    const int nbits = min(8, cur_hi + 1);
     const int shift = cur_hi + 1 - nbits;
-    const int nbins = 1 << nbits;
-    for (int i = tid; i < nbins; i += kRegThreads) hist[i] = 0;
+    const uint32_t dmask = (1u << nbits) - 1u;
+    for (int i = tid; i < kRegWarps * 256; i += kRegThreads) whist[i] = 0;
     __syncthreads();
 #pragma unroll
     for (int i = 0; i < KPT; ++i) {
       if (base + i < n && (key[i] & mask) == prefix)
-        atomicAdd(&hist[(key[i] >> shift) & (uint32_t)(nbins - 1)], 1);
+        atomicAdd(&my_hist[(key[i] >> shift) & dmask], 1);
     }
     __syncthreads();
-    const int per = (nbins + kRegThreads - 1) / kRegThreads;
-    const int dtop = nbins - 1 - tid * per;
+    // thread t < 256 owns digit 255 - t (descending order for the scan)
     int cnt = 0;
-    for (int p = 0; p < per; ++p)
-      if (dtop - p >= 0) cnt += hist[dtop - p];
+    if (tid < 256) {
+      const int d = 255 - tid;
+#pragma unroll
+      for (int w = 0; w < kRegWarps; ++w) cnt += whist[w * 256 + d];
+    }
     int total;
     const int before = reg_block_scan(cnt, tot, &total);
-    if (before < need && before + cnt >= need) {
-      int acc = before;
-      for (int p = 0; p < per; ++p) {
-        const int d = dtop - p;
-        if (d < 0) break;
-        const int h = hist[d];
-        if (acc + h >= need) {
-          s_digit = d;
-          s_above = acc;
-          s_cnt = h;
-          break;
-        }
-        acc += h;
-      }
+    if (tid < 256 && before < need && before + cnt >= need) {
+      s_digit = 255 - tid;
+      s_above = before;
+      s_cnt = cnt;
     }
     __syncthreads();
     need -= s_above;
     prefix |= (uint32_t)s_digit << shift;
-    mask |= (uint32_t)(nbins - 1) << shift;
+    mask |= dmask << shift;
     cur_hi = shift - 1;
     done = (cur_hi < 0) || (s_cnt == need);
     __syncthreads();
