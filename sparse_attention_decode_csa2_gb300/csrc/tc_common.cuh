@@ -40,13 +40,27 @@ __device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
-// Bounded wait for the phase with the given parity; false after ~2 s.
+// As mbar_try, but the thread may sleep up to `hint_ns` waiting for the
+// phase, instead of returning after the default (short) suspend window.
+__device__ __forceinline__ bool mbar_try_sleep(uint32_t bar, uint32_t parity, uint32_t hint_ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity), "r"(hint_ns)
+      : "memory");
+  return ok != 0;
+}
+
+// Bounded wait for the phase with the given parity; false after ~2 s.  The
+// waiting thread sleeps in the barrier (woken when the phase completes), so
+// waiting warps do not take issue slots from the working ones.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, int32_t* status) {
   if (mbar_try(bar, parity)) return true;
   const uint64_t t0 = globaltimer();
   while (true) {
-    for (int i = 0; i < 64; ++i)
-      if (mbar_try(bar, parity)) return true;
+    if (mbar_try_sleep(bar, parity, 1000000u)) return true;
     if (globaltimer() - t0 > kWaitLimitNs) {
       set_status(status, kStatusTimeout);
       return false;
