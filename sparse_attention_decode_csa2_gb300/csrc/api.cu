@@ -171,7 +171,8 @@ csa2_status csa2_hier_pool_index(const uint8_t* q_fp8, const uint8_t* k_fp8, int
   cudaError_t e = launch_pool_scores(q_fp8, k_fp8, B, H_I, D_I, N, kv_seq_stride, q_per_seq, pool,
                                      P, pscores, nullptr, status_ptr(ws), stream);
   if (e != cudaSuccess) return CSA2_ERR_CUDA;
-  return check_launch(launch_topk(pscores, B, P, k, nullptr, 1, nullptr, pool, idx, stream));
+  return check_launch(
+      launch_topk(pscores, B, P, k, nullptr, 1, nullptr, pool, idx, stream, /*pdl=*/true));
 }
 
 csa2_status csa2_sparse_attn_fp4(const uint16_t* q_bf16, const uint8_t* kv_fp4, int B, int H,
@@ -246,10 +247,10 @@ csa2_status csa2_layer_group(const csa2_layer* layers, int n_layers, const csa2_
                               g->q_per_seq, g->q_pos, g->ratio, scores, status, stream);
       if (e == cudaSuccess && L.mode == CSA2_FULL && g->pool_size > 0)
         e = launch_topk(scores, g->B, g->N, g->pool_size, g->q_pos, g->ratio, nullptr, nullptr,
-                        g->pool_out, stream);
+                        g->pool_out, stream, /*pdl=*/true);
       if (e == cudaSuccess)
         e = launch_topk(scores, g->B, g->N, g->k, g->q_pos, g->ratio, nullptr, nullptr, L.idx_out,
-                        stream);
+                        stream, /*pdl=*/true);
       use = L.idx_out;
     } else if (L.mode == CSA2_REINDEX) {
       e = launch_pool_scores(L.qi_fp8, g->ki_fp8, g->B, g->H_I, g->D_I, g->N, g->kv_seq_stride,
@@ -257,7 +258,7 @@ csa2_status csa2_layer_group(const csa2_layer* layers, int n_layers, const csa2_
                              stream);
       if (e == cudaSuccess)
         e = launch_topk(pscores, g->B, g->pool_size, g->k, nullptr, 1, nullptr, g->pool_out,
-                        L.idx_out, stream);
+                        L.idx_out, stream, /*pdl=*/true);
       use = L.idx_out;
     } else {  // REUSE
       use = latest;
@@ -267,9 +268,11 @@ csa2_status csa2_layer_group(const csa2_layer* layers, int n_layers, const csa2_
     }
     if (e != cudaSuccess) break;
     latest = use;
+    // After a top-k of this layer the attention starts early (programmatic
+    // dependent launch): it loads Q and sets up while the selection finishes.
     e = launch_sparse_attn(L.q_bf16, g->kv_fp4, g->B, g->H, g->N, g->kv_seq_stride, g->q_per_seq,
                            use, g->k, g->softmax_scale, L.out, L.lse, wsb + w.attn, status,
-                           stream);
+                           stream, /*pdl=*/L.mode != CSA2_REUSE);
   }
   return check_launch(e);
 }

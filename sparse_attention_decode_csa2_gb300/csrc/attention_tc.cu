@@ -127,8 +127,10 @@ sparse_attn_tc_kernel(const uint16_t* __restrict__ q_bf16, const uint8_t* __rest
   // slot s of this chunk (s < cnt): entry id, -1 if empty
   auto slot_at = [&](int s) -> int32_t { return s < kIdxCache ? idx_s[s] : slots[s]; };
 
-  // ---- prologue: slot indices, Q (bf16 -> fp16, swizzled, zero-padded to 64 rows) ----
-  for (int i = tid; i < min(cnt, kIdxCache); i += kThreadsTc) idx_s[i] = slots[i];
+  pdl_trigger();
+  // ---- prologue: Q (bf16 -> fp16, swizzled, zero-padded to 64 rows), TMEM,
+  //      barriers; then (once the kernel that selected them has finished) the
+  //      slot indices ----
   {
     constexpr int kQChunks = kHN * (kD / 8);
     constexpr int kPer = (kQChunks + kThreadsTc - 1) / kThreadsTc;
@@ -170,6 +172,8 @@ sparse_attn_tc_kernel(const uint16_t* __restrict__ q_bf16, const uint8_t* __rest
     ctl.rescale = 0;
   }
   if (tid < kHN) ctl.mref[tid] = -INFINITY;
+  pdl_wait();
+  for (int i = tid; i < min(cnt, kIdxCache); i += kThreadsTc) idx_s[i] = slots[i];
   proxy_fence();
   tc_fence_before();
   __syncthreads();
@@ -454,33 +458,32 @@ static cudaError_t launch_tc_t(const uint16_t* q_bf16, const uint8_t* kv_fp4, in
                                int64_t kv_seq_stride, int q_per_seq, const int32_t* idx, int k,
                                int nsplit, int chunk, float scale_log2, float* out, float* lse,
                                float* part_o, float* part_lse, int32_t* status,
-                               cudaStream_t stream) {
+                               cudaStream_t stream, bool pdl) {
   using L = TcLayout;
   cudaError_t e = cudaFuncSetAttribute(sparse_attn_tc_kernel<H>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)L::alloc);
   if (e != cudaSuccess) return e;
-  dim3 grid((unsigned)nsplit, (unsigned)B);
-  sparse_attn_tc_kernel<H><<<grid, kThreadsTc, L::alloc, stream>>>(
-      q_bf16, kv_fp4, N, kv_seq_stride, q_per_seq, idx, k, chunk, scale_log2, out, lse, part_o,
-      part_lse, status);
-  return cudaGetLastError();
+  return launch_kernel(sparse_attn_tc_kernel<H>, dim3((unsigned)nsplit, (unsigned)B),
+                       dim3(kThreadsTc), L::alloc, stream, pdl, q_bf16, kv_fp4, N, kv_seq_stride,
+                       q_per_seq, idx, k, chunk, scale_log2, out, lse, part_o, part_lse, status);
 }
 
 cudaError_t launch_sparse_attn_tc(const uint16_t* q_bf16, const uint8_t* kv_fp4, int B, int H,
                                   int64_t N, int64_t kv_seq_stride, int q_per_seq,
                                   const int32_t* idx, int k, int nsplit, int chunk,
                                   float scale_log2, float* out, float* lse, float* part_o,
-                                  float* part_lse, int32_t* status, cudaStream_t stream) {
+                                  float* part_lse, int32_t* status, cudaStream_t stream,
+                                  bool pdl) {
   switch (H) {
     case 16:
       return launch_tc_t<16>(q_bf16, kv_fp4, B, N, kv_seq_stride, q_per_seq, idx, k, nsplit,
-                             chunk, scale_log2, out, lse, part_o, part_lse, status, stream);
+                             chunk, scale_log2, out, lse, part_o, part_lse, status, stream, pdl);
     case 32:
       return launch_tc_t<32>(q_bf16, kv_fp4, B, N, kv_seq_stride, q_per_seq, idx, k, nsplit,
-                             chunk, scale_log2, out, lse, part_o, part_lse, status, stream);
+                             chunk, scale_log2, out, lse, part_o, part_lse, status, stream, pdl);
     default:
       return launch_tc_t<64>(q_bf16, kv_fp4, B, N, kv_seq_stride, q_per_seq, idx, k, nsplit,
-                             chunk, scale_log2, out, lse, part_o, part_lse, status, stream);
+                             chunk, scale_log2, out, lse, part_o, part_lse, status, stream, pdl);
   }
 }
 

@@ -77,6 +77,34 @@ __device__ __forceinline__ void set_status(int32_t* status, int32_t bits) {
   if (status) atomicOr(status, bits);
 }
 
+// Programmatic dependent launch.  A kernel launched with `pdl` set may begin
+// while the previous kernel of its stream is still running: it calls
+// pdl_wait() before it reads anything that kernel writes (without the launch
+// attribute the wait returns at once).  Kernels call pdl_trigger() as they
+// start, so that the next kernel's CTAs may be scheduled onto SMs they leave
+// free and run their independent set-up early.
+__device__ __forceinline__ void pdl_trigger() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+// Kernel launch with an optional programmatic-dependent-launch attribute.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_kernel(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                          cudaStream_t stream, bool pdl, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = pdl ? attr : nullptr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
+
 // ---------------------------------------------------------------------------
 // Launchers (each returns cudaGetLastError() of its launch)
 // ---------------------------------------------------------------------------
@@ -107,9 +135,10 @@ cudaError_t launch_pool_scores(const uint8_t* q_fp8, const uint8_t* k_fp8, int B
 // Top-k over rows of `scores` [B][N].  The number of candidates of row b is
 // n_visible(q_pos, b, ratio, N) when n_valid is null, else n_valid[b].  When
 // `map` is non-null the selected position p is written as map[b*N + p].
+// pdl: launched as a programmatic dependent of the kernel before it.
 cudaError_t launch_topk(const float* scores, int B, int64_t N, int k, const int32_t* q_pos,
                         int ratio, const int32_t* n_valid, const int32_t* map, int32_t* idx,
-                        cudaStream_t stream);
+                        cudaStream_t stream, bool pdl = false);
 
 // Sparse attention.  scratch: partial outputs when split over several CTAs.
 size_t attn_scratch_bytes(int B, int H, int k);
@@ -117,14 +146,15 @@ int attn_launches(int B, int k);  // kernels one sparse-attention call launches
 cudaError_t launch_sparse_attn(const uint16_t* q_bf16, const uint8_t* kv_fp4, int B, int H,
                                int64_t N, int64_t kv_seq_stride, int q_per_seq, const int32_t* idx,
                                int k, float softmax_scale, float* out, float* lse, void* scratch,
-                               int32_t* status, cudaStream_t stream);
+                               int32_t* status, cudaStream_t stream, bool pdl = false);
 
 // tcgen05 kernel of one sparse-attention call (partials when nsplit > 1).
 cudaError_t launch_sparse_attn_tc(const uint16_t* q_bf16, const uint8_t* kv_fp4, int B, int H,
                                   int64_t N, int64_t kv_seq_stride, int q_per_seq,
                                   const int32_t* idx, int k, int nsplit, int chunk,
                                   float scale_log2, float* out, float* lse, float* part_o,
-                                  float* part_lse, int32_t* status, cudaStream_t stream);
+                                  float* part_lse, int32_t* status, cudaStream_t stream,
+                                  bool pdl);
 
 int device_sm_count();
 

@@ -70,6 +70,8 @@ pool_scores_kernel(const uint8_t* __restrict__ q_fp8, const uint8_t* __restrict_
                    int32_t* status) {
   constexpr int TPE = D_I / 16;
   constexpr int EPI = kThreads / TPE;
+  pdl_trigger();
+  pdl_wait();
   __shared__ __align__(16) float qf[32 * 128];
   __shared__ float qsum[D_I];
   const int q = blockIdx.y;

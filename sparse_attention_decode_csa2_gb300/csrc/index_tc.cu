@@ -58,6 +58,8 @@ index_tc_kernel(const __grid_constant__ CUtensorMap tmap, const uint8_t* __restr
                 int tiles_per_cta, const int32_t* __restrict__ q_pos, int ratio,
                 float* __restrict__ scores, int32_t* status) {
   using L = IdxLayout<D_I>;
+  pdl_trigger();
+  pdl_wait();
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_s = su32(smem_raw);
   const uint32_t pad = (1024u - (raw_s & 1023u)) & 1023u;

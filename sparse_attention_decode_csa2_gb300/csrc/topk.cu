@@ -120,6 +120,8 @@ topk_reg_kernel(const float* __restrict__ scores, int64_t N, int k,
   __shared__ uint32_t red_min[kRegWarps], red_max[kRegWarps];
   __shared__ int32_t s_digit, s_above, s_cnt;
 
+  pdl_trigger();
+  pdl_wait();  // scores, n_valid and map come from the kernel before
   const int b = blockIdx.x;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const float* row = scores + (int64_t)b * N;
@@ -281,6 +283,8 @@ topk_long_kernel(const float* __restrict__ scores, int64_t N, int k, const int32
   // warp_tot scratch for scans needs kWarps + 1 slots
   __shared__ int32_t scan_tot[kWarps + 1];
 
+  pdl_trigger();
+  pdl_wait();  // scores, n_valid and map come from the kernel before
   const int b = blockIdx.x;
   const int tid = threadIdx.x;
   const int lane = tid & 31, warp = tid >> 5;
@@ -414,27 +418,25 @@ topk_long_kernel(const float* __restrict__ scores, int64_t N, int k, const int32
 
 cudaError_t launch_topk(const float* scores, int B, int64_t N, int k, const int32_t* q_pos,
                         int ratio, const int32_t* n_valid, const int32_t* map, int32_t* idx,
-                        cudaStream_t stream) {
+                        cudaStream_t stream, bool pdl) {
   if (B == 0) return cudaSuccess;
+  const dim3 grid((unsigned)B);
   if (N <= kRegMaxKeys) {
     if (N <= kRegThreads * 8)
-      topk_reg_kernel<8><<<B, kRegThreads, 0, stream>>>(scores, N, k, q_pos, ratio, n_valid, map,
-                                                        idx);
-    else if (N <= kRegThreads * 16)
-      topk_reg_kernel<16><<<B, kRegThreads, 0, stream>>>(scores, N, k, q_pos, ratio, n_valid, map,
-                                                         idx);
-    else if (N <= kRegThreads * 32)
-      topk_reg_kernel<32><<<B, kRegThreads, 0, stream>>>(scores, N, k, q_pos, ratio, n_valid, map,
-                                                         idx);
-    else
-      topk_reg_kernel<64><<<B, kRegThreads, 0, stream>>>(scores, N, k, q_pos, ratio, n_valid, map,
-                                                         idx);
-    return cudaGetLastError();
+      return launch_kernel(topk_reg_kernel<8>, grid, dim3(kRegThreads), 0, stream, pdl, scores, N,
+                           k, q_pos, ratio, n_valid, map, idx);
+    if (N <= kRegThreads * 16)
+      return launch_kernel(topk_reg_kernel<16>, grid, dim3(kRegThreads), 0, stream, pdl, scores,
+                           N, k, q_pos, ratio, n_valid, map, idx);
+    if (N <= kRegThreads * 32)
+      return launch_kernel(topk_reg_kernel<32>, grid, dim3(kRegThreads), 0, stream, pdl, scores,
+                           N, k, q_pos, ratio, n_valid, map, idx);
+    return launch_kernel(topk_reg_kernel<64>, grid, dim3(kRegThreads), 0, stream, pdl, scores, N,
+                         k, q_pos, ratio, n_valid, map, idx);
   }
   const size_t base = align_up(sizeof(TopkShared), 16);
-  topk_long_kernel<false><<<B, kThreads, base, stream>>>(scores, N, k, q_pos, ratio, n_valid, map,
-                                                         idx);
-  return cudaGetLastError();
+  return launch_kernel(topk_long_kernel<false>, grid, dim3(kThreads), base, stream, pdl, scores, N,
+                       k, q_pos, ratio, n_valid, map, idx);
 }
 
 }  // namespace csa2
