@@ -9,12 +9,18 @@
 // and the first `need` members of the class, in ascending position.
 //
 // Rows of up to 32768 candidates (topk_reg_kernel, one 512-thread CTA per
-// row): each thread holds KPT consecutive keys in registers, so the ordered
-// sweep needs only two block scans.  The radix passes start at the highest
-// bit where the row's min and max keys differ and take 8-bit digits counted
-// in per-warp private histograms (rows with few distinct scores, such as
-// integer-valued ones, would otherwise serialise on a handful of shared
-// bins); they stop as soon as the threshold bin is consumed exactly.
+// row): each thread holds KPT consecutive keys in registers.  The radix
+// passes take 8-bit digits from the highest bit where the row's min and max
+// keys differ down to the lowest bit that differs between two keys of the
+// selected sign (OR ^ AND per sign; integer-valued scores skip their zero
+// low mantissa),
+// counted in per-warp private histograms (rows with few distinct scores
+// would otherwise serialise on a handful of shared bins), and stop as soon
+// as the threshold bin is consumed exactly.  The histograms are
+// double-buffered (one is cleared while the other is summed) and every warp
+// picks the digit from the summed counts itself: two barriers per pass.  The
+// ordered sweep builds above / class bit masks, needs one block scan, and is
+// staged in shared memory so that the output is written coalesced.
 // Longer rows (topk_long_kernel, 1024 threads): keys are re-read from the
 // (L2-resident) scores on every pass, three 11/11/10-bit passes, and the
 // ordered sweep runs in 1024-element rounds with warp ballots.
@@ -110,15 +116,55 @@ __device__ __forceinline__ int reg_block_scan(int v, int32_t* tot, int* total) {
   return r;
 }
 
+// Warp-wide choice of the radix digit that holds the need-th largest key:
+// csum[t] = number of keys with digit 255 - t (descending digit order).
+// Every warp runs it on the same counts and reaches the same answer, so no
+// broadcast (and no barrier) is needed.  Returns the digit; *above = keys in
+// larger digits, *cnt = keys with this digit.
+__device__ __forceinline__ int select_digit(const int32_t* csum, int need, int* above, int* cnt) {
+  const int lane = threadIdx.x & 31;
+  const int4 a = reinterpret_cast<const int4*>(csum)[2 * lane];
+  const int4 b = reinterpret_cast<const int4*>(csum)[2 * lane + 1];
+  const int c[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+  int local = 0;
+#pragma unroll
+  for (int j = 0; j < 8; ++j) local += c[j];
+  int incl = local;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += y;
+  }
+  int before = incl - local;
+  int hit = -1, hit_before = 0, hit_cnt = 0;
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    if (hit < 0 && before < need && before + c[j] >= need) {
+      hit = j;
+      hit_before = before;
+      hit_cnt = c[j];
+    }
+    before += c[j];
+  }
+  const unsigned m = __ballot_sync(0xffffffffu, hit >= 0);
+  const int src = __ffs(m) - 1;
+  const int t = __shfl_sync(0xffffffffu, 8 * lane + hit, src);
+  *above = __shfl_sync(0xffffffffu, hit_before, src);
+  *cnt = __shfl_sync(0xffffffffu, hit_cnt, src);
+  return 255 - t;
+}
+
 template <int KPT>
 __global__ void __launch_bounds__(kRegThreads, 1)
 topk_reg_kernel(const float* __restrict__ scores, int64_t N, int k,
                 const int32_t* __restrict__ q_pos, int ratio, const int32_t* __restrict__ n_valid,
                 const int32_t* __restrict__ map, int32_t* __restrict__ idx) {
-  __shared__ int32_t whist[kRegWarps * 256];  // per-warp 8-bit digit histograms
+  // two sets of per-warp 8-bit digit histograms: one is counted into while
+  // the other is cleared for the next pass; reused to stage the output
+  __shared__ __align__(16) int32_t whist[2][kRegWarps * 256];
+  __shared__ __align__(16) int32_t csum[256];
   __shared__ int32_t tot[kRegWarps + 1];
-  __shared__ uint32_t red_min[kRegWarps], red_max[kRegWarps];
-  __shared__ int32_t s_digit, s_above, s_cnt;
+  __shared__ uint32_t red[4][kRegWarps];
 
   pdl_trigger();
   pdl_wait();  // scores, n_valid and map come from the kernel before
@@ -164,110 +210,144 @@ topk_reg_kernel(const float* __restrict__ scores, int64_t N, int k,
     for (int e = 0; e < 4; ++e) key[i + e] = float_to_ordered(v[e]);
   }
 
-  // highest bit where the row's keys differ
-  uint32_t kmin = 0xFFFFFFFFu, kmax = 0u;
+  // OR / AND of the keys, per sign of the score.  Over the whole row they
+  // give the highest differing bit (where the passes start) and the common
+  // prefix above it.  Once the sign is decided (the first pass covers it when
+  // both occur), bits below the lowest one that differs among keys of that
+  // sign (the zero low mantissa of integer-valued scores, say) are never
+  // counted.
+  uint32_t por = 0u, pand = 0xFFFFFFFFu, nor = 0u, nand = 0xFFFFFFFFu;  // >= 0 / < 0
 #pragma unroll
   for (int i = 0; i < KPT; ++i) {
-    if (base + i < n) {
-      kmin = min(kmin, key[i]);
-      kmax = max(kmax, key[i]);
-    }
+    const uint32_t valid = base + i < n ? 0xFFFFFFFFu : 0u;
+    const uint32_t pos = valid & (0u - (key[i] >> 31));  // all ones for a valid key >= 0
+    const uint32_t neg = valid & ~pos;
+    por |= key[i] & pos;
+    pand &= key[i] | ~pos;
+    nor |= key[i] & neg;
+    nand &= key[i] | ~neg;
   }
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
-    kmin = min(kmin, __shfl_xor_sync(0xffffffffu, kmin, o));
-    kmax = max(kmax, __shfl_xor_sync(0xffffffffu, kmax, o));
-  }
+  por = __reduce_or_sync(0xffffffffu, por);
+  pand = __reduce_and_sync(0xffffffffu, pand);
+  nor = __reduce_or_sync(0xffffffffu, nor);
+  nand = __reduce_and_sync(0xffffffffu, nand);
   if (lane == 0) {
-    red_min[warp] = kmin;
-    red_max[warp] = kmax;
+    red[0][warp] = por;
+    red[1][warp] = pand;
+    red[2][warp] = nor;
+    red[3][warp] = nand;
   }
+  for (int i = tid; i < kRegWarps * 256; i += kRegThreads) whist[0][i] = 0;
   __syncthreads();
-  kmin = red_min[0];
-  kmax = red_max[0];
 #pragma unroll
-  for (int w = 1; w < kRegWarps; ++w) {
-    kmin = min(kmin, red_min[w]);
-    kmax = max(kmax, red_max[w]);
+  for (int w = 0; w < kRegWarps; ++w) {
+    por |= red[0][w];
+    pand &= red[1][w];
+    nor |= red[2][w];
+    nand &= red[3][w];
   }
+  // lowest differing bit among the keys of one sign (32: they are all equal)
+  const int lo_pos = (por ^ pand) ? __ffs(por ^ pand) - 1 : 32;
+  const int lo_neg = (nor ^ nand) ? __ffs(nor ^ nand) - 1 : 32;
+  const uint32_t kor = por | nor, kand = pand & nand;  // over the whole row
 
-  uint32_t prefix, mask;
-  int cur_hi;
-  const uint32_t diff = kmin ^ kmax;
-  if (diff == 0u) {
-    prefix = kmax;
-    mask = 0xFFFFFFFFu;
-    cur_hi = -1;
-  } else {
-    const int hb = 31 - __clz(diff);
-    mask = ~((2u << hb) - 1u);  // hb = 31: 2u << 31 wraps to 0, mask = 0
-    prefix = kmax & mask;
-    cur_hi = hb;
+  uint32_t prefix = kand, mask = 0xFFFFFFFFu;  // all keys equal: one class
+  int cur_hi = -1, lo = 0;
+  if (kor != kand) {
+    cur_hi = 31 - __clz(kor ^ kand);
+    mask = ~((2u << cur_hi) - 1u);  // cur_hi = 31: 2u << 31 wraps to 0, mask = 0
+    prefix = kand & mask;
+    // both signs present: bit 31 itself differs, so the first pass covers it
+    lo = min(cur_hi, cur_hi == 31 ? min(lo_pos, lo_neg) : ((kor >> 31) ? lo_pos : lo_neg));
   }
   int need = k;
-  bool done = cur_hi < 0;
-  int32_t* my_hist = whist + warp * 256;  // this warp's private histogram
-  while (!done) {
-    const int nbits = min(8, cur_hi + 1);
+  for (int pass = 0; cur_hi >= lo; ++pass) {
+    const int nbits = min(8, cur_hi + 1 - lo);
     const int shift = cur_hi + 1 - nbits;
     const uint32_t dmask = (1u << nbits) - 1u;
-    for (int i = tid; i < kRegWarps * 256; i += kRegThreads) whist[i] = 0;
-    __syncthreads();
+    int32_t* hist = whist[pass & 1];
+    int32_t* my_hist = hist + warp * 256;  // this warp's private histogram
 #pragma unroll
     for (int i = 0; i < KPT; ++i) {
       if (base + i < n && (key[i] & mask) == prefix)
         atomicAdd(&my_hist[(key[i] >> shift) & dmask], 1);
     }
     __syncthreads();
-    // thread t < 256 owns digit 255 - t (descending order for the scan)
-    int cnt = 0;
     if (tid < 256) {
+      // thread t sums digit 255 - t over the warps (descending order for the scan)
       const int d = 255 - tid;
+      int c = 0;
 #pragma unroll
-      for (int w = 0; w < kRegWarps; ++w) cnt += whist[w * 256 + d];
-    }
-    int total;
-    const int before = reg_block_scan(cnt, tot, &total);
-    if (tid < 256 && before < need && before + cnt >= need) {
-      s_digit = 255 - tid;
-      s_above = before;
-      s_cnt = cnt;
+      for (int w = 0; w < kRegWarps; ++w) c += hist[w * 256 + d];
+      csum[tid] = c;
+    } else {
+      int32_t* next = whist[(pass + 1) & 1];
+      for (int i = tid - 256; i < kRegWarps * 256; i += kRegThreads - 256) next[i] = 0;
     }
     __syncthreads();
-    need -= s_above;
-    prefix |= (uint32_t)s_digit << shift;
+    int above, cnt;
+    const int digit = select_digit(csum, need, &above, &cnt);
+    need -= above;
+    prefix |= (uint32_t)digit << shift;
     mask |= dmask << shift;
     cur_hi = shift - 1;
-    done = (cur_hi < 0) || (s_cnt == need);
-    __syncthreads();
+    lo = (prefix >> 31) ? lo_pos : lo_neg;  // the sign bit is decided now
+    if (cnt == need) break;  // the whole class is taken
   }
+  // (keys agree on every bit below `lo`, so comparing on the bits of `mask`
+  // orders them completely)
 
-  // ordered write: keys above the class, then the first `need` class members
+  // ordered write: every key above the class (key & mask > prefix), then the
+  // first `need` class members in position order.  One scan of the two
+  // counts packed in 16-bit halves (n <= 32768) gives both prefixes; the
+  // class members taken before this thread are min(eq_before, need).
+  uint32_t gtm[(KPT + 31) / 32], eqm[(KPT + 31) / 32];
   int gt = 0, eq = 0;
 #pragma unroll
-  for (int i = 0; i < KPT; ++i) {
-    if (base + i < n) {
-      const uint32_t km = key[i] & mask;
-      gt += km > prefix;
-      eq += km == prefix;
+  for (int w = 0; w < (KPT + 31) / 32; ++w) {
+    uint32_t g = 0u, e = 0u;
+#pragma unroll
+    for (int i = 0; i < 32 && 32 * w + i < KPT; ++i) {
+      const int ii = 32 * w + i;
+      const uint32_t km = key[ii] & mask;
+      const bool valid = base + ii < n;
+      g |= (uint32_t)(valid && km > prefix) << i;
+      e |= (uint32_t)(valid && km == prefix) << i;
+    }
+    gtm[w] = g;
+    eqm[w] = e;
+    gt += __popc(g);
+    eq += __popc(e);
+  }
+  int tot_packed;
+  const int before = reg_block_scan((gt << 16) | eq, tot, &tot_packed);
+  const int eq_before = before & 0xFFFF;
+  int take = max(0, min(eq, need - eq_before));
+  int off = (before >> 16) + min(eq_before, need);
+  const bool staged = k <= 2 * kRegWarps * 256;
+  int32_t* stage = &whist[0][0];
+#pragma unroll
+  for (int w = 0; w < (KPT + 31) / 32; ++w) {
+    uint32_t sel = gtm[w];
+    for (uint32_t c = eqm[w]; take > 0 && c != 0u; --take) {
+      sel |= c & (~c + 1u);  // lowest remaining class member
+      c &= c - 1u;
+    }
+    while (sel != 0u && off < k) {
+      const int p = base + 32 * w + __ffs(sel) - 1;
+      sel &= sel - 1u;
+      if (staged)
+        stage[off] = p;
+      else
+        out[off] = mrow ? mrow[p] : p;
+      ++off;
     }
   }
-  int tot_eq, tot_sel;
-  const int eq_before = reg_block_scan(eq, tot, &tot_eq);
-  const int take_eq = max(0, min(eq, need - eq_before));
-  int off = reg_block_scan(gt + take_eq, tot, &tot_sel);
-  int taken = 0;
-#pragma unroll
-  for (int i = 0; i < KPT; ++i) {
-    if (base + i < n) {
-      const uint32_t km = key[i] & mask;
-      const bool is_eq = km == prefix;
-      const bool t = (km > prefix) || (is_eq && taken < take_eq);
-      taken += (is_eq && t);
-      if (t && off < k) {
-        out[off] = mrow ? mrow[base + i] : base + i;
-        ++off;
-      }
+  if (staged) {
+    __syncthreads();
+    for (int j = tid; j < k; j += kRegThreads) {
+      const int32_t p = stage[j];
+      out[j] = mrow ? mrow[p] : p;
     }
   }
 }
