@@ -10,12 +10,21 @@
 // query in the group.  FP8 products are exact; each head's 64-term sum and
 // the head sum accumulate in fp32 (exact for integer-valued inputs).
 //
-// Roles (192 threads): warp 0 lane 0 streams 128-entry K tiles with 2D TMA
-// (swizzle matching the UMMA layout) into an 8-stage ring; warp 1 owns the
-// TMEM accumulator (two buffers) and lane 0 issues the MMAs; warps 2-5 (one
-// thread per TMEM lane = entry) sum the head columns, apply causal
-// visibility and store the scores.  Tiles wholly past every query's visible
-// prefix are not loaded; their scores are written as -inf directly.
+// Work split: the (query group, 128-entry tile) items of the whole call are
+// cut into one contiguous range per CTA, and the grid holds no more CTAs than
+// fit on the GPU at once, so every SM streams K tiles for the whole kernel
+// (no second, partly empty wave).  A range spans at most two query groups;
+// both groups' B operands are kept.
+//
+// Roles (192 threads): warp 0 lane 0 streams K tiles with 2D TMA (swizzle
+// matching the UMMA layout) into an 8-stage ring, the first 8 requested
+// before the queries' visibility is known; warp 1 owns the TMEM accumulator (two buffers) and lane 0
+// issues the MMAs; warps 2-5 first stage the B operands and the queries'
+// visible lengths (signalled on an mbarrier), then, one thread per TMEM lane
+// = entry, sum the head columns, apply causal visibility and store the
+// scores.  Tiles wholly past every query's visible prefix are not loaded
+// (beyond the first ring's worth, which is requested speculatively); their
+// scores are written as -inf directly.
 #include <cuda.h>
 
 #include "csa2_internal.cuh"
@@ -35,27 +44,36 @@ struct IdxCtl {
   uint64_t empty[kStages];
   uint64_t acc_full[2];
   uint64_t acc_empty[2];
+  uint64_t meta;           // B operands, visible lengths and live_end staged
   uint32_t tmem_base;
-  int32_t nvis[16];
+  int32_t live_end[2];     // per group of the range: tiles holding any visible entry
+  int32_t nvis[2][16];
 };
 
 template <int D_I>
 struct IdxLayout {
   static constexpr uint32_t tile_bytes = kTile * D_I;
   static constexpr uint32_t k_off = 0;
-  static constexpr uint32_t b_off = k_off + kStages * tile_bytes;  // up to 256 rows x D_I
-  static constexpr uint32_t b_bytes = 256 * D_I;
-  static constexpr uint32_t ctl_off = b_off + b_bytes;
-  static constexpr uint32_t bytes = ctl_off + 512;
-  static constexpr uint32_t alloc = bytes + 1024;
+  static constexpr uint32_t b_off = k_off + kStages * tile_bytes;
+  static constexpr uint32_t b_max = 256 * D_I;  // one group's B: up to 256 rows x D_I
+  // B stride for NB rows, whole 8-row swizzle atoms, 1 KiB aligned
+  __host__ __device__ static uint32_t b_stride(int NB) {
+    return (uint32_t)((NB * D_I + 1023) / 1024 * 1024);
+  }
+  __host__ __device__ static uint32_t ctl_off(int NB) { return b_off + 2 * b_stride(NB); }
+  __host__ __device__ static uint32_t alloc(int NB) { return ctl_off(NB) + 512 + 1024; }
 };
 
-// One CTA: query group [q0, q0 + QG) (one sequence) x tiles [t0, t0 + nt) of 128 entries.
+__device__ __forceinline__ uint32_t idx_tmem_cols(int NB) {
+  return NB <= 16 ? 32u : (NB <= 32 ? 64u : (NB <= 64 ? 128u : (NB <= 128 ? 256u : 512u)));
+}
+
+// One CTA: items [w0, w1) of the call, item w = (group w / T, tile w % T).
 template <int D_I>
 __global__ void __launch_bounds__(kIdxThreads, 1)
 index_tc_kernel(const __grid_constant__ CUtensorMap tmap, const uint8_t* __restrict__ q_fp8,
                 int B, int H_I, int64_t N, int64_t kv_seq_stride, int q_per_seq, int QG, int NB,
-                int tiles_per_cta, const int32_t* __restrict__ q_pos, int ratio,
+                int64_t T, int64_t W, const int32_t* __restrict__ q_pos, int ratio,
                 float* __restrict__ scores, int32_t* status) {
   using L = IdxLayout<D_I>;
   pdl_trigger();
@@ -65,31 +83,31 @@ index_tc_kernel(const __grid_constant__ CUtensorMap tmap, const uint8_t* __restr
   const uint32_t pad = (1024u - (raw_s & 1023u)) & 1023u;
   uint8_t* smem = smem_raw + pad;
   const uint32_t sbase = raw_s + pad;
-  IdxCtl& ctl = *reinterpret_cast<IdxCtl*>(smem + L::ctl_off);
+  const uint32_t bstride = L::b_stride(NB);
+  IdxCtl& ctl = *reinterpret_cast<IdxCtl*>(smem + L::ctl_off(NB));
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int q0 = blockIdx.y * QG;
-  const int nq = min(QG, B - q0);
-  const int64_t total_tiles = (N + kTile - 1) / kTile;
-  const int64_t t0 = (int64_t)blockIdx.x * tiles_per_cta;
-  const int nt = (int)(total_tiles - t0 < tiles_per_cta ? total_tiles - t0 : tiles_per_cta);
-  const int64_t row0 = (int64_t)(q0 / q_per_seq) * kv_seq_stride;  // first row of the sequence
-
-  // ---- prologue: B operand (heads of the group's queries), barriers, TMEM ----
-  for (int i = tid; i < 256 * D_I / 16; i += kIdxThreads) {
-    const int n = i / (D_I / 16), c = i % (D_I / 16);
-    uint4 v = make_uint4(0, 0, 0, 0);
-    if (n < NB) {
-      const int qq = n / H_I, h = n % H_I;
-      if (qq < nq)
-        v = __ldg(reinterpret_cast<const uint4*>(q_fp8 + ((int64_t)(q0 + qq) * H_I + h) * D_I) +
-                  c);
+  const int64_t C = gridDim.x;
+  const int64_t w0 = (int64_t)blockIdx.x * W / C, w1 = ((int64_t)blockIdx.x + 1) * W / C;
+  const int nitems = (int)(w1 - w0);
+  const int64_t g0 = w0 / T;  // first group of the range (the range ends in g0 or g0 + 1)
+  const uint32_t cols = idx_tmem_cols(NB);
+  const int ng = (int)((w1 - 1) / T - g0) + 1;  // groups in the range: 1 or 2
+  if (warp >= 2) {
+    // The heads and positions of the range's queries are requested first,
+    // ahead of the K stream in the memory queues (read again, from L2, below).
+    const int et = tid - 64;
+    for (int gi = 0; gi < ng; ++gi) {
+      const int64_t q0 = (g0 + gi) * QG;
+      const int nq = (int)min((int64_t)QG, (int64_t)B - q0);
+      const uint8_t* qb = q_fp8 + q0 * H_I * D_I;
+      for (int off = et * 128; off < nq * H_I * D_I; off += 128 * 128)
+        asm volatile("prefetch.global.L2 [%0];" ::"l"(qb + off));
+      if (q_pos && et < nq) asm volatile("prefetch.global.L2 [%0];" ::"l"(q_pos + q0 + et));
     }
-    *reinterpret_cast<uint4*>(smem + L::b_off + swz_off(n, c * 16, D_I)) = v;
   }
-  if (tid < 16) ctl.nvis[tid] = (tid < nq) ? (int)n_visible(q_pos, q0 + tid, ratio, N) : 0;
+
   if (warp == 1) {
-    const uint32_t cols = NB <= 16 ? 32u : (NB <= 32 ? 64u : (NB <= 64 ? 128u : (NB <= 128 ? 256u : 512u)));
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
                      su32(&ctl.tmem_base)),
                  "r"(cols));
@@ -104,30 +122,42 @@ index_tc_kernel(const __grid_constant__ CUtensorMap tmap, const uint8_t* __restr
       mbar_init(su32(&ctl.acc_full[i]), 1);
       mbar_init(su32(&ctl.acc_empty[i]), 4);
     }
+    mbar_init(su32(&ctl.meta), 1);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
-  proxy_fence();
+  // first row of the sequence of group g0 + gi
+  const int64_t row_g0 = ((g0 * QG) / q_per_seq) * kv_seq_stride;
+  const int64_t row_g1 = (((g0 + 1) * QG) / q_per_seq) * kv_seq_stride;
+  const int n_spec = nitems < kStages ? nitems : kStages;
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = ctl.tmem_base;
-  int nvis_max = 0;
-#pragma unroll 1
-  for (int i = 0; i < nq; ++i) nvis_max = max(nvis_max, ctl.nvis[i]);
-  // tiles [t0, t0 + n_live) hold visible entries of some query
-  const int64_t live_end = (nvis_max + kTile - 1) / kTile;
-  const int64_t live_n = live_end - t0 < nt ? live_end - t0 : nt;
-  const int n_live = (int)(live_n > 0 ? live_n : 0);
+  // item i of the range is loaded, multiplied and read back iff it is in the
+  // first (speculative) ring's worth or its tile holds a visible entry
+  auto processed = [&](int i, int64_t g, int64_t t) {
+    return i < n_spec || t < ctl.live_end[g - g0];
+  };
 
   if (warp == 0) {
     if (lane == 0) {
-      for (int i = 0; i < n_live; ++i) {
-        const int s = i % kStages;
-        const uint32_t ph = (uint32_t)(i / kStages) & 1u;
+      // the first ring's worth is requested at once (speculatively: the
+      // visible lengths may still be on their way)
+      int n = 0;
+      bool meta = false;
+      int64_t g = g0, t = w0 - g0 * T;
+      for (int i = 0; i < nitems; ++i, t = (t + 1 == T) ? (++g, 0) : t + 1) {
+        if (i >= n_spec) {
+          if (!meta && !(meta = mbar_wait(su32(&ctl.meta), 0, status))) break;
+          if (!processed(i, g, t)) continue;
+        }
+        const int s = n % kStages;
+        const uint32_t ph = (uint32_t)(n / kStages) & 1u;
         if (!mbar_wait(su32(&ctl.empty[s]), ph ^ 1u, status)) break;
         mbar_expect_tx(su32(&ctl.full[s]), L::tile_bytes);
         tma_load_2d(sbase + L::k_off + s * L::tile_bytes, &tmap, 0,
-                    (int)(row0 + (t0 + i) * kTile), su32(&ctl.full[s]));
+                    (int)((g == g0 ? row_g0 : row_g1) + t * kTile), su32(&ctl.full[s]));
+        ++n;
       }
     }
   } else if (warp == 1) {
@@ -135,41 +165,79 @@ index_tc_kernel(const __grid_constant__ CUtensorMap tmap, const uint8_t* __restr
       const uint32_t idesc = idesc_e4m3(NB);
       const uint64_t dA0 = swz_desc(sbase + L::k_off, D_I);
       const uint64_t dB0 = swz_desc(sbase + L::b_off, D_I);
-      bool alive = true;
-      for (int i = 0; i < n_live && alive; ++i) {
-        const int s = i % kStages;
-        const uint32_t ph = (uint32_t)(i / kStages) & 1u;
-        const int ab = i & 1;
+      bool alive = mbar_wait(su32(&ctl.meta), 0, status);
+      int n = 0;
+      int64_t g = g0, t = w0 - g0 * T;
+      for (int i = 0; i < nitems && alive; ++i, t = (t + 1 == T) ? (++g, 0) : t + 1) {
+        if (!processed(i, g, t)) continue;
+        const int s = n % kStages;
+        const uint32_t ph = (uint32_t)(n / kStages) & 1u;
+        const int ab = n & 1;
         if (!mbar_wait(su32(&ctl.full[s]), ph, status) ||
-            !mbar_wait(su32(&ctl.acc_empty[ab]), (((uint32_t)i >> 1) & 1u) ^ 1u, status)) {
+            !mbar_wait(su32(&ctl.acc_empty[ab]), (((uint32_t)n >> 1) & 1u) ^ 1u, status)) {
           alive = false;
           break;
         }
         tc_fence_after();
         const uint64_t da0 = dA0 + ((uint32_t)(s * L::tile_bytes) >> 4);
+        const uint64_t db0 = dB0 + ((uint32_t)((g - g0) * bstride) >> 4);
 #pragma unroll
         for (int kk = 0; kk < D_I / 32; ++kk)
-          mma_e4m3(tmem + ab * NB, da0 + ((kk * 32) >> 4), dB0 + ((kk * 32) >> 4), idesc,
+          mma_e4m3(tmem + ab * NB, da0 + ((kk * 32) >> 4), db0 + ((kk * 32) >> 4), idesc,
                    kk > 0 ? 1u : 0u);
         mma_commit(su32(&ctl.acc_full[ab]));
         mma_commit(su32(&ctl.empty[s]));
+        ++n;
       }
-      if (alive && n_live > 0)
-        mbar_wait(su32(&ctl.acc_full[(n_live - 1) & 1]), (((uint32_t)(n_live - 1)) >> 1) & 1u,
-                  status);
+      if (alive && n > 0)
+        mbar_wait(su32(&ctl.acc_full[(n - 1) & 1]), (((uint32_t)(n - 1)) >> 1) & 1u, status);
     }
   } else {
-    // epilogue: thread = TMEM lane = entry row of the tile
+    // ---- stage the B operands (heads of each group's queries) and the visible lengths ----
+    const int et = tid - 64;  // 0..127
+    for (int gi = 0; gi < ng; ++gi) {
+      const int64_t q0 = (g0 + gi) * QG;
+      const int nq = (int)min((int64_t)QG, (int64_t)B - q0);
+      for (int i = et; i < NB * D_I / 16; i += 128) {
+        const int nrow = i / (D_I / 16), c = i % (D_I / 16);
+        uint4 v = make_uint4(0, 0, 0, 0);
+        const int qq = nrow / H_I, h = nrow % H_I;
+        if (qq < nq)
+          v = __ldg(reinterpret_cast<const uint4*>(q_fp8 + ((q0 + qq) * H_I + h) * D_I) + c);
+        *reinterpret_cast<uint4*>(smem + L::b_off + gi * bstride + swz_off(nrow, c * 16, D_I)) = v;
+      }
+      if (et < 16) ctl.nvis[gi][et] = (et < nq) ? (int)n_visible(q_pos, (int)(q0 + et), ratio, N) : 0;
+    }
+    proxy_fence();
+    asm volatile("bar.sync 1, 128;" ::: "memory");
+    if (et == 0) {
+      for (int gi = 0; gi < 2; ++gi) {
+        int m = 0;
+        if (gi < ng)
+          for (int i = 0; i < 16; ++i) m = max(m, ctl.nvis[gi][i]);
+        ctl.live_end[gi] = (int)((m + kTile - 1) / kTile);
+      }
+      mbar_arrive(su32(&ctl.meta));
+    }
+    asm volatile("bar.sync 1, 128;" ::: "memory");
+
+    // ---- epilogue: thread = TMEM lane = entry row of the tile ----
     const int r = (warp & 3) * 32 + lane;
     const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
     bool alive = true;
-    for (int i = 0; i < nt; ++i) {
-      const int64_t e = (t0 + i) * kTile + r;
-      if (i < n_live && alive) {
-        const int ab = i & 1;
-        if (!mbar_wait(su32(&ctl.acc_full[ab]), ((uint32_t)i >> 1) & 1u, status)) {
-          alive = false;
-        } else {
+    int n = 0;
+    int64_t g = g0, t = w0 - g0 * T;
+    for (int i = 0; i < nitems; ++i, t = (t + 1 == T) ? (++g, 0) : t + 1) {
+      const int64_t e = t * kTile + r;
+      const int64_t q0 = g * QG;
+      const int nq = (int)min((int64_t)QG, (int64_t)B - q0);
+      const int32_t* nv = ctl.nvis[g - g0];
+      if (processed(i, g, t)) {
+        const int ab = n & 1;
+        const uint32_t ph = ((uint32_t)n >> 1) & 1u;
+        ++n;
+        if (alive && !mbar_wait(su32(&ctl.acc_full[ab]), ph, status)) alive = false;
+        if (alive) {
           tc_fence_after();
           for (int qq = 0; qq < nq; ++qq) {
             // this query's H_I head columns
@@ -194,7 +262,7 @@ index_tc_kernel(const __grid_constant__ CUtensorMap tmap, const uint8_t* __restr
               for (int j = 0; j < 16; ++j)
                 if (j >= off && j < off + (H_I - h)) acc += v[j];
             }
-            if (e < N) scores[(int64_t)(q0 + qq) * N + e] = (e < ctl.nvis[qq]) ? acc : -INFINITY;
+            if (e < N) scores[(q0 + qq) * N + e] = (e < nv[qq]) ? acc : -INFINITY;
           }
           tc_fence_before();
           __syncwarp();
@@ -203,17 +271,15 @@ index_tc_kernel(const __grid_constant__ CUtensorMap tmap, const uint8_t* __restr
         }
       }
       if (e < N)
-        for (int qq = 0; qq < nq; ++qq) scores[(int64_t)(q0 + qq) * N + e] = -INFINITY;
+        for (int qq = 0; qq < nq; ++qq) scores[(q0 + qq) * N + e] = -INFINITY;
     }
   }
 
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  if (warp == 1) {
-    const uint32_t cols = NB <= 16 ? 32u : (NB <= 32 ? 64u : (NB <= 64 ? 128u : (NB <= 128 ? 256u : 512u)));
+  if (warp == 1)
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(cols));
-  }
 }
 
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
@@ -257,27 +323,37 @@ cudaError_t launch_t(const uint8_t* q_fp8, const uint8_t* k_fp8, int B, int H_I,
           estr, CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
     return cudaErrorInvalidValue;
-  const int64_t total_tiles = (N + kTile - 1) / kTile;
-  const int groups = (B + QG - 1) / QG;
-  const int64_t target = 3LL * device_sm_count();
-  int64_t per = (total_tiles * groups + target - 1) / target;
-  if (per < 4) per = 4;
-  if (per > total_tiles) per = total_tiles;
-  const int64_t gx = (total_tiles + per - 1) / per;
+  const int64_t T = (N + kTile - 1) / kTile;  // tiles per query group
+  const int64_t groups = (B + QG - 1) / QG;
+  const int64_t W = groups * T;                // items of the call
   // Co-resident CTAs must never need more than the SM's 512 TMEM columns (an
   // allocation would block): request enough shared memory to cap residency.
   const uint32_t cols = NB <= 16 ? 32u : (NB <= 32 ? 64u : (NB <= 64 ? 128u : (NB <= 128 ? 256u : 512u)));
   const uint32_t max_ctas = 512u / cols;
-  uint32_t smem = L::alloc;
+  uint32_t smem = L::alloc(NB);
   const uint32_t cap_smem = 232448u / max_ctas - 1024u;  // leaves room for the runtime's reservation
   if (max_ctas < 16 && smem < cap_smem) smem = cap_smem;
   cudaError_t e = cudaFuncSetAttribute(index_tc_kernel<D_I>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  index_tc_kernel<D_I><<<dim3((unsigned)gx, (unsigned)groups), kIdxThreads, smem, stream>>>(
-      map, q_fp8, B, H_I, N, kv_seq_stride, q_per_seq, QG, NB, (int)per, q_pos, ratio, scores,
-      status);
-  return cudaGetLastError();
+  // one wave: as many CTAs as fit at once, but each range within two groups
+  e = cudaFuncSetAttribute(index_tc_kernel<D_I>, cudaFuncAttributePreferredSharedMemoryCarveout,
+                           100);
+  if (e != cudaSuccess) return e;
+  int dev = 0, smem_sm = 0;
+  if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+  if ((e = cudaDeviceGetAttribute(&smem_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev)) !=
+      cudaSuccess)
+    return e;
+  int per_sm = smem_sm / (int)(smem + 1024);  // the runtime reserves 1 KiB per CTA
+  if (per_sm > 4) per_sm = 4;
+  if (per_sm < 1) per_sm = 1;
+  int64_t C = (int64_t)per_sm * device_sm_count();
+  if (C > W) C = W;
+  if (C < groups) C = groups;  // W / C <= T: no range spans more than two groups
+  return launch_kernel(index_tc_kernel<D_I>, dim3((unsigned)C), dim3(kIdxThreads), smem, stream,
+                       false, map, q_fp8, B, H_I, N, kv_seq_stride, q_per_seq, QG, NB, T, W, q_pos,
+                       ratio, scores, status);
 }
 
 }  // namespace
