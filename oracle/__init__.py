@@ -62,8 +62,9 @@ def _load():
                                                vp]),
                 "orc_sparse_attn": (None, [vp, vp, i32, i32, i32, i64, i64, i32, vp, i32, dbl,
                                            vp, vp]),
+                "orc_block_pool": (None, [vp, i32, i64, vp, i32, i32, i32, vp]),
                 "orc_layer_group": (i32, [i32, vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32,
-                                          i32, i64, i64, i32, vp, i32, i32, i32, vp, dbl]),
+                                          i32, i64, i64, i32, vp, i32, i32, i32, i32, vp, dbl]),
             }
             for name, (res, args) in sig.items():
                 f = getattr(lib, name)
@@ -149,6 +150,17 @@ def topk(scores, k: int, q_pos=None, ratio: int = 1) -> np.ndarray:
     return out
 
 
+def block_pool(scores, block: int, n_blocks: int, q_pos=None, ratio: int = 1) -> np.ndarray:
+    """Blockwise candidate pool of the Hierarchical Sparse Indexer (walkthrough
+    1.(4).2): scores [B][N] -> int32 pool [B][n_blocks * block]."""
+    scores = _c(scores, np.float64)
+    B, N = scores.shape
+    qp = None if q_pos is None else _c(q_pos, np.int32)
+    out = np.empty((B, n_blocks * block), dtype=np.int32)
+    _load().orc_block_pool(_ptr(scores), B, N, _ptr(qp), ratio, block, n_blocks, _ptr(out))
+    return out
+
+
 def hier_pool_index(q_fp8, k_fp8, N: int, kv_seq_stride: int, q_per_seq: int, pool, k: int):
     q_fp8 = _c(q_fp8, np.uint8)
     k_fp8 = _c(k_fp8, np.uint8)
@@ -179,8 +191,9 @@ def sparse_attn(q_bf16, kv_fp4, N: int, kv_seq_stride: int, q_per_seq: int, idx,
 
 def layer_group(modes: Sequence[int], q_bf16: Sequence[np.ndarray], qi_fp8: Sequence[np.ndarray],
                 kv_fp4, ki_fp8, N: int, kv_seq_stride: int, q_per_seq: int, q_pos, ratio: int,
-                k: int, pool_size: int, scale: float):
-    """Runs the layer schedule (walkthrough 1.(4).1 and 1.(4).2).
+                k: int, pool_size: int, scale: float, pool_block: int = 0):
+    """Runs the layer schedule (walkthrough 1.(4).1 and 1.(4).2).  pool_block > 0
+    builds the blockwise pool (pool_size / pool_block blocks of pool_block entries).
 
     Returns (outs, lses, idxs, pool) with one array per layer."""
     L = len(modes)
@@ -209,7 +222,7 @@ def layer_group(modes: Sequence[int], q_bf16: Sequence[np.ndarray], qi_fp8: Sequ
     rc = _load().orc_layer_group(L, modes_c, arr(q_bf16), arr(qis), arr(outs), arr(lses),
                                  arr(idxs), _ptr(kv_fp4), _ptr(ki_fp8), B, H, H_I, D, D_I, N,
                                  kv_seq_stride, q_per_seq, _ptr(qp), ratio, k, pool_size,
-                                 _ptr(pool), float(scale))
+                                 pool_block, _ptr(pool), float(scale))
     if rc != 0:
         raise ValueError("invalid layer schedule")
     return outs, lses, idxs, (pool if pool_size > 0 else None)

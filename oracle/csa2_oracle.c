@@ -51,6 +51,12 @@
  *      after RoPE).
  *  R8  a Reuse layer takes the indices of the nearest preceding Full or
  *      Reindex layer.
+ *  R9  blockwise candidate pool [P4c]: entries are cut into aligned blocks of
+ *      `block` consecutive entries; a block's score is the largest score of
+ *      its visible entries (a block without one is no candidate); the
+ *      n_blocks best blocks by (score desc, block index asc) are kept; the
+ *      pool is the visible entries of the kept blocks in ascending order,
+ *      padded with -1 to n_blocks * block slots.
  */
 #include <math.h>
 #include <stdint.h>
@@ -269,6 +275,42 @@ void orc_topk(const double* scores, int B, int64_t N, int k, const int32_t* q_po
 }
 
 /* ---------------------------------------------------------------------- */
+/* Hierarchical Sparse Indexer, blockwise candidate pool [P4c], reading R9 */
+/* ---------------------------------------------------------------------- */
+
+/* scores [B][N] -> pool [B][n_blocks * block].  The steps follow the page:
+ * block score = max of the index scores in the block, the top-scoring
+ * blocks are chosen, and the positions they cover form the pool. */
+void orc_block_pool(const double* scores, int B, int64_t N, const int32_t* q_pos, int ratio,
+                    int block, int n_blocks, int32_t* pool) {
+  int64_t nb_max = (N + block - 1) / block;
+  cand_t* c = (cand_t*)malloc(sizeof(cand_t) * (nb_max > 0 ? nb_max : 1));
+  int32_t* chosen = (int32_t*)malloc(sizeof(int32_t) * (n_blocks > 0 ? n_blocks : 1));
+  int64_t P = (int64_t)n_blocks * block;
+  for (int q = 0; q < B; ++q) {
+    int64_t nv = orc_n_visible(q_pos, q, ratio, N);
+    int64_t nb = (nv + block - 1) / block; /* blocks holding a visible entry */
+    for (int64_t b = 0; b < nb; ++b) {
+      double m = -INFINITY;
+      for (int64_t j = b * block; j < (b + 1) * block && j < nv; ++j)
+        if (scores[(int64_t)q * N + j] > m) m = scores[(int64_t)q * N + j];
+      c[b].s = m;
+      c[b].j = b;
+    }
+    select_topk(c, nb, n_blocks, chosen); /* chosen blocks, ascending, -1 padded */
+    int64_t o = 0;
+    for (int t = 0; t < n_blocks; ++t) {
+      if (chosen[t] < 0) continue;
+      for (int64_t j = (int64_t)chosen[t] * block; j < ((int64_t)chosen[t] + 1) * block && j < nv; ++j)
+        pool[(int64_t)q * P + o++] = (int32_t)j;
+    }
+    for (; o < P; ++o) pool[(int64_t)q * P + o] = -1;
+  }
+  free(c);
+  free(chosen);
+}
+
+/* ---------------------------------------------------------------------- */
 /* Hierarchical Sparse Indexer, Reindex-in-pool [P4c], reading R6          */
 /* ---------------------------------------------------------------------- */
 
@@ -371,15 +413,19 @@ enum { ORC_FULL = 0, ORC_REINDEX = 1, ORC_REUSE = 2 };
  *   qi_fp8[l]         [B][H_I][D_I] indexer query (ignored for REUSE)
  *   out[l], lse[l]    [B][H][D], [B][H] outputs (lse may be NULL)
  *   idx_out[l]        [B][k] indices layer l attended (written for every layer)
- *   pool_out          [B][pool_size] when pool_size > 0 (built by FULL layers)
+ *   pool_out          [B][pool_size] when pool_size > 0 (built by FULL layers):
+ *                     pool_block == 0: the top pool_size entries (R6);
+ *                     pool_block > 0: the blockwise pool of pool_size /
+ *                     pool_block blocks of pool_block entries (R9)
  * Returns 0, or -1 for an invalid schedule. */
 int orc_layer_group(int n_layers, const int* modes, const uint16_t* const* q_bf16,
                     const uint8_t* const* qi_fp8, double* const* out, double* const* lse,
                     int32_t* const* idx_out, const uint8_t* kv_fp4, const uint8_t* ki_fp8, int B,
                     int H, int H_I, int D, int D_I, int64_t N, int64_t kv_seq_stride,
                     int q_per_seq, const int32_t* q_pos, int ratio, int k, int pool_size,
-                    int32_t* pool_out, double scale) {
+                    int pool_block, int32_t* pool_out, double scale) {
   if (n_layers < 1 || modes[0] != ORC_FULL) return -1;
+  if (pool_block < 0 || (pool_block > 0 && pool_size % pool_block != 0)) return -1;
   double* scores = (double*)malloc(sizeof(double) * (size_t)B * (size_t)(N > 0 ? N : 1));
   const int32_t* latest = NULL;
   for (int l = 0; l < n_layers; ++l) {
@@ -388,7 +434,10 @@ int orc_layer_group(int n_layers, const int* modes, const uint16_t* const* q_bf1
       orc_index_scores(qi_fp8[l], ki_fp8, B, H_I, D_I, N, kv_seq_stride, q_per_seq, q_pos, ratio,
                        scores);
       orc_topk(scores, B, N, k, q_pos, ratio, idx);
-      if (pool_size > 0) orc_topk(scores, B, N, pool_size, q_pos, ratio, pool_out);
+      if (pool_size > 0 && pool_block == 0)
+        orc_topk(scores, B, N, pool_size, q_pos, ratio, pool_out);
+      else if (pool_size > 0)
+        orc_block_pool(scores, B, N, q_pos, ratio, pool_block, pool_size / pool_block, pool_out);
       latest = idx;
     } else if (modes[l] == ORC_REINDEX) {
       if (pool_size > 0) {

@@ -180,3 +180,20 @@ def test_schedule_must_start_with_full():
     with pytest.raises(ValueError):
         oracle.layer_group([1, 2], qs[:2], [qis[0], None], kv, ki, 200, 200, 1, None, 4, 16, 0,
                            SCALE)
+
+
+def test_blockwise_pool_schedule_selects_inside_the_pool():
+    # Full builds the blockwise pool (walkthrough 1.(4).2); Reindex layers pick
+    # their top-k among pool entries only; Reuse repeats the latest indices.
+    rng = np.random.default_rng(21)
+    B, N, k = 2, 96, 8
+    kv, ki, qs, qis = _group_inputs(rng, B, N)
+    pos = np.array([4 * N - 1, 4 * 70 + 1], np.int32)
+    outs, lses, idxs, pool = oracle.layer_group([0, 1, 2], qs, [qis[0], qis[1], None], kv, ki, N,
+                                                N, 1, pos, 4, k, 24, SCALE, pool_block=8)
+    scores = oracle.index_scores(qis[0], ki, N, N, 1, pos, 4)
+    assert np.array_equal(pool, oracle.block_pool(scores, 8, 3, pos, 4))
+    for q in range(B):
+        members = set(pool[q][pool[q] >= 0].tolist())
+        assert set(idxs[1][q][idxs[1][q] >= 0].tolist()) <= members
+    assert np.array_equal(idxs[2], idxs[1])

@@ -177,3 +177,81 @@ def test_pool_restricts_selection_and_skips_padding():
     # fewer pool entries than k: padded with -1
     got = oracle.hier_pool_index(qi, ki, N, N, 1, pool[:, :5], k)
     assert (got[:, 5:] == -1).all() and (got[:, :5] >= 0).all()
+
+
+# ---------------------------------------------------------------- blockwise pool
+
+def _golden_block_pool():
+    from conftest import golden_lines
+    scores, cases = None, []
+    for line in golden_lines("block_pool.txt"):
+        tok = line.split()
+        if tok[0] == "scores":
+            scores = np.array([float(t) for t in tok[1:]])
+        elif tok[0] == "case":
+            colon = tok.index(":")
+            cases.append((int(tok[1]), int(tok[2]), [int(t) for t in tok[colon + 1:]]))
+    return scores, cases
+
+
+def test_block_pool_matches_hand_derived_cases():
+    scores, cases = _golden_block_pool()
+    assert scores is not None and len(cases) == 4
+    for pos, nblk, want in cases:
+        got = oracle.block_pool(scores[None, :], 4, nblk, np.array([pos], np.int32), 1)
+        assert got[0].tolist() == want, (pos, nblk)
+
+
+def _check_block_pool(scores, q_pos, ratio, block, nblk, pool):
+    """Properties that fix the blockwise pool: ascending visible entries of
+    whole kept blocks, -1 only at the tail, and no unkept block beats a kept
+    one (ties: the lower block index is kept)."""
+    B, N = scores.shape
+    for q in range(B):
+        nv = oracle.n_visible(q_pos, q, ratio, N)
+        nb = -(-nv // block)
+        row = pool[q]
+        valid = row[row >= 0]
+        assert np.all(row[len(valid):] == -1), "padding only at the tail"
+        assert np.all(np.diff(valid) > 0) and (len(valid) == 0 or valid[-1] < nv)
+        kept = sorted(set((valid // block).tolist()))
+        assert len(kept) == min(nblk, nb)
+        want = [j for b in kept for j in range(b * block, min((b + 1) * block, nv))]
+        assert valid.tolist() == want, "the pool is every visible entry of the kept blocks"
+        bmax = [scores[q, b * block:min((b + 1) * block, nv)].max() for b in range(nb)]
+        for s in kept:
+            for u in set(range(nb)) - set(kept):
+                assert bmax[s] > bmax[u] or (bmax[s] == bmax[u] and s < u), (q, s, u)
+        if nv > 0:
+            assert int(np.argmax(scores[q, :nv])) // block in kept
+
+
+def test_block_pool_properties_on_random_rows_with_ties():
+    rng = np.random.default_rng(11)
+    for trial in range(60):
+        B, N = 4, int(rng.integers(1, 90))
+        block = int(rng.choice([1, 2, 3, 8]))
+        nblk = int(rng.integers(1, 12))
+        ratio = int(rng.choice([1, 4]))
+        scores = rng.integers(-3, 4, (B, N)).astype(np.float64)  # heavy ties
+        q_pos = rng.integers(-2, ratio * N + 3, B).astype(np.int32)
+        pool = oracle.block_pool(scores, block, nblk, q_pos, ratio)
+        assert pool.shape == (B, nblk * block)
+        _check_block_pool(scores, q_pos, ratio, block, nblk, pool)
+
+
+def test_block_pool_of_one_entry_blocks_is_the_flat_top_p():
+    rng = np.random.default_rng(12)
+    scores = rng.standard_normal((5, 300))
+    q_pos = np.array([1199, 800, 3, -1, 500], np.int32)
+    for P in (1, 17, 300, 400):
+        assert np.array_equal(oracle.block_pool(scores, 1, P, q_pos, 4),
+                              oracle.topk(scores, P, q_pos, 4))
+
+
+def test_block_pool_with_every_block_kept_is_every_visible_entry():
+    rng = np.random.default_rng(13)
+    scores = rng.standard_normal((3, 64))
+    pool = oracle.block_pool(scores, 8, 8, np.array([63, 40, 0], np.int32), 1)
+    for q, nv in enumerate((64, 41, 1)):
+        assert pool[q].tolist() == list(range(nv)) + [-1] * (64 - nv)
