@@ -122,6 +122,34 @@ csa2_status csa2_topk(const float* scores, int B, int64_t N, int k, const int32_
                       int ratio, int32_t* idx, void* ws, size_t ws_bytes, cudaStream_t stream);
 
 /*
+ * csa2_block_pool -- blockwise candidate pool of the Hierarchical Sparse
+ * Indexer (walkthrough 1.(4).2 "Hierarchical Sparse Indexer": the Full
+ * layer's index score of a block is the largest score among its positions,
+ * the top-scoring blocks are chosen and the positions they cover form the
+ * candidate pool that later Reindex layers score).
+ *   scores   fp32 [B][N] index scores (as csa2_index_scores writes them);
+ *            only the visible entries of each query count (q_pos, ratio as
+ *            in csa2_index_scores)
+ *   block    entries per block (>= 1): aligned runs [block*b, block*b+block)
+ *   n_blocks blocks kept per query (>= 1), ranked by (block score desc,
+ *            block index asc); a block without a visible entry is no candidate
+ *   pool     int32 [B][n_blocks * block]: the visible entries of the kept
+ *            blocks in ascending order, padded with -1 (the layout
+ *            csa2_hier_pool_index takes).  Bit-exact.
+ *   ws       device scratch, at least
+ *            csa2_block_pool_workspace_size(B, N, block, n_blocks) bytes,
+ *            owned by the caller; contents need no initialisation.
+ * Returns CSA2_ERR_INVALID_ARG for negative sizes, block or n_blocks < 1 or
+ * missing pointers, CSA2_ERR_WORKSPACE for a short workspace.
+ */
+csa2_status csa2_block_pool(const float* scores, int B, int64_t N, const int32_t* q_pos,
+                            int ratio, int block, int n_blocks, int32_t* pool, void* ws,
+                            size_t ws_bytes, cudaStream_t stream);
+
+/* Scratch bytes csa2_block_pool needs for these dimensions. */
+size_t csa2_block_pool_workspace_size(int B, int64_t N, int block, int n_blocks);
+
+/*
  * csa2_hier_pool_index -- a Reindex layer of the Hierarchical Sparse Indexer
  * (walkthrough 1.(4).2): scores only the candidate-pool entries with this
  * layer's indexer q and keeps its own top-k inside the pool.
@@ -209,17 +237,20 @@ typedef struct csa2_group_args {
   const int32_t* q_pos;    /* [B] or NULL */
   int ratio;
   int k;
-  int pool_size;           /* 0: flat indexer; P > 0: FULL layers build a top-P pool and
+  int pool_size;           /* 0: flat indexer; P > 0: FULL layers build a P-entry pool and
                               REINDEX layers select inside it (walkthrough 1.(4).2) */
   int32_t* pool_out;       /* int32 [B][pool_size] when pool_size > 0 */
   float softmax_scale;
+  int pool_block;          /* how FULL layers build the pool: 0 or 1: the top pool_size
+                              entries; b > 1: the blockwise pool of pool_size / b blocks
+                              of b entries (csa2_block_pool; pool_size % b == 0) */
 } csa2_group_args;
 
 /*
  * csa2_layer_group -- runs a static schedule of CSA2 layers over one shared
  * FP4 main KV and indexer K (walkthrough 1.(4).1, 1.(4).2):
  *   FULL    scores all visible entries with its own indexer q, takes top-k
- *           (and the top-pool_size pool when pool_size > 0), attends;
+ *           (and builds the pool when pool_size > 0: see pool_block), attends;
  *   REINDEX re-scores the shared indexer K (only the pool when pool_size > 0)
  *           with its own indexer q, takes top-k, attends;
  *   REUSE   attends with the indices of the nearest preceding FULL/REINDEX.

@@ -56,7 +56,7 @@ class Csa2GroupArgs(ctypes.Structure):
                 ("N", ctypes.c_int64), ("kv_seq_stride", ctypes.c_int64),
                 ("q_per_seq", ctypes.c_int), ("q_pos", _vp), ("ratio", ctypes.c_int),
                 ("k", ctypes.c_int), ("pool_size", ctypes.c_int), ("pool_out", _vp),
-                ("softmax_scale", ctypes.c_float)]
+                ("softmax_scale", ctypes.c_float), ("pool_block", ctypes.c_int)]
 
 
 _SIGS = {
@@ -67,6 +67,8 @@ _SIGS = {
     "csa2_index_scores": (_i32, [_vp, _vp, _i32, _i32, _i32, _i64, _i64, _i32, _vp, _i32, _vp,
                                  _vp]),
     "csa2_topk": (_i32, [_vp, _i32, _i64, _i32, _vp, _i32, _vp, _vp, _sz, _vp]),
+    "csa2_block_pool": (_i32, [_vp, _i32, _i64, _vp, _i32, _i32, _i32, _vp, _vp, _sz, _vp]),
+    "csa2_block_pool_workspace_size": (_sz, [_i32, _i64, _i32, _i32]),
     "csa2_hier_pool_index": (_i32, [_vp, _vp, _i32, _i32, _i32, _i64, _i64, _i32, _vp, _i32,
                                     _i32, _vp, _vp, _sz, _vp]),
     "csa2_sparse_attn_fp4": (_i32, [_vp, _vp, _i32, _i32, _i32, _i64, _i64, _i32, _vp, _i32,
@@ -215,6 +217,24 @@ def hier_pool_index(q_fp8: torch.Tensor, k_fp8: torch.Tensor, N: int, kv_seq_str
     return out
 
 
+def block_pool(scores: torch.Tensor, block: int, n_blocks: int,
+               q_pos: Optional[torch.Tensor] = None, ratio: int = 1,
+               ws: Optional[torch.Tensor] = None, out: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """Blockwise candidate pool: fp32 scores [B][N] -> int32 pool [B][n_blocks * block]."""
+    scores = _dev(scores, torch.float32, "scores")
+    B, N = scores.shape
+    qp = _opt_pos(q_pos)
+    if ws is None:
+        n = max(int(lib.csa2_block_pool_workspace_size(B, N, block, n_blocks)), 256)
+        ws = torch.empty(n, dtype=torch.uint8, device=scores.device)
+    if out is None:
+        out = torch.empty((B, n_blocks * block), dtype=torch.int32, device=scores.device)
+    _dev(out, torch.int32, "pool")
+    _check(lib.csa2_block_pool(_ptr(scores), B, N, _ptr(qp), ratio, block, n_blocks, _ptr(out),
+                               _ptr(ws), ws.numel(), _stream()), "csa2_block_pool")
+    return out
+
+
 def sparse_attn_fp4(q_bf16: torch.Tensor, kv_fp4: torch.Tensor, N: int, kv_seq_stride: int,
                     q_per_seq: int, idx: torch.Tensor, softmax_scale: Optional[float] = None,
                     out: Optional[torch.Tensor] = None, lse: Optional[torch.Tensor] = None,
@@ -250,7 +270,7 @@ class LayerGroup:
                  ki_fp8: torch.Tensor, N: int, kv_seq_stride: int, q_per_seq: int,
                  q_pos: Optional[torch.Tensor], ratio: int, k: int, pool_size: int = 0,
                  softmax_scale: Optional[float] = None, want_lse: bool = True,
-                 reuse_idx_copy: bool = True):
+                 reuse_idx_copy: bool = True, pool_block: int = 0):
         L = len(modes)
         self.modes = list(modes)
         self.q = [_bits16(q, f"q_bf16[{l}]") for l, q in enumerate(q_bf16)]
@@ -282,7 +302,7 @@ class LayerGroup:
                                         _ptr(self.out[l]), _ptr(self.lse[l]), _ptr(self.idx[l]))
         self._args = Csa2GroupArgs(_ptr(self.kv), _ptr(self.ki), B, H, H_I, D, D_I, N,
                                    kv_seq_stride, q_per_seq, _ptr(self.q_pos), ratio, k,
-                                   pool_size, _ptr(self.pool), softmax_scale)
+                                   pool_size, _ptr(self.pool), softmax_scale, pool_block)
 
     def __call__(self):
         _check(lib.csa2_layer_group(self._layers, len(self.modes), ctypes.byref(self._args),
@@ -298,7 +318,7 @@ def group_launches(group: LayerGroup) -> int:
 
 
 def layer_group(modes, q_bf16, qi_fp8, kv_fp4, ki_fp8, N, kv_seq_stride, q_per_seq, q_pos, ratio,
-                k, pool_size=0, softmax_scale=None):
+                k, pool_size=0, softmax_scale=None, pool_block=0):
     """One-shot csa2_layer_group; returns (outs, lses, idxs, pool)."""
     return LayerGroup(modes, q_bf16, qi_fp8, kv_fp4, ki_fp8, N, kv_seq_stride, q_per_seq, q_pos,
-                      ratio, k, pool_size, softmax_scale)()
+                      ratio, k, pool_size, softmax_scale, pool_block=pool_block)()

@@ -24,6 +24,7 @@ struct WsLayout {
   size_t scores = 0;       // [B][N] fp32
   size_t pool_scores = 0;  // [B][P] fp32
   size_t attn = 0;         // attention partials
+  size_t bpool = 0;        // blockwise-pool scratch (blocks of 2 or more entries)
   size_t total = 0;
 };
 
@@ -36,6 +37,8 @@ WsLayout layout(int B, int64_t N, int k, int H, int P) {
   off += align_up((size_t)(B > 0 ? B : 0) * (size_t)(P > 0 ? P : 0) * 4, 256);
   w.attn = off;
   off += attn_scratch_bytes(B, H, k);
+  w.bpool = off;
+  if (P > 0) off += block_pool_scratch_bytes(B, N, 2, P / 2 > 0 ? P / 2 : 1);
   w.total = off;
   return w;
 }
@@ -155,6 +158,23 @@ csa2_status csa2_topk(const float* scores, int B, int64_t N, int k, const int32_
   return check_launch(launch_topk(scores, B, N, k, q_pos, ratio, nullptr, nullptr, idx, stream));
 }
 
+size_t csa2_block_pool_workspace_size(int B, int64_t N, int block, int n_blocks) {
+  return block_pool_scratch_bytes(B, N, block, n_blocks);
+}
+
+csa2_status csa2_block_pool(const float* scores, int B, int64_t N, const int32_t* q_pos,
+                            int ratio, int block, int n_blocks, int32_t* pool, void* ws,
+                            size_t ws_bytes, cudaStream_t stream) {
+  if (B < 0 || N < 0 || N > INT32_MAX - 1 || ratio < 1 || block < 1 || n_blocks < 1)
+    return CSA2_ERR_INVALID_ARG;
+  if ((int64_t)n_blocks * block > INT32_MAX) return CSA2_ERR_INVALID_ARG;
+  if (B > 0 && (!pool || (N > 0 && !scores))) return CSA2_ERR_INVALID_ARG;
+  if (B == 0) return CSA2_OK;
+  if (!ws || ws_bytes < block_pool_scratch_bytes(B, N, block, n_blocks)) return CSA2_ERR_WORKSPACE;
+  return check_launch(
+      launch_block_pool(scores, B, N, q_pos, ratio, block, n_blocks, pool, ws, stream, false));
+}
+
 csa2_status csa2_hier_pool_index(const uint8_t* q_fp8, const uint8_t* k_fp8, int B, int H_I,
                                  int D_I, int64_t N, int64_t kv_seq_stride, int q_per_seq,
                                  const int32_t* pool, int P, int k, int32_t* idx, void* ws,
@@ -197,7 +217,7 @@ int csa2_layer_group_launches(const csa2_layer* layers, int n_layers, const csa2
   int n = 0;
   for (int l = 0; l < n_layers; ++l) {
     const int m = layers[l].mode;
-    if (m == CSA2_FULL) n += 2 + (g->pool_size > 0 ? 1 : 0);
+    if (m == CSA2_FULL) n += 2 + (g->pool_size > 0 ? (g->pool_block > 1 ? 3 : 1) : 0);
     else if (m == CSA2_REINDEX) n += 2;
     else if (m != CSA2_REUSE) return -1;
     n += attn_launches(g->B, g->k);
@@ -214,6 +234,8 @@ csa2_status csa2_layer_group(const csa2_layer* layers, int n_layers, const csa2_
   if (g->pool_size < 0) return CSA2_ERR_INVALID_ARG;
   if (g->pool_size > 0 && g->B > 0 && !g->pool_out) return CSA2_ERR_INVALID_ARG;
   if (g->pool_size > 0 && g->pool_size < g->k) return CSA2_ERR_INVALID_ARG;
+  if (g->pool_block < 0 || (g->pool_block > 1 && g->pool_size % g->pool_block != 0))
+    return CSA2_ERR_INVALID_ARG;
   // validate every layer before launching anything
   for (int l = 0; l < n_layers; ++l) {
     const csa2_layer& L = layers[l];
@@ -245,9 +267,15 @@ csa2_status csa2_layer_group(const csa2_layer* layers, int n_layers, const csa2_
     if (L.mode == CSA2_FULL || (L.mode == CSA2_REINDEX && g->pool_size == 0)) {
       e = launch_index_scores(L.qi_fp8, g->ki_fp8, g->B, g->H_I, g->D_I, g->N, g->kv_seq_stride,
                               g->q_per_seq, g->q_pos, g->ratio, scores, status, stream);
-      if (e == cudaSuccess && L.mode == CSA2_FULL && g->pool_size > 0)
-        e = launch_topk(scores, g->B, g->N, g->pool_size, g->q_pos, g->ratio, nullptr, nullptr,
-                        g->pool_out, stream, /*pdl=*/true);
+      if (e == cudaSuccess && L.mode == CSA2_FULL && g->pool_size > 0) {
+        if (g->pool_block > 1)  // blockwise pool (a one-entry block pool is the flat one)
+          e = launch_block_pool(scores, g->B, g->N, g->q_pos, g->ratio, g->pool_block,
+                                g->pool_size / g->pool_block, g->pool_out, wsb + w.bpool, stream,
+                                /*pdl=*/true);
+        else
+          e = launch_topk(scores, g->B, g->N, g->pool_size, g->q_pos, g->ratio, nullptr, nullptr,
+                          g->pool_out, stream, /*pdl=*/true);
+      }
       if (e == cudaSuccess)
         e = launch_topk(scores, g->B, g->N, g->k, g->q_pos, g->ratio, nullptr, nullptr, L.idx_out,
                         stream, /*pdl=*/true);

@@ -140,6 +140,21 @@ cudaError_t launch_topk(const float* scores, int B, int64_t N, int k, const int3
                         int ratio, const int32_t* n_valid, const int32_t* map, int32_t* idx,
                         cudaStream_t stream, bool pdl = false);
 
+// Blockwise candidate pool of the Hierarchical Sparse Indexer: scores [B][N]
+// -> pool [B][n_blocks * block] (ascending entries of the kept blocks, -1
+// padded).  scratch: block_pool_scratch(...).bytes bytes.
+struct BlockPoolScratch {
+  float* bscores;    // [B][ceil(N / block)]
+  int32_t* n_valid;  // [B] blocks holding a visible entry
+  int32_t* blk;      // [B][n_blocks] kept blocks
+  size_t bytes;
+};
+BlockPoolScratch block_pool_scratch(void* base, int B, int64_t N, int block, int n_blocks);
+size_t block_pool_scratch_bytes(int B, int64_t N, int block, int n_blocks);
+cudaError_t launch_block_pool(const float* scores, int B, int64_t N, const int32_t* q_pos,
+                              int ratio, int block, int n_blocks, int32_t* pool, void* scratch,
+                              cudaStream_t stream, bool pdl);
+
 // Sparse attention.  scratch: partial outputs when split over several CTAs.
 size_t attn_scratch_bytes(int B, int H, int k);
 int attn_launches(int B, int k);  // kernels one sparse-attention call launches

@@ -151,6 +151,7 @@ class Workload:
     first_pos: Optional[int] = None      # position of query 0 of each sequence (None: last token)
     modes: Sequence[int] = (FULL,)
     pool: int = 0          # hierarchical candidate pool size (0 = flat indexer)
+    pool_block: int = 0    # > 1: blockwise pool of pool / pool_block blocks (else top-pool)
     float_indexer: bool = False          # bf16 N(0,1) indexer inputs instead of integers
 
     @property
@@ -259,7 +260,13 @@ GROUP_128K = Workload("group_full_reindex_reuse_b64_ctx128k", 3, B=64, N=32768, 
 HIER_1M = Workload("hier_pool8192_b16_ctx1m", 4, B=16, N=262144, H=64, H_I=8, k=2048,
                    seeds=tuple(_seeds(4000, 16)), modes=(FULL, REINDEX, REINDEX, REINDEX),
                    pool=8192)
+# The pages' own candidate pool: at most 2048 blocks of 8 positions (16384
+# candidates), block score = max index score in the block.
+HIER_BLOCK_1M = Workload("hier_block2048x8_b16_ctx1m", 6, B=16, N=262144, H=64, H_I=8, k=2048,
+                         seeds=tuple(_seeds(6000, 16)), modes=(FULL, REINDEX, REINDEX, REINDEX),
+                         pool=16384, pool_block=8)
 PREFILL_128K = Workload("prefill_4096q_ctx128k", 5, B=4096, N=32768, H=64, H_I=8, k=2048,
                         q_per_seq=4096, seeds=(5000,), first_pos=126976, float_indexer=True)
 
-WORKLOADS = {w.name: w for w in (TINY_FULL, DECODE_64K, GROUP_128K, HIER_1M, PREFILL_128K)}
+WORKLOADS = {w.name: w for w in (TINY_FULL, DECODE_64K, GROUP_128K, HIER_1M, PREFILL_128K,
+                                  HIER_BLOCK_1M)}

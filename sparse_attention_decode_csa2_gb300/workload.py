@@ -33,7 +33,7 @@ class DeviceInputs:
         w = self.w
         return csa2.LayerGroup(w.modes, self.q, self.qi, self.kv_fp4, self.ki_fp8, w.N,
                                w.kv_seq_stride, w.q_per_seq, self.q_pos, w.ratio, w.k, w.pool,
-                               self.scale, **kw)
+                               self.scale, pool_block=w.pool_block, **kw)
 
 
 def _to_dev(a: np.ndarray, device, dtype=None) -> torch.Tensor:

@@ -248,6 +248,47 @@ def test_attention_out_of_range_index_sets_status_and_is_skipped(C):
     assert_attn_close(out.cpu().numpy(), ref_o)
 
 
+# ---------------------------------------------------------------- blockwise pool
+
+@pytest.mark.parametrize("B,N,block,nblk,ties", [(3, 1000, 8, 20, False), (4, 4096, 8, 64, True),
+                                                (2, 777, 3, 300, True), (5, 70000, 8, 2048, False),
+                                                (2, 262144, 8, 2048, True), (3, 129, 1, 40, True)])
+def test_block_pool_bit_exact(C, B, N, block, nblk, ties):
+    # walkthrough 1.(4).2: block score = max over its visible entries, top
+    # blocks by (score desc, block asc), pool = their visible entries, -1 padded
+    rng = np.random.default_rng(B * 1000 + block + nblk)
+    if ties:
+        scores = rng.integers(-40, 41, (B, N)).astype(np.float32)
+    else:
+        scores = rng.standard_normal((B, N)).astype(np.float32)
+    ratio = 4
+    pos = rng.integers(-2, ratio * N + 5, B).astype(np.int32)
+    pos[0] = ratio * N - 1            # everything visible
+    if B > 2:
+        pos[1] = ratio * 5 + 2        # 5 visible entries: fewer blocks than asked
+    got = C.block_pool(cuda(scores), block, nblk, cuda(pos), ratio).cpu().numpy()
+    want = oracle.block_pool(scores.astype(np.float64), block, nblk, pos, ratio)
+    assert np.array_equal(got, want)
+
+
+def test_layer_group_with_blockwise_pool_matches_oracle(C):
+    rng = np.random.default_rng(77)
+    modes = (0, 1, 2, 1)
+    B, N, H, H_I, k = 3, 6000, 64, 8, 256
+    kv, ki, qs, qis, pos = _group(rng, B, N, H, H_I, k, modes, 0)
+    outs, lses, idxs, gpool = C.layer_group(modes, [cuda(q, torch.int16) for q in qs],
+                                            [None if qi is None else cuda(qi) for qi in qis],
+                                            cuda(kv), cuda(ki), N, N, 1, cuda(pos), 4, k, 1024,
+                                            SCALE, pool_block=8)
+    r_outs, r_lses, r_idxs, r_pool = oracle.layer_group(modes, qs, qis, kv, ki, N, N, 1, pos, 4,
+                                                        k, 1024, SCALE, pool_block=8)
+    assert (gpool.cpu().numpy() == r_pool).all()
+    for l in range(len(modes)):
+        assert (idxs[l].cpu().numpy() == r_idxs[l]).all(), l
+        assert_attn_close(outs[l].cpu().numpy(), r_outs[l], l)
+        assert_lse_close(lses[l].cpu().numpy(), r_lses[l])
+
+
 # ---------------------------------------------------------------- layer group
 
 def _group(rng, B, N, H, H_I, k, layers, pool, ratio=4):

@@ -1,4 +1,4 @@
-"""Parity of the whole CSA2 path at the five workloads' full sizes, in the
+"""Parity of the whole CSA2 path at the six workloads' full sizes, in the
 launch configuration the benchmark times (csa2_layer_group over the
 device-resident cache).  The oracle recomputes sampled queries one by one:
 their FP4 rows (from the same seeded latent), indexer scores, top-k / pool
@@ -13,7 +13,7 @@ from helpers import assert_attn_close, assert_float_selection_ok, assert_lse_clo
 pytestmark = pytest.mark.gpu
 
 NAMES = ["tiny_full_1q_ctx4k", "decode_b32_ctx64k", "group_full_reindex_reuse_b64_ctx128k",
-         "hier_pool8192_b16_ctx1m", "prefill_4096q_ctx128k"]
+         "hier_pool8192_b16_ctx1m", "prefill_4096q_ctx128k", "hier_block2048x8_b16_ctx1m"]
 
 
 def _sample(B, n):
@@ -37,7 +37,7 @@ def test_workload_parity(name):
     code, bits = csa2.read_status(lg.ws)
     assert code == 0, bits
     pos = w.q_pos()
-    n_samples = {1: 1, 2: 4, 3: 3, 4: 3, 5: 6}[w.workload_id]
+    n_samples = {1: 1, 2: 4, 3: 3, 4: 3, 5: 6, 6: 3}[w.workload_id]
     for q in _sample(w.B, n_samples):
         s = q // w.q_per_seq
         ki = w.ki_fp8(s)
@@ -58,7 +58,11 @@ def test_workload_parity(name):
                     sc = oracle.index_scores(qi, ki, w.N, 0, 1, qpos, w.ratio)
                     ref_idx = oracle.topk(sc, w.k, qpos, w.ratio)[0]
                     if w.pool and l == 0:
-                        opool = oracle.topk(sc, w.pool, qpos, w.ratio)
+                        if w.pool_block > 1:
+                            opool = oracle.block_pool(sc, w.pool_block, w.pool // w.pool_block,
+                                                      qpos, w.ratio)
+                        else:
+                            opool = oracle.topk(sc, w.pool, qpos, w.ratio)
                         assert (pool[q].cpu().numpy() == opool[0]).all(), (name, q)
                     if w.float_indexer:
                         assert_float_selection_ok(got_idx, ref_idx, sc[0], (name, q, l))
