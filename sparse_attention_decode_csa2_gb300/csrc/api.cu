@@ -25,6 +25,8 @@ struct WsLayout {
   size_t pool_scores = 0;  // [B][P] fp32
   size_t attn = 0;         // attention partials
   size_t bpool = 0;        // blockwise-pool scratch (blocks of 2 or more entries)
+  size_t topk = 0;         // chunked selection of rows longer than 32768 entries
+  size_t topk_bytes = 0;
   size_t total = 0;
 };
 
@@ -39,6 +41,10 @@ WsLayout layout(int B, int64_t N, int k, int H, int P) {
   off += attn_scratch_bytes(B, H, k);
   w.bpool = off;
   if (P > 0) off += block_pool_scratch_bytes(B, N, 2, P / 2 > 0 ? P / 2 : 1);
+  w.topk = off;
+  w.topk_bytes = topk_scratch_bytes(B, N, k);
+  if (P > 0 && topk_scratch_bytes(B, N, P) > w.topk_bytes) w.topk_bytes = topk_scratch_bytes(B, N, P);
+  off += w.topk_bytes;
   w.total = off;
   return w;
 }
@@ -155,7 +161,13 @@ csa2_status csa2_topk(const float* scores, int B, int64_t N, int k, const int32_
   if (B < 0 || N < 0 || N > INT32_MAX - 1 || k < 1 || ratio < 1) return CSA2_ERR_INVALID_ARG;
   if (B > 0 && (!idx || (N > 0 && !scores))) return CSA2_ERR_INVALID_ARG;
   if (!ws || ws_bytes < kStatusBytes) return CSA2_ERR_WORKSPACE;
-  return check_launch(launch_topk(scores, B, N, k, q_pos, ratio, nullptr, nullptr, idx, stream));
+  // a workspace of csa2_workspace_size(B, N, k, 0, 0) bytes enables the
+  // chunked selection of long rows; a smaller one falls back to one kernel
+  const WsLayout w = layout(B, N, k, 0, 0);
+  uint8_t* wsb = reinterpret_cast<uint8_t*>(ws);
+  const bool room = ws_bytes >= w.total;
+  return check_launch(launch_topk(scores, B, N, k, q_pos, ratio, nullptr, nullptr, idx, stream,
+                                  false, room ? wsb + w.topk : nullptr, room ? w.topk_bytes : 0));
 }
 
 size_t csa2_block_pool_workspace_size(int B, int64_t N, int block, int n_blocks) {
@@ -217,7 +229,11 @@ int csa2_layer_group_launches(const csa2_layer* layers, int n_layers, const csa2
   int n = 0;
   for (int l = 0; l < n_layers; ++l) {
     const int m = layers[l].mode;
-    if (m == CSA2_FULL) n += 2 + (g->pool_size > 0 ? (g->pool_block > 1 ? 3 : 1) : 0);
+    if (m == CSA2_FULL)
+      n += 1 + topk_launches(g->B, g->N, g->k, (size_t)-1) +
+           (g->pool_size > 0 ? (g->pool_block > 1 ? 3 : topk_launches(g->B, g->N, g->pool_size,
+                                                                        (size_t)-1))
+                             : 0);
     else if (m == CSA2_REINDEX) n += 2;
     else if (m != CSA2_REUSE) return -1;
     n += attn_launches(g->B, g->k);
@@ -274,11 +290,11 @@ csa2_status csa2_layer_group(const csa2_layer* layers, int n_layers, const csa2_
                                 /*pdl=*/true);
         else
           e = launch_topk(scores, g->B, g->N, g->pool_size, g->q_pos, g->ratio, nullptr, nullptr,
-                          g->pool_out, stream, /*pdl=*/true);
+                          g->pool_out, stream, /*pdl=*/true, wsb + w.topk, w.topk_bytes);
       }
       if (e == cudaSuccess)
         e = launch_topk(scores, g->B, g->N, g->k, g->q_pos, g->ratio, nullptr, nullptr, L.idx_out,
-                        stream, /*pdl=*/true);
+                        stream, /*pdl=*/true, wsb + w.topk, w.topk_bytes);
       use = L.idx_out;
     } else if (L.mode == CSA2_REINDEX) {
       e = launch_pool_scores(L.qi_fp8, g->ki_fp8, g->B, g->H_I, g->D_I, g->N, g->kv_seq_stride,

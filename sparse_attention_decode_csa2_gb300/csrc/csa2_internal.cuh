@@ -136,9 +136,15 @@ cudaError_t launch_pool_scores(const uint8_t* q_fp8, const uint8_t* k_fp8, int B
 // n_visible(q_pos, b, ratio, N) when n_valid is null, else n_valid[b].  When
 // `map` is non-null the selected position p is written as map[b*N + p].
 // pdl: launched as a programmatic dependent of the kernel before it.
+// Rows longer than 32768 entries are selected in three launches when
+// `scratch` holds topk_scratch_bytes(B, N, k) bytes, else by one slower
+// kernel.
 cudaError_t launch_topk(const float* scores, int B, int64_t N, int k, const int32_t* q_pos,
                         int ratio, const int32_t* n_valid, const int32_t* map, int32_t* idx,
-                        cudaStream_t stream, bool pdl = false);
+                        cudaStream_t stream, bool pdl = false, void* scratch = nullptr,
+                        size_t scratch_bytes = 0);
+size_t topk_scratch_bytes(int B, int64_t N, int k);
+int topk_launches(int B, int64_t N, int k, size_t scratch_bytes);
 
 // Blockwise candidate pool of the Hierarchical Sparse Indexer: scores [B][N]
 // -> pool [B][n_blocks * block] (ascending entries of the kept blocks, -1

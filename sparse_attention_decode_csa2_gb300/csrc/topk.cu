@@ -154,11 +154,15 @@ __device__ __forceinline__ int select_digit(const int32_t* csum, int need, int* 
   return 255 - t;
 }
 
+// chunk == 0: CTA b selects row b.  chunk > 0 (map must be null): CTA (c, b)
+// selects among the candidates [c*chunk, (c+1)*chunk) of row b and writes
+// their positions in the row to idx[b][c][0..k) (one level of the long-row
+// selection).
 template <int KPT>
 __global__ void __launch_bounds__(kRegThreads, 1)
 topk_reg_kernel(const float* __restrict__ scores, int64_t N, int k,
                 const int32_t* __restrict__ q_pos, int ratio, const int32_t* __restrict__ n_valid,
-                const int32_t* __restrict__ map, int32_t* __restrict__ idx) {
+                const int32_t* __restrict__ map, int32_t* __restrict__ idx, int chunk) {
   // two sets of per-warp 8-bit digit histograms: one is counted into while
   // the other is cleared for the next pass; reused to stage the output
   __shared__ __align__(16) int32_t whist[2][kRegWarps * 256];
@@ -168,11 +172,12 @@ topk_reg_kernel(const float* __restrict__ scores, int64_t N, int k,
 
   pdl_trigger();
   pdl_wait();  // scores, n_valid and map come from the kernel before
-  const int b = blockIdx.x;
+  const int b = chunk ? blockIdx.y : blockIdx.x;
+  const int64_t pos0 = chunk ? (int64_t)blockIdx.x * chunk : 0;  // first entry of the chunk
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const float* row = scores + (int64_t)b * N;
+  const float* row = scores + (int64_t)b * N + pos0;
   const int32_t* mrow = map ? map + (int64_t)b * N : nullptr;
-  int32_t* out = idx + (int64_t)b * k;
+  int32_t* out = idx + ((int64_t)b * (chunk ? gridDim.x : 1) + (chunk ? blockIdx.x : 0)) * k;
 
   int n;
   if (map) {
@@ -186,8 +191,10 @@ topk_reg_kernel(const float* __restrict__ scores, int64_t N, int k,
   } else {
     n = (int)n_visible(q_pos, b, ratio, N);
   }
+  if (chunk) n = (int)max((int64_t)0, min((int64_t)chunk, (int64_t)n - pos0));
   if (n <= k) {
-    for (int j = tid; j < k; j += kRegThreads) out[j] = (j < n) ? (mrow ? mrow[j] : j) : -1;
+    for (int j = tid; j < k; j += kRegThreads)
+      out[j] = (j < n) ? (mrow ? mrow[j] : (int32_t)(pos0 + j)) : -1;
     return;
   }
 
@@ -339,7 +346,7 @@ topk_reg_kernel(const float* __restrict__ scores, int64_t N, int k,
       if (staged)
         stage[off] = p;
       else
-        out[off] = mrow ? mrow[p] : p;
+        out[off] = mrow ? mrow[p] : (int32_t)(pos0 + p);
       ++off;
     }
   }
@@ -347,7 +354,7 @@ topk_reg_kernel(const float* __restrict__ scores, int64_t N, int k,
     __syncthreads();
     for (int j = tid; j < k; j += kRegThreads) {
       const int32_t p = stage[j];
-      out[j] = mrow ? mrow[p] : p;
+      out[j] = mrow ? mrow[p] : (int32_t)(pos0 + p);
     }
   }
 }
@@ -496,27 +503,165 @@ topk_long_kernel(const float* __restrict__ scores, int64_t N, int k, const int32
 
 }  // namespace
 
+namespace {
+
+// One level of the long-row selection, second half: the chunks' selections
+// (each a valid prefix of k positions, -1 after) are packed in chunk order --
+// so in ascending position order -- with their scores and entry ids
+// (ids_in[pos], or pos itself at the first level); slots past the packed
+// count get id -1.  count[b] = packed candidates of row b.
+__global__ void __launch_bounds__(256)
+topk_pack_kernel(const float* __restrict__ scores, int64_t M_in, const int32_t* __restrict__ ids_in,
+                 const int32_t* __restrict__ sel, int C, int k, float* __restrict__ score_out,
+                 int32_t* __restrict__ id_out, int32_t* __restrict__ count) {
+  pdl_trigger();
+  pdl_wait();  // the chunk selections come from the kernel before
+  __shared__ int32_t off[65];
+  const int b = blockIdx.x;
+  const int32_t* s = sel + (int64_t)b * C * k;
+  if (threadIdx.x < C) {
+    // valid prefix length of chunk c: binary search for the first -1
+    const int32_t* sc = s + (int64_t)threadIdx.x * k;
+    int lo = 0, hi = k;
+    while (lo < hi) {
+      const int mid = (lo + hi) >> 1;
+      if (sc[mid] >= 0) lo = mid + 1; else hi = mid;
+    }
+    off[threadIdx.x + 1] = lo;
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    off[0] = 0;
+    for (int c = 0; c < C; ++c) off[c + 1] += off[c];
+    count[b] = off[C];
+  }
+  __syncthreads();
+  const int M = C * k;
+  float* so = score_out + (int64_t)b * M;
+  int32_t* io = id_out + (int64_t)b * M;
+  for (int j = threadIdx.x; j < M; j += blockDim.x) {
+    const int c = j / k, t = j % k;
+    if (t < off[c + 1] - off[c]) {
+      const int32_t pos = s[j];
+      so[off[c] + t] = scores[(int64_t)b * M_in + pos];
+      io[off[c] + t] = ids_in ? ids_in[(int64_t)b * M_in + pos] : pos;
+    }
+    if (j >= off[C]) io[j] = -1;
+  }
+}
+
+// Rows longer than one register CTA holds are cut into chunks of kRegMaxKeys
+// entries: every member of the row's top-k is in its chunk's top-k (the
+// ranking inside a chunk is the row's ranking), so the top-k of the union of
+// the chunk selections, taken in entry order, is the row's top-k.  Levels
+// repeat until the union fits one CTA (each shrinks the row by at least
+// kRegMaxKeys / k >= 2 for k <= 16384).
+int long_chunks(int64_t N) { return (int)((N + kRegMaxKeys - 1) / kRegMaxKeys); }
+bool chunked_ok(int64_t N, int k) {
+  return N > kRegMaxKeys && long_chunks(N) <= 64 && k <= kRegMaxKeys / 2;
+}
+
+template <int KPT>
+cudaError_t launch_reg(dim3 grid, const float* scores, int64_t N, int k, const int32_t* q_pos,
+                       int ratio, const int32_t* n_valid, const int32_t* map, int32_t* idx,
+                       int chunk, cudaStream_t stream, bool pdl) {
+  return launch_kernel(topk_reg_kernel<KPT>, grid, dim3(kRegThreads), 0, stream, pdl, scores, N, k,
+                       q_pos, ratio, n_valid, map, idx, chunk);
+}
+
+cudaError_t launch_reg_any(dim3 grid, const float* scores, int64_t N, int64_t keys, int k,
+                           const int32_t* q_pos, int ratio, const int32_t* n_valid,
+                           const int32_t* map, int32_t* idx, int chunk, cudaStream_t stream,
+                           bool pdl) {
+  if (keys <= kRegThreads * 8)
+    return launch_reg<8>(grid, scores, N, k, q_pos, ratio, n_valid, map, idx, chunk, stream, pdl);
+  if (keys <= kRegThreads * 16)
+    return launch_reg<16>(grid, scores, N, k, q_pos, ratio, n_valid, map, idx, chunk, stream, pdl);
+  if (keys <= kRegThreads * 32)
+    return launch_reg<32>(grid, scores, N, k, q_pos, ratio, n_valid, map, idx, chunk, stream, pdl);
+  return launch_reg<64>(grid, scores, N, k, q_pos, ratio, n_valid, map, idx, chunk, stream, pdl);
+}
+
+struct LongScratch {
+  int32_t* sel;        // [B][C1 * k] chunk selections
+  float* score[2];     // ping-pong packed candidates
+  int32_t* id[2];
+  int32_t* count[2];   // [B]
+};
+
+size_t long_scratch(void* base, int B, int64_t N, int k, LongScratch* ls) {
+  const size_t M = (size_t)long_chunks(N) * k;
+  const size_t a = align_up((size_t)B * M * 4, 256), c = align_up((size_t)B * 4, 256);
+  if (ls) {
+    uint8_t* p = reinterpret_cast<uint8_t*>(base);
+    ls->sel = reinterpret_cast<int32_t*>(p);
+    for (int i = 0; i < 2; ++i) {
+      ls->score[i] = reinterpret_cast<float*>(p + a + i * (2 * a + c));
+      ls->id[i] = reinterpret_cast<int32_t*>(p + 2 * a + i * (2 * a + c));
+      ls->count[i] = reinterpret_cast<int32_t*>(p + 3 * a + i * (2 * a + c));
+    }
+  }
+  return a + 2 * (2 * a + c);
+}
+
+}  // namespace
+
+size_t topk_scratch_bytes(int B, int64_t N, int k) {
+  if (B <= 0 || k < 1 || !chunked_ok(N, k)) return 0;
+  return long_scratch(nullptr, B, N, k, nullptr);
+}
+
+int topk_launches(int B, int64_t N, int k, size_t scratch_bytes) {
+  if (B <= 0) return 0;
+  const size_t need = topk_scratch_bytes(B, N, k);
+  if (need == 0 || scratch_bytes < need) return 1;
+  int n = 1;
+  for (int64_t M = N; M > kRegMaxKeys; M = (int64_t)long_chunks(M) * k) n += 2;
+  return n;
+}
+
 cudaError_t launch_topk(const float* scores, int B, int64_t N, int k, const int32_t* q_pos,
                         int ratio, const int32_t* n_valid, const int32_t* map, int32_t* idx,
-                        cudaStream_t stream, bool pdl) {
+                        cudaStream_t stream, bool pdl, void* scratch, size_t scratch_bytes) {
   if (B == 0) return cudaSuccess;
-  const dim3 grid((unsigned)B);
-  if (N <= kRegMaxKeys) {
-    if (N <= kRegThreads * 8)
-      return launch_kernel(topk_reg_kernel<8>, grid, dim3(kRegThreads), 0, stream, pdl, scores, N,
-                           k, q_pos, ratio, n_valid, map, idx);
-    if (N <= kRegThreads * 16)
-      return launch_kernel(topk_reg_kernel<16>, grid, dim3(kRegThreads), 0, stream, pdl, scores,
-                           N, k, q_pos, ratio, n_valid, map, idx);
-    if (N <= kRegThreads * 32)
-      return launch_kernel(topk_reg_kernel<32>, grid, dim3(kRegThreads), 0, stream, pdl, scores,
-                           N, k, q_pos, ratio, n_valid, map, idx);
-    return launch_kernel(topk_reg_kernel<64>, grid, dim3(kRegThreads), 0, stream, pdl, scores, N,
-                         k, q_pos, ratio, n_valid, map, idx);
+  if (N <= kRegMaxKeys)
+    return launch_reg_any(dim3((unsigned)B), scores, N, N, k, q_pos, ratio, n_valid, map, idx, 0,
+                          stream, pdl);
+  const size_t need = topk_scratch_bytes(B, N, k);
+  if (!map && need > 0 && scratch && scratch_bytes >= need) {
+    LongScratch ls;
+    long_scratch(scratch, B, N, k, &ls);
+    const float* cur_score = scores;
+    const int32_t* cur_id = nullptr;       // ids of the current candidates (null: positions)
+    const int32_t* cur_count = n_valid;    // candidates per row (null: visibility via q_pos)
+    const int32_t* cur_pos = q_pos;
+    int cur_ratio = ratio;
+    int64_t M = N;
+    cudaError_t e = cudaSuccess;
+    for (int lvl = 0; M > kRegMaxKeys; ++lvl) {
+      const int C = long_chunks(M);
+      e = launch_reg_any(dim3((unsigned)C, (unsigned)B), cur_score, M, kRegMaxKeys, k, cur_pos,
+                         cur_ratio, cur_count, nullptr, ls.sel, kRegMaxKeys, stream,
+                         lvl == 0 ? pdl : true);
+      if (e != cudaSuccess) return e;
+      const int o = lvl & 1;
+      e = launch_kernel(topk_pack_kernel, dim3((unsigned)B), dim3(256), 0, stream, true, cur_score,
+                        M, cur_id, ls.sel, C, k, ls.score[o], ls.id[o], ls.count[o]);
+      if (e != cudaSuccess) return e;
+      cur_score = ls.score[o];
+      cur_id = ls.id[o];
+      cur_count = ls.count[o];
+      cur_pos = nullptr;
+      cur_ratio = 1;
+      M = (int64_t)C * k;
+    }
+    // the packed ids serve as the map: the selected candidates' entry ids
+    return launch_reg_any(dim3((unsigned)B), cur_score, M, M, k, nullptr, 1, nullptr, cur_id, idx,
+                          0, stream, true);
   }
   const size_t base = align_up(sizeof(TopkShared), 16);
-  return launch_kernel(topk_long_kernel<false>, grid, dim3(kThreads), base, stream, pdl, scores, N,
-                       k, q_pos, ratio, n_valid, map, idx);
+  return launch_kernel(topk_long_kernel<false>, dim3((unsigned)B), dim3(kThreads), base, stream,
+                       pdl, scores, N, k, q_pos, ratio, n_valid, map, idx);
 }
 
 }  // namespace csa2

@@ -123,7 +123,8 @@ def test_index_scores_float_inputs_within_fp32_rounding(C, q_per_seq):
     (5, 1000, 7, "ties"), (3, 16384 + 37, 2048, "ties"), (2, 50000, 2048, "ties"),
     (2, 50000, 4096, "normal"), (4, 3000, 1, "normal"), (3, 700, 2048, "ties"),
     (2, 2048, 2048, "normal"), (2, 1000, 128, "equal"), (2, 70000, 100, "signed_zero"),
-    (16, 8192, 2048, "ties")])
+    (16, 8192, 2048, "ties"), (2, 262144, 8192, "ties"), (3, 300001, 2048, "normal"),
+    (2, 262144, 16384, "ties"), (2, 1 << 21, 2048, "ties")])
 def test_topk_bit_exact(C, B, N, k, kind):
     rng = np.random.default_rng(N + k)
     if kind == "ties":
