@@ -63,8 +63,11 @@ def _load():
                 "orc_sparse_attn": (None, [vp, vp, i32, i32, i32, i64, i64, i32, vp, i32, dbl,
                                            vp, vp]),
                 "orc_block_pool": (None, [vp, i32, i64, vp, i32, i32, i32, vp]),
+                "orc_sparse_attn_swa": (None, [vp, vp, i32, i32, i32, i64, i64, i32, vp, i32, vp,
+                                               i64, i32, vp, dbl, vp, vp]),
                 "orc_layer_group": (i32, [i32, vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32,
-                                          i32, i64, i64, i32, vp, i32, i32, i32, i32, vp, dbl]),
+                                          i32, i64, i64, i32, vp, i32, i32, i32, i32, vp, vp,
+                                          i64, i32, dbl]),
             }
             for name, (res, args) in sig.items():
                 f = getattr(lib, name)
@@ -189,9 +192,29 @@ def sparse_attn(q_bf16, kv_fp4, N: int, kv_seq_stride: int, q_per_seq: int, idx,
     return out, lse
 
 
+def sparse_attn_swa(q_bf16, kv_fp4, N: int, kv_seq_stride: int, q_per_seq: int, idx,
+                    swa_kv, swa_ring: int, n_win: int, q_pos, scale: float):
+    """Sparse attention with the query's sliding window of the layer's SWA KV in the
+    same softmax (reading R10).  swa_kv E4M3 [S][swa_ring][D] -> (out, lse) fp64."""
+    q_bf16 = _c(q_bf16, np.uint16)
+    kv_fp4 = _c(kv_fp4, np.uint8)
+    idx = _c(idx, np.int32)
+    swa = None if swa_kv is None else _c(swa_kv, np.uint8)
+    qp = None if q_pos is None else _c(q_pos, np.int32)
+    B, H, D = q_bf16.shape
+    k = idx.shape[1]
+    out = np.empty((B, H, D), dtype=np.float64)
+    lse = np.empty((B, H), dtype=np.float64)
+    _load().orc_sparse_attn_swa(_ptr(q_bf16), _ptr(kv_fp4), B, H, D, N, kv_seq_stride, q_per_seq,
+                                _ptr(idx), k, _ptr(swa), swa_ring, n_win, _ptr(qp), float(scale),
+                                _ptr(out), _ptr(lse))
+    return out, lse
+
+
 def layer_group(modes: Sequence[int], q_bf16: Sequence[np.ndarray], qi_fp8: Sequence[np.ndarray],
                 kv_fp4, ki_fp8, N: int, kv_seq_stride: int, q_per_seq: int, q_pos, ratio: int,
-                k: int, pool_size: int, scale: float, pool_block: int = 0):
+                k: int, pool_size: int, scale: float, pool_block: int = 0,
+                swa_kv: Optional[Sequence[np.ndarray]] = None, swa_ring: int = 0, n_win: int = 0):
     """Runs the layer schedule (walkthrough 1.(4).1 and 1.(4).2).  pool_block > 0
     builds the blockwise pool (pool_size / pool_block blocks of pool_block entries).
 
@@ -219,10 +242,12 @@ def layer_group(modes: Sequence[int], q_bf16: Sequence[np.ndarray], qi_fp8: Sequ
     P = ctypes.c_void_p
     arr = lambda xs: (P * L)(*[_ptr(x) for x in xs])
     modes_c = (ctypes.c_int * L)(*modes)
+    swas = None if swa_kv is None else [_c(x, np.uint8) for x in swa_kv]
     rc = _load().orc_layer_group(L, modes_c, arr(q_bf16), arr(qis), arr(outs), arr(lses),
                                  arr(idxs), _ptr(kv_fp4), _ptr(ki_fp8), B, H, H_I, D, D_I, N,
                                  kv_seq_stride, q_per_seq, _ptr(qp), ratio, k, pool_size,
-                                 pool_block, _ptr(pool), float(scale))
+                                 pool_block, _ptr(pool), None if swas is None else arr(swas),
+                                 swa_ring, n_win, float(scale))
     if rc != 0:
         raise ValueError("invalid layer schedule")
     return outs, lses, idxs, (pool if pool_size > 0 else None)

@@ -51,6 +51,13 @@
  *      after RoPE).
  *  R8  a Reuse layer takes the indices of the nearest preceding Full or
  *      Reindex layer.
+ *  R10 SWA branch [P4a], [P4d]: each layer's sliding-window KV holds one
+ *      512-channel latent per token in plain E4M3 (the page keeps SWA KV in
+ *      FP8; RMS-normalised latents stay far inside E4M3's +-448), kept per
+ *      sequence in a ring of swa_ring rows (token t at row t mod swa_ring).
+ *      The query at position pos attends tokens max(0, pos - n_win + 1) ..
+ *      pos (its own token included) together with its selected entries, in
+ *      one softmax; K = V = the decoded latent, same scale.
  *  R9  blockwise candidate pool [P4c]: entries are cut into aligned blocks of
  *      `block` consecutive entries; a block's score is the largest score of
  *      its visible entries (a block without one is no candidate); the
@@ -349,17 +356,55 @@ void orc_hier_pool_index(const uint8_t* q_fp8, const uint8_t* k_fp8, int B, int 
 /* Sparse MQA attention over the selected FP4 entries [P4a], [P4d], R7     */
 /* ---------------------------------------------------------------------- */
 
+/* Attention of one query's heads over n gathered latent rows v [n][D]. */
+static void attend(const uint16_t* q_bf16, int H, int D, const double* v, int n, double scale,
+                   double* out, double* lse, double* logit, double* qh) {
+  for (int h = 0; h < H; ++h) {
+    double* o = out + (int64_t)h * D;
+    for (int c = 0; c < D; ++c) qh[c] = bf16_value(q_bf16[(int64_t)h * D + c]);
+    if (n == 0) {
+      for (int c = 0; c < D; ++c) o[c] = 0.0;
+      if (lse) lse[h] = -INFINITY;
+      continue;
+    }
+    double m = -INFINITY;
+    for (int t = 0; t < n; ++t) {
+      double dot = 0.0;
+      for (int c = 0; c < D; ++c) dot += qh[c] * v[(int64_t)t * D + c];
+      logit[t] = scale * dot;
+      if (logit[t] > m) m = logit[t];
+    }
+    double l = 0.0;
+    for (int t = 0; t < n; ++t) {
+      logit[t] = exp(logit[t] - m); /* now the unnormalised weight */
+      l += logit[t];
+    }
+    for (int c = 0; c < D; ++c) o[c] = 0.0;
+    for (int t = 0; t < n; ++t) {
+      double p = logit[t] / l;
+      for (int c = 0; c < D; ++c) o[c] += p * v[(int64_t)t * D + c];
+    }
+    if (lse) lse[h] = m + log(l);
+  }
+}
+
 /* q_bf16 [B][H][D] (bf16 bits), kv_fp4 [S][N][D/2 + D/16], idx [B][k]
- * -> out [B][H][D] (fp64), lse [B][H] (fp64, may be NULL). */
-void orc_sparse_attn(const uint16_t* q_bf16, const uint8_t* kv_fp4, int B, int H, int D, int64_t N,
-                     int64_t kv_seq_stride, int q_per_seq, const int32_t* idx, int k,
-                     double scale, double* out, double* lse) {
+ * -> out [B][H][D] (fp64), lse [B][H] (fp64, may be NULL).
+ * With swa_kv (R10): E4M3 [S][swa_ring][D]; the window of n_win tokens
+ * ending at q_pos[q] joins the selected entries in the same softmax
+ * (swa_kv NULL or n_win 0: no window). */
+void orc_sparse_attn_swa(const uint16_t* q_bf16, const uint8_t* kv_fp4, int B, int H, int D,
+                         int64_t N, int64_t kv_seq_stride, int q_per_seq, const int32_t* idx,
+                         int k, const uint8_t* swa_kv, int64_t swa_ring, int n_win,
+                         const int32_t* q_pos, double scale, double* out, double* lse) {
   int64_t rb = orc_fp4_row_bytes(D);
-  double* v = (double*)malloc(sizeof(double) * (size_t)(k > 0 ? k : 1) * D);
-  double* logit = (double*)malloc(sizeof(double) * (size_t)(k > 0 ? k : 1));
+  int64_t cap = (int64_t)(k > 0 ? k : 0) + (swa_kv && n_win > 0 ? n_win : 0);
+  double* v = (double*)malloc(sizeof(double) * (size_t)(cap > 0 ? cap : 1) * D);
+  double* logit = (double*)malloc(sizeof(double) * (size_t)(cap > 0 ? cap : 1));
   double* qh = (double*)malloc(sizeof(double) * D);
   for (int q = 0; q < B; ++q) {
-    const uint8_t* kvseq = kv_fp4 + (int64_t)(q / q_per_seq) * kv_seq_stride * rb;
+    int64_t s = q / q_per_seq;
+    const uint8_t* kvseq = kv_fp4 + s * kv_seq_stride * rb;
     /* gather and dequantise the selected rows */
     int n = 0;
     for (int t = 0; t < k; ++t) {
@@ -368,37 +413,29 @@ void orc_sparse_attn(const uint16_t* q_bf16, const uint8_t* kv_fp4, int B, int H
       orc_dequantize_row(kvseq + (int64_t)j * rb, D, v + (int64_t)n * D);
       ++n;
     }
-    for (int h = 0; h < H; ++h) {
-      double* o = out + ((int64_t)q * H + h) * D;
-      for (int c = 0; c < D; ++c) qh[c] = bf16_value(q_bf16[((int64_t)q * H + h) * D + c]);
-      if (n == 0) {
-        for (int c = 0; c < D; ++c) o[c] = 0.0;
-        if (lse) lse[(int64_t)q * H + h] = -INFINITY;
-        continue;
+    /* the query's own sliding window of the layer's SWA KV */
+    if (swa_kv && n_win > 0 && q_pos && q_pos[q] >= 0) {
+      int64_t pos = q_pos[q];
+      int64_t t0 = pos - n_win + 1 > 0 ? pos - n_win + 1 : 0;
+      for (int64_t t = t0; t <= pos; ++t) {
+        const uint8_t* row = swa_kv + (s * swa_ring + t % swa_ring) * D;
+        for (int c = 0; c < D; ++c) v[(int64_t)n * D + c] = orc_e4m3_value(row[c]);
+        ++n;
       }
-      double m = -INFINITY;
-      for (int t = 0; t < n; ++t) {
-        double dot = 0.0;
-        for (int c = 0; c < D; ++c) dot += qh[c] * v[(int64_t)t * D + c];
-        logit[t] = scale * dot;
-        if (logit[t] > m) m = logit[t];
-      }
-      double l = 0.0;
-      for (int t = 0; t < n; ++t) {
-        logit[t] = exp(logit[t] - m); /* now the unnormalised weight */
-        l += logit[t];
-      }
-      for (int c = 0; c < D; ++c) o[c] = 0.0;
-      for (int t = 0; t < n; ++t) {
-        double p = logit[t] / l;
-        for (int c = 0; c < D; ++c) o[c] += p * v[(int64_t)t * D + c];
-      }
-      if (lse) lse[(int64_t)q * H + h] = m + log(l);
     }
+    attend(q_bf16 + (int64_t)q * H * D, H, D, v, n, scale, out + (int64_t)q * H * D,
+           lse ? lse + (int64_t)q * H : NULL, logit, qh);
   }
   free(v);
   free(logit);
   free(qh);
+}
+
+void orc_sparse_attn(const uint16_t* q_bf16, const uint8_t* kv_fp4, int B, int H, int D, int64_t N,
+                     int64_t kv_seq_stride, int q_per_seq, const int32_t* idx, int k,
+                     double scale, double* out, double* lse) {
+  orc_sparse_attn_swa(q_bf16, kv_fp4, B, H, D, N, kv_seq_stride, q_per_seq, idx, k, NULL, 0, 0,
+                      NULL, scale, out, lse);
 }
 
 /* ---------------------------------------------------------------------- */
@@ -413,6 +450,8 @@ enum { ORC_FULL = 0, ORC_REINDEX = 1, ORC_REUSE = 2 };
  *   qi_fp8[l]         [B][H_I][D_I] indexer query (ignored for REUSE)
  *   out[l], lse[l]    [B][H][D], [B][H] outputs (lse may be NULL)
  *   idx_out[l]        [B][k] indices layer l attended (written for every layer)
+ *   swa_kv[l]         E4M3 [S][swa_ring][D] SWA KV of layer l (R10), or NULL;
+ *                     with n_win > 0 each layer also attends its window
  *   pool_out          [B][pool_size] when pool_size > 0 (built by FULL layers):
  *                     pool_block == 0: the top pool_size entries (R6);
  *                     pool_block > 0: the blockwise pool of pool_size /
@@ -423,7 +462,8 @@ int orc_layer_group(int n_layers, const int* modes, const uint16_t* const* q_bf1
                     int32_t* const* idx_out, const uint8_t* kv_fp4, const uint8_t* ki_fp8, int B,
                     int H, int H_I, int D, int D_I, int64_t N, int64_t kv_seq_stride,
                     int q_per_seq, const int32_t* q_pos, int ratio, int k, int pool_size,
-                    int pool_block, int32_t* pool_out, double scale) {
+                    int pool_block, int32_t* pool_out, const uint8_t* const* swa_kv,
+                    int64_t swa_ring, int n_win, double scale) {
   if (n_layers < 1 || modes[0] != ORC_FULL) return -1;
   if (pool_block < 0 || (pool_block > 0 && pool_size % pool_block != 0)) return -1;
   double* scores = (double*)malloc(sizeof(double) * (size_t)B * (size_t)(N > 0 ? N : 1));
@@ -455,8 +495,9 @@ int orc_layer_group(int n_layers, const int* modes, const uint16_t* const* q_bf1
       free(scores);
       return -1;
     }
-    orc_sparse_attn(q_bf16[l], kv_fp4, B, H, D, N, kv_seq_stride, q_per_seq, idx, k, scale, out[l],
-                    lse ? lse[l] : NULL);
+    orc_sparse_attn_swa(q_bf16[l], kv_fp4, B, H, D, N, kv_seq_stride, q_per_seq, idx, k,
+                        swa_kv ? swa_kv[l] : NULL, swa_ring, n_win, q_pos, scale, out[l],
+                        lse ? lse[l] : NULL);
   }
   free(scores);
   return 0;

@@ -197,3 +197,96 @@ def test_blockwise_pool_schedule_selects_inside_the_pool():
         members = set(pool[q][pool[q] >= 0].tolist())
         assert set(idxs[1][q][idxs[1][q] >= 0].tolist()) <= members
     assert np.array_equal(idxs[2], idxs[1])
+
+
+# ---------------------------------------------------------------- SWA branch
+
+def _e4m3_rows(rng, n, scale=1.0):
+    x = (rng.standard_normal((n, D)) * scale).astype(np.float32)
+    return torch.from_numpy(x).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+
+
+def _e4m3_decode(b):
+    return torch.from_numpy(np.ascontiguousarray(b)).view(torch.float8_e4m3fn).double().numpy()
+
+
+def _sdpa(q_bits, v):
+    """fp64 softmax attention of every head of one query over rows v [n][D]."""
+    qt = torch.from_numpy(_bf16_to_f64(q_bits))                            # [H][D]
+    vt = torch.from_numpy(v)
+    H, n = qt.shape[0], vt.shape[0]
+    o = torch.nn.functional.scaled_dot_product_attention(
+        qt[:, None], vt[None].expand(H, n, D), vt[None].expand(H, n, D), scale=SCALE)[:, 0]
+    return o.numpy(), torch.logsumexp(SCALE * qt @ vt.T, dim=-1).numpy()
+
+
+def test_swa_window_alone_equals_dense_attention_over_the_window():
+    # R10: the query at position pos attends tokens max(0, pos - n_win + 1) .. pos,
+    # token t at ring row t mod ring.  Rows outside the window hold 448s that
+    # would dominate any softmax they entered.
+    rng = np.random.default_rng(30)
+    H, ring, n_win = 4, 40, 16
+    q = _bf16(rng.standard_normal((3, H, D)))
+    kv = _kv(rng, 8)
+    idx = np.full((3, 4), -1, np.int32)
+    for pos in (0, 9, 15, 16, 57, 1000):
+        swa = np.full((3, ring, D), 0x7E, np.uint8)       # E4M3 448 everywhere
+        toks = list(range(max(0, pos - n_win + 1), pos + 1))
+        rows = _e4m3_rows(rng, len(toks))
+        for s in range(3):
+            for i, t in enumerate(toks):
+                swa[s, t % ring] = rows[i]
+        out, lse = oracle.sparse_attn_swa(q, kv, 8, 0, 3, idx, swa, ring, n_win,
+                                          np.full(3, pos, np.int32), SCALE)
+        for b in range(3):
+            ref_o, ref_l = _sdpa(q[b], _e4m3_decode(rows))
+            np.testing.assert_allclose(out[b], ref_o, rtol=1e-11, atol=1e-12)
+            np.testing.assert_allclose(lse[b], ref_l, rtol=1e-12)
+
+
+def test_joint_softmax_is_the_lse_merge_of_its_two_parts():
+    rng = np.random.default_rng(31)
+    B, H, N, k, ring, n_win = 3, 8, 200, 24, 160, 128
+    kv = _kv(rng, B * N)
+    q = _bf16(rng.standard_normal((B, H, D)))
+    idx = np.stack([np.sort(rng.choice(N, k, replace=False)) for _ in range(B)]).astype(np.int32)
+    idx[1, -5:] = -1
+    swa = np.stack([_e4m3_rows(rng, ring, 0.7) for _ in range(B)])
+    pos = np.array([4000, 70, 127], np.int32)
+    o, l = oracle.sparse_attn_swa(q, kv, N, N, 1, idx, swa, ring, n_win, pos, SCALE)
+    o1, l1 = oracle.sparse_attn(q, kv, N, N, 1, idx, SCALE)
+    none = np.full((B, 1), -1, np.int32)
+    o2, l2 = oracle.sparse_attn_swa(q, kv, N, N, 1, none, swa, ring, n_win, pos, SCALE)
+    L = np.logaddexp(l1, l2)
+    merged = np.exp(l1 - L)[..., None] * o1 + np.exp(l2 - L)[..., None] * o2
+    np.testing.assert_allclose(o, merged, rtol=1e-10, atol=1e-12)
+    np.testing.assert_allclose(l, L, rtol=1e-12)
+
+
+def test_without_a_window_the_swa_attention_is_the_sparse_attention():
+    rng = np.random.default_rng(32)
+    B, H, N, k = 2, 4, 64, 10
+    kv = _kv(rng, B * N)
+    q = _bf16(rng.standard_normal((B, H, D)))
+    idx = rng.integers(-1, N, (B, k)).astype(np.int32)
+    o1, l1 = oracle.sparse_attn(q, kv, N, N, 1, idx, SCALE)
+    swa = np.stack([_e4m3_rows(rng, 8) for _ in range(B)])
+    for args in ((None, 0, 0), (swa, 8, 0)):
+        o2, l2 = oracle.sparse_attn_swa(q, kv, N, N, 1, idx, *args, np.array([50, 60], np.int32),
+                                        SCALE)
+        assert np.array_equal(o1, o2) and np.array_equal(l1, l2)
+
+
+def test_layer_group_with_swa_matches_per_layer_attention():
+    rng = np.random.default_rng(33)
+    B, N, k, ring, n_win = 2, 150, 12, 128, 128
+    kv, ki, qs, qis = _group_inputs(rng, B, N)
+    swas = [np.stack([_e4m3_rows(rng, ring) for _ in range(B)]) for _ in range(3)]
+    pos = np.array([4 * N - 1, 300], np.int32)
+    outs, lses, idxs, _ = oracle.layer_group([0, 1, 2], qs, [qis[0], qis[1], None], kv, ki, N, N,
+                                             1, pos, 4, k, 0, SCALE, swa_kv=swas, swa_ring=ring,
+                                             n_win=n_win)
+    for l in range(3):
+        o, lse = oracle.sparse_attn_swa(qs[l], kv, N, N, 1, idxs[l], swas[l], ring, n_win, pos,
+                                        SCALE)
+        assert np.array_equal(outs[l], o) and np.array_equal(lses[l], lse)
