@@ -160,7 +160,8 @@ class ClockSampler:
 
 def algorithmic_bytes(w):
     """Per step: indexer K of every scored entry, indexer q, selected FP4 rows,
-    main queries (bf16) and outputs (fp32), as the workload's layers read them."""
+    SWA window rows, main queries (bf16) and outputs (fp32), as the workload's
+    layers read them."""
     from sparse_attention_decode_csa2_gb300.synthetic import FULL, REINDEX, REUSE
     B, N, k = w.B, w.N, w.k
     total = 0
@@ -175,6 +176,8 @@ def algorithmic_bytes(w):
                 b += w.n_seq * N * w.D_I
         elif m == REINDEX:
             b += B * w.pool * (w.D_I + 4) + B * w.H_I * w.D_I
+        if w.n_win:   # each query's SWA window (E4M3 rows of D bytes)
+            b += sum(min(w.n_win, int(p) + 1) for p in w.q_pos() if p >= 0) * w.D
         per_layer.append(b)
         total += b
     return total, per_layer
@@ -184,15 +187,17 @@ def kernel_bytes(w):
     """Algorithmic bytes of each timed component op (one launch over the batch)."""
     B, N, k = w.B, w.N, w.k
     n_scored = sum(min(N, (int(p) + 1) // w.ratio) for p in w.q_pos())
+    n_win = sum(min(w.n_win, int(p) + 1) for p in w.q_pos() if p >= 0) if w.n_win else 0
     return {
         "index_scores": n_scored * w.D_I + B * w.H_I * w.D_I + B * N * 4,
         "topk": n_scored * 4 + B * k * 4,
-        "sparse_attn_fp4": B * k * (w.row_bytes + 4) + B * w.H * w.D * (2 + 4) + B * w.H * 4,
+        "sparse_attn_fp4": B * k * (w.row_bytes + 4) + n_win * w.D + B * w.H * w.D * (2 + 4) +
+                           B * w.H * 4,
     }
 
 
 def attn_flops(w):
-    return 4.0 * w.B * w.H * w.k * w.D
+    return 4.0 * w.B * w.H * (w.k + w.n_win) * w.D
 
 
 def run_gpu(args, rank, world, local):
@@ -266,9 +271,11 @@ def run_gpu(args, rank, world, local):
         "index_scores": lambda: csa2.index_scores(inp.qi[0], inp.ki_fp8, w.N, w.kv_seq_stride,
                                                   w.q_per_seq, inp.q_pos, w.ratio, out=scores),
         "topk": lambda: csa2.topk(scores, w.k, inp.q_pos, w.ratio, ws, out=idx),
-        "sparse_attn_fp4": lambda: csa2.sparse_attn_fp4(inp.q[0], inp.kv_fp4, w.N,
-                                                        w.kv_seq_stride, w.q_per_seq, idx,
-                                                        inp.scale, out=out, lse=lse, ws=ws),
+        "sparse_attn_fp4": (lambda: csa2.sparse_attn_fp4_swa(
+            inp.q[0], inp.kv_fp4, w.N, w.kv_seq_stride, w.q_per_seq, idx, inp.swa[0], w.n_win,
+            inp.q_pos, inp.scale, out=out, lse=lse, ws=ws)) if w.n_win else
+        (lambda: csa2.sparse_attn_fp4(inp.q[0], inp.kv_fp4, w.N, w.kv_seq_stride, w.q_per_seq,
+                                      idx, inp.scale, out=out, lse=lse, ws=ws)),
     }
     for name, fn in ops.items():
         fn()
@@ -416,12 +423,16 @@ class OracleSample:
             self.items.append(dict(q=q, kv=kv, ki=ki, qpos=w.q_pos()[q:q + 1],
                                    qb=[w.q_bf16(l, [q]) for l in range(L)],
                                    qi=[w.qi_fp8(l, [q]) if w.modes[l] != 2 else None
-                                       for l in range(L)]))
+                                       for l in range(L)],
+                                   swa=[w.swa_kv(l, s)[None] for l in range(L)]
+                                   if w.n_win else None))
 
     def run(self, item):
         w, o = self.w, self.oracle
         o.layer_group(w.modes, item["qb"], item["qi"], item["kv"], item["ki"], w.N, 0, 1,
-                      item["qpos"], w.ratio, w.k, w.pool, 1.0 / math.sqrt(w.D))
+                      item["qpos"], w.ratio, w.k, w.pool, 1.0 / math.sqrt(w.D),
+                      pool_block=w.pool_block, swa_kv=item["swa"], swa_ring=w.swa_ring,
+                      n_win=w.n_win)
 
 
 def cpu_baseline(w, budget_s=12.0):

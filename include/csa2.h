@@ -185,6 +185,32 @@ csa2_status csa2_sparse_attn_fp4(const uint16_t* q_bf16, const uint8_t* kv_fp4, 
                                  float* lse, void* ws, size_t ws_bytes, cudaStream_t stream);
 
 /*
+ * csa2_sparse_attn_fp4_swa -- csa2_sparse_attn_fp4 with the query's sliding
+ * window of the layer's SWA KV in the same softmax (walkthrough 1.(4): every
+ * query attends the selected entries and its layer's own SWA KV; 1.(5).4:
+ * SWA KV stays FP8; 2.(2).1: window n_win = 128).
+ *   swa_kv   E4M3 [S][swa_ring][D] one latent per token (plain E4M3, no
+ *            scale), per sequence a ring: token t at row t mod swa_ring
+ *            (16-byte aligned)
+ *   swa_ring rows per sequence, >= n_win; when several queries share a
+ *            sequence the ring must hold all of their windows
+ *   n_win    window length (>= 1): the query at q_pos[b] attends tokens
+ *            max(0, q_pos[b] - n_win + 1) .. q_pos[b] (none when q_pos[b] < 0)
+ *   q_pos    int32 [B] token positions (required)
+ *   out, lse as csa2_sparse_attn_fp4, over the union of both sets: K = V, one
+ *            softmax with the same scale.
+ *   ws       at least csa2_workspace_size(B, 0, k, H, 0) bytes.
+ * Errors as csa2_sparse_attn_fp4; CSA2_ERR_INVALID_ARG for a missing swa_kv /
+ * q_pos, n_win < 1 or swa_ring < n_win.
+ */
+csa2_status csa2_sparse_attn_fp4_swa(const uint16_t* q_bf16, const uint8_t* kv_fp4, int B, int H,
+                                     int D, int64_t N, int64_t kv_seq_stride, int q_per_seq,
+                                     const int32_t* idx, int k, const uint8_t* swa_kv,
+                                     int64_t swa_ring, int n_win, const int32_t* q_pos,
+                                     float softmax_scale, float* out, float* lse, void* ws,
+                                     size_t ws_bytes, cudaStream_t stream);
+
+/*
  * csa2_sparse_attn_fp4_noalloc -- csa2_sparse_attn_fp4 for callers that cannot
  * allocate device memory.  The pages have no counterpart: this is a deployment
  * variant, not part of the method.
@@ -225,6 +251,8 @@ typedef struct csa2_layer {
   int32_t* idx_out;        /* int32 [B][k]: indices this layer attended.  Required for
                               FULL and REINDEX; for REUSE, NULL or a buffer that
                               receives a copy of the reused indices */
+  const uint8_t* swa_kv;   /* E4M3 [S][swa_ring][D] this layer's SWA KV (see
+                              csa2_sparse_attn_fp4_swa), or NULL: no window */
 } csa2_layer;
 
 /* What the layers of one group share (walkthrough 1.(4).1). */
@@ -244,6 +272,10 @@ typedef struct csa2_group_args {
   int pool_block;          /* how FULL layers build the pool: 0 or 1: the top pool_size
                               entries; b > 1: the blockwise pool of pool_size / b blocks
                               of b entries (csa2_block_pool; pool_size % b == 0) */
+  int64_t swa_ring;        /* rows per sequence of the layers' SWA KV rings */
+  int n_win;               /* SWA window; 0: no layer attends a window.  With n_win > 0
+                              each layer with swa_kv also attends its window (q_pos
+                              required, swa_ring >= n_win) */
 } csa2_group_args;
 
 /*

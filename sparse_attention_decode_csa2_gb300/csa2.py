@@ -47,7 +47,7 @@ _vp, _i32, _i64, _sz, _f32 = (ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, cty
 
 class Csa2Layer(ctypes.Structure):
     _fields_ = [("mode", ctypes.c_int), ("q_bf16", _vp), ("qi_fp8", _vp), ("out", _vp),
-                ("lse", _vp), ("idx_out", _vp)]
+                ("lse", _vp), ("idx_out", _vp), ("swa_kv", _vp)]
 
 
 class Csa2GroupArgs(ctypes.Structure):
@@ -56,7 +56,8 @@ class Csa2GroupArgs(ctypes.Structure):
                 ("N", ctypes.c_int64), ("kv_seq_stride", ctypes.c_int64),
                 ("q_per_seq", ctypes.c_int), ("q_pos", _vp), ("ratio", ctypes.c_int),
                 ("k", ctypes.c_int), ("pool_size", ctypes.c_int), ("pool_out", _vp),
-                ("softmax_scale", ctypes.c_float), ("pool_block", ctypes.c_int)]
+                ("softmax_scale", ctypes.c_float), ("pool_block", ctypes.c_int),
+                ("swa_ring", ctypes.c_int64), ("n_win", ctypes.c_int)]
 
 
 _SIGS = {
@@ -73,6 +74,8 @@ _SIGS = {
                                     _i32, _vp, _vp, _sz, _vp]),
     "csa2_sparse_attn_fp4": (_i32, [_vp, _vp, _i32, _i32, _i32, _i64, _i64, _i32, _vp, _i32,
                                     _f32, _vp, _vp, _vp, _sz, _vp]),
+    "csa2_sparse_attn_fp4_swa": (_i32, [_vp, _vp, _i32, _i32, _i32, _i64, _i64, _i32, _vp, _i32,
+                                        _vp, _i64, _i32, _vp, _f32, _vp, _vp, _vp, _sz, _vp]),
     "csa2_sparse_attn_fp4_noalloc": (_i32, [_vp, _vp, _i32, _i32, _i32, _i64, _i64, _i32, _vp,
                                             _i32, _f32, _vp, _vp, _vp]),
     "csa2_layer_group": (_i32, [ctypes.POINTER(Csa2Layer), _i32, ctypes.POINTER(Csa2GroupArgs),
@@ -260,6 +263,37 @@ def sparse_attn_fp4(q_bf16: torch.Tensor, kv_fp4: torch.Tensor, N: int, kv_seq_s
     return out, lse
 
 
+def sparse_attn_fp4_swa(q_bf16: torch.Tensor, kv_fp4: torch.Tensor, N: int, kv_seq_stride: int,
+                        q_per_seq: int, idx: torch.Tensor, swa_kv: torch.Tensor, n_win: int,
+                        q_pos: torch.Tensor, softmax_scale: Optional[float] = None,
+                        out: Optional[torch.Tensor] = None, lse: Optional[torch.Tensor] = None,
+                        ws: Optional[torch.Tensor] = None, want_lse: bool = True):
+    """sparse_attn_fp4 plus each query's window of the layer's SWA KV (E4M3
+    [S][ring][512], token t at row t mod ring) in the same softmax."""
+    q = _bits16(q_bf16, "q_bf16")
+    kv_fp4 = _dev(kv_fp4, torch.uint8, "kv_fp4")
+    idx = _dev(idx, torch.int32, "idx")
+    swa_kv = _dev(swa_kv, torch.uint8, "swa_kv")
+    qp = _dev(q_pos, torch.int32, "q_pos")
+    B, H, D = q.shape
+    k = idx.shape[1]
+    ring = swa_kv.shape[-2]
+    if softmax_scale is None:
+        softmax_scale = 1.0 / math.sqrt(D)
+    if ws is None:
+        ws = make_workspace(B, 0, k, H, 0, q.device)
+    if out is None:
+        out = torch.empty((B, H, D), dtype=torch.float32, device=q.device)
+    if lse is None and want_lse:
+        lse = torch.empty((B, H), dtype=torch.float32, device=q.device)
+    _dev(out, torch.float32, "out")
+    _check(lib.csa2_sparse_attn_fp4_swa(_ptr(q), _ptr(kv_fp4), B, H, D, N, kv_seq_stride,
+                                        q_per_seq, _ptr(idx), k, _ptr(swa_kv), ring, n_win,
+                                        _ptr(qp), softmax_scale, _ptr(out), _ptr(lse), _ptr(ws),
+                                        ws.numel(), _stream()), "csa2_sparse_attn_fp4_swa")
+    return out, lse
+
+
 class LayerGroup:
     """Prepared arguments of csa2_layer_group: tensors are kept alive and the
     ctypes structs are built once, so repeated calls (and CUDA-graph capture)
@@ -270,7 +304,8 @@ class LayerGroup:
                  ki_fp8: torch.Tensor, N: int, kv_seq_stride: int, q_per_seq: int,
                  q_pos: Optional[torch.Tensor], ratio: int, k: int, pool_size: int = 0,
                  softmax_scale: Optional[float] = None, want_lse: bool = True,
-                 reuse_idx_copy: bool = True, pool_block: int = 0):
+                 reuse_idx_copy: bool = True, pool_block: int = 0,
+                 swa_kv: Optional[Sequence[Optional[torch.Tensor]]] = None, n_win: int = 0):
         L = len(modes)
         self.modes = list(modes)
         self.q = [_bits16(q, f"q_bf16[{l}]") for l, q in enumerate(q_bf16)]
@@ -296,13 +331,19 @@ class LayerGroup:
         self.pool = (torch.empty((B, pool_size), dtype=torch.int32, device=dev)
                      if pool_size > 0 else None)
         self.ws = make_workspace(B, N, k, H, pool_size, dev)
+        self.swa = ([None] * L if swa_kv is None else
+                    [None if x is None else _dev(x, torch.uint8, f"swa_kv[{l}]")
+                     for l, x in enumerate(swa_kv)])
+        ring = next((x.shape[-2] for x in self.swa if x is not None), 0)
         self._layers = (Csa2Layer * L)()
         for l in range(L):
             self._layers[l] = Csa2Layer(self.modes[l], _ptr(self.q[l]), _ptr(self.qi[l]),
-                                        _ptr(self.out[l]), _ptr(self.lse[l]), _ptr(self.idx[l]))
+                                        _ptr(self.out[l]), _ptr(self.lse[l]), _ptr(self.idx[l]),
+                                        _ptr(self.swa[l]))
         self._args = Csa2GroupArgs(_ptr(self.kv), _ptr(self.ki), B, H, H_I, D, D_I, N,
                                    kv_seq_stride, q_per_seq, _ptr(self.q_pos), ratio, k,
-                                   pool_size, _ptr(self.pool), softmax_scale, pool_block)
+                                   pool_size, _ptr(self.pool), softmax_scale, pool_block, ring,
+                                   n_win)
 
     def __call__(self):
         _check(lib.csa2_layer_group(self._layers, len(self.modes), ctypes.byref(self._args),
@@ -318,7 +359,8 @@ def group_launches(group: LayerGroup) -> int:
 
 
 def layer_group(modes, q_bf16, qi_fp8, kv_fp4, ki_fp8, N, kv_seq_stride, q_per_seq, q_pos, ratio,
-                k, pool_size=0, softmax_scale=None, pool_block=0):
+                k, pool_size=0, softmax_scale=None, pool_block=0, swa_kv=None, n_win=0):
     """One-shot csa2_layer_group; returns (outs, lses, idxs, pool)."""
     return LayerGroup(modes, q_bf16, qi_fp8, kv_fp4, ki_fp8, N, kv_seq_stride, q_per_seq, q_pos,
-                      ratio, k, pool_size, softmax_scale, pool_block=pool_block)()
+                      ratio, k, pool_size, softmax_scale, pool_block=pool_block, swa_kv=swa_kv,
+                      n_win=n_win)()

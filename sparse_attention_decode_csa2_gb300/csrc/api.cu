@@ -223,6 +223,26 @@ csa2_status csa2_sparse_attn_fp4(const uint16_t* q_bf16, const uint8_t* kv_fp4, 
                                          status_ptr(ws), stream));
 }
 
+csa2_status csa2_sparse_attn_fp4_swa(const uint16_t* q_bf16, const uint8_t* kv_fp4, int B, int H,
+                                     int D, int64_t N, int64_t kv_seq_stride, int q_per_seq,
+                                     const int32_t* idx, int k, const uint8_t* swa_kv,
+                                     int64_t swa_ring, int n_win, const int32_t* q_pos,
+                                     float softmax_scale, float* out, float* lse, void* ws,
+                                     size_t ws_bytes, cudaStream_t stream) {
+  csa2_status s = check_seq(B, N, kv_seq_stride, q_per_seq);
+  if (s != CSA2_OK) return s;
+  if ((s = check_attn(q_bf16, kv_fp4, B, H, D, k, softmax_scale, out)) != CSA2_OK) return s;
+  if (B > 0 && (!idx || !swa_kv || !q_pos)) return CSA2_ERR_INVALID_ARG;
+  if (n_win < 1 || swa_ring < n_win || !aligned16(swa_kv)) return CSA2_ERR_INVALID_ARG;
+  WsLayout w = layout(B, 0, k, H, 0);
+  if (!ws || ws_bytes < w.total) return CSA2_ERR_WORKSPACE;
+  uint8_t* wsb = reinterpret_cast<uint8_t*>(ws);
+  const SwaArgs swa{swa_kv, swa_ring, n_win, q_pos};
+  return check_launch(launch_sparse_attn(q_bf16, kv_fp4, B, H, N, kv_seq_stride, q_per_seq, idx,
+                                         k, softmax_scale, out, lse, wsb + w.attn,
+                                         status_ptr(ws), stream, false, &swa));
+}
+
 int csa2_layer_group_launches(const csa2_layer* layers, int n_layers, const csa2_group_args* g) {
   if (!layers || !g || n_layers < 1 || layers[0].mode != CSA2_FULL) return -1;
   if (g->B == 0) return 0;
@@ -252,11 +272,14 @@ csa2_status csa2_layer_group(const csa2_layer* layers, int n_layers, const csa2_
   if (g->pool_size > 0 && g->pool_size < g->k) return CSA2_ERR_INVALID_ARG;
   if (g->pool_block < 0 || (g->pool_block > 1 && g->pool_size % g->pool_block != 0))
     return CSA2_ERR_INVALID_ARG;
+  if (g->n_win < 0 || (g->n_win > 0 && (g->swa_ring < g->n_win || (g->B > 0 && !g->q_pos))))
+    return CSA2_ERR_INVALID_ARG;
   // validate every layer before launching anything
   for (int l = 0; l < n_layers; ++l) {
     const csa2_layer& L = layers[l];
     if (L.mode != CSA2_FULL && L.mode != CSA2_REINDEX && L.mode != CSA2_REUSE)
       return CSA2_ERR_INVALID_ARG;
+    if (g->n_win > 0 && L.swa_kv && !aligned16(L.swa_kv)) return CSA2_ERR_INVALID_ARG;
     if ((s = check_attn(L.q_bf16, g->kv_fp4, g->B, g->H, g->D, g->k, g->softmax_scale, L.out)) !=
         CSA2_OK)
       return s;
@@ -314,9 +337,11 @@ csa2_status csa2_layer_group(const csa2_layer* layers, int n_layers, const csa2_
     latest = use;
     // After a top-k of this layer the attention starts early (programmatic
     // dependent launch): it loads Q and sets up while the selection finishes.
+    const SwaArgs swa{L.swa_kv, g->swa_ring, g->n_win, g->q_pos};
+    const bool with_swa = g->n_win > 0 && L.swa_kv;
     e = launch_sparse_attn(L.q_bf16, g->kv_fp4, g->B, g->H, g->N, g->kv_seq_stride, g->q_per_seq,
                            use, g->k, g->softmax_scale, L.out, L.lse, wsb + w.attn, status,
-                           stream, /*pdl=*/L.mode != CSA2_REUSE);
+                           stream, /*pdl=*/L.mode != CSA2_REUSE, with_swa ? &swa : nullptr);
   }
   return check_launch(e);
 }

@@ -52,10 +52,15 @@ int choose_splits(int B, int k) {
   return (k + chunk - 1) / chunk;
 }
 
+size_t partial_bytes(int B, int H, int nsplit) {
+  if (nsplit <= 1) return 0;
+  return align_up((size_t)B * nsplit * H * kD * 4 + (size_t)B * nsplit * H * 4, 256);
+}
+
 cudaError_t launch_attn(const uint16_t* q_bf16, const uint8_t* kv_fp4, int B, int H, int64_t N,
                         int64_t kv_seq_stride, int q_per_seq, const int32_t* idx, int k,
                         float softmax_scale, float* out, float* lse, void* scratch,
-                        int32_t* status, cudaStream_t stream, bool pdl) {
+                        int32_t* status, cudaStream_t stream, bool pdl, const SwaArgs* swa) {
   const int nsplit = choose_splits(B, k);
   const int chunk = ((k + nsplit - 1) / nsplit + kSplitTile - 1) / kSplitTile * kSplitTile;
   float* part_o = nullptr;
@@ -67,7 +72,7 @@ cudaError_t launch_attn(const uint16_t* q_bf16, const uint8_t* kv_fp4, int B, in
   const float scale_log2 = softmax_scale * 1.4426950408889634f;
   cudaError_t e = launch_sparse_attn_tc(q_bf16, kv_fp4, B, H, N, kv_seq_stride, q_per_seq, idx, k,
                                         nsplit, chunk, scale_log2, out, lse, part_o, part_lse,
-                                        status, stream, pdl);
+                                        status, swa, stream, pdl);
   if (e != cudaSuccess || nsplit == 1) return e;
   return launch_kernel(attn_combine_kernel, dim3((unsigned)H, (unsigned)B), dim3(128), 0, stream,
                        true, part_o, part_lse, H, nsplit, out, lse);
@@ -82,18 +87,16 @@ int attn_launches(int B, int k) {
 
 size_t attn_scratch_bytes(int B, int H, int k) {
   if (B <= 0 || H <= 0 || k <= 0) return 0;
-  const int nsplit = choose_splits(B, k);
-  if (nsplit <= 1) return 0;
-  return align_up((size_t)B * nsplit * H * kD * 4 + (size_t)B * nsplit * H * 4, 256);
+  return partial_bytes(B, H, choose_splits(B, k));
 }
 
 cudaError_t launch_sparse_attn(const uint16_t* q_bf16, const uint8_t* kv_fp4, int B, int H,
                                int64_t N, int64_t kv_seq_stride, int q_per_seq, const int32_t* idx,
                                int k, float softmax_scale, float* out, float* lse, void* scratch,
-                               int32_t* status, cudaStream_t stream, bool pdl) {
+                               int32_t* status, cudaStream_t stream, bool pdl, const SwaArgs* swa) {
   if (B == 0) return cudaSuccess;
   return launch_attn(q_bf16, kv_fp4, B, H, N, kv_seq_stride, q_per_seq, idx, k, softmax_scale, out,
-                     lse, scratch, status, stream, pdl);
+                     lse, scratch, status, stream, pdl, swa);
 }
 
 }  // namespace csa2

@@ -99,13 +99,21 @@ __device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
   return r;
 }
 
+// SWA branch (swa_kv non-null): the CTA of the last chunk of query b also
+// attends the query's sliding window of the layer's SWA KV (E4M3 rows, per
+// sequence a ring with token t at row t mod swa_ring; window
+// max(0, pos - n_win + 1) .. pos) as extra tiles after its selected entries,
+// in the same online softmax; the split-k merge then combines everything
+// into one softmax over both sets.
 template <int H>
 __global__ void __launch_bounds__(kThreadsTc, 1)
 sparse_attn_tc_kernel(const uint16_t* __restrict__ q_bf16, const uint8_t* __restrict__ kv_fp4,
                       int64_t N, int64_t kv_seq_stride, int q_per_seq,
                       const int32_t* __restrict__ idx, int k, int chunk, float scale_log2,
                       float* __restrict__ out, float* __restrict__ lse, float* __restrict__ part_o,
-                      float* __restrict__ part_lse, int32_t* status) {
+                      float* __restrict__ part_lse, int32_t* status,
+                      const uint8_t* __restrict__ swa_kv, int64_t swa_ring, int n_win,
+                      const int32_t* __restrict__ q_pos) {
   using L = TcLayout;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_s = su32(smem_raw);
@@ -120,7 +128,17 @@ sparse_attn_tc_kernel(const uint16_t* __restrict__ q_bf16, const uint8_t* __rest
   const int s0 = split * chunk;
   const int s1 = min(k, s0 + chunk);
   const int cnt = max(0, s1 - s0);
-  const int ntiles = (cnt + kTileE - 1) / kTileE;
+  const int nmain = (cnt + kTileE - 1) / kTileE;  // tiles of selected entries
+  // the query's SWA window: tiles [nmain, ntiles) of the last chunk's CTA
+  int64_t w0 = 0;
+  int wcnt = 0;
+  if (swa_kv && split == nsplit - 1) {
+    const int64_t pos = q_pos[b];
+    w0 = pos - n_win + 1 > 0 ? pos - n_win + 1 : 0;
+    wcnt = pos >= 0 ? (int)(pos - w0 + 1) : 0;
+  }
+  const int ntiles = nmain + (wcnt + kTileE - 1) / kTileE;
+  const uint8_t* swaseq = swa_kv ? swa_kv + (int64_t)(b / q_per_seq) * swa_ring * kD : nullptr;
   const int32_t* slots = idx + (int64_t)b * k + s0;
   const uint8_t* kvseq = kv_fp4 + (int64_t)(b / q_per_seq) * kv_seq_stride * kRowBytes;
   const uint32_t q_s = sbase + L::q_off, v_s = sbase + L::v_off, p_s = sbase + L::p_off;
@@ -202,13 +220,63 @@ sparse_attn_tc_kernel(const uint16_t* __restrict__ q_bf16, const uint8_t* __rest
         for (int i = 0; i < 9; ++i) r[i] = make_uint4(0, 0, 0, 0);
       }
     };
-    if (ntiles > 0) load_row(0, raw);
+    // this thread's 256 bytes of window row sw*128 + e (tile sw of the window)
+    auto swa_row = [&](int sw) -> const uint4* {
+      const int sl = sw * kTileE + e;
+      return sl < wcnt ? reinterpret_cast<const uint4*>(swaseq + ((w0 + sl) % swa_ring) * kD) +
+                             16 * half
+                       : nullptr;
+    };
+    if (nmain > 0) load_row(0, raw);
     bool alive = true;
     for (int t = 0; t < ntiles && alive; ++t) {
+      if (t >= nmain) {
+        // ---- a tile of the SWA window: E4M3 -> fp16 (exact), two atoms per load ----
+        const uint4* src = swa_row(t - nmain);
+        if (t + 1 < ntiles)
+          if (const uint4* nx = swa_row(t + 1 - nmain))
+            for (int i = 0; i < 2; ++i) asm volatile("prefetch.global.L2 [%0];" ::"l"(nx + 8 * i));
+#pragma unroll 1
+        for (int ap = 0; ap < 2 && alive; ++ap) {
+          uint4 wv[8];
+#pragma unroll
+          for (int i = 0; i < 8; ++i) wv[i] = src ? __ldg(src + 8 * ap + i) : make_uint4(0, 0, 0, 0);
+#pragma unroll
+          for (int aj = 0; aj < 2; ++aj) {
+            const int ai = 2 * ap + aj;
+            const int a = half * 4 + ai;
+            if (t > 0 && aj == 0 && !mbar_wait(su32(&ctl.bar_o[a >> 1]), (t - 1) & 1, status)) {
+              alive = false;
+              break;
+            }
+#pragma unroll
+            for (int ci = 0; ci < 8; ++ci) {
+              // channels 8 ci .. 8 ci + 7 of atom a: bytes 8 (ci & 1) .. of wv[4 aj + ci / 2]
+              const uint4 u = wv[4 * aj + (ci >> 1)];
+              const uint32_t lo = (ci & 1) ? u.z : u.x, hi = (ci & 1) ? u.w : u.y;
+              const uint32_t off = L::v_off + (uint32_t)a * L::v_atom +
+                                   (uint32_t)(e >> 3) * 1024u + (uint32_t)(e & 7) * 128u +
+                                   (uint32_t)((ci ^ (e & 7)) << 4);
+              *reinterpret_cast<uint4*>(smem + off) =
+                  make_uint4(e4m3x2_to_f16x2((uint16_t)(lo & 0xFFFFu)),
+                             e4m3x2_to_f16x2((uint16_t)(lo >> 16)),
+                             e4m3x2_to_f16x2((uint16_t)(hi & 0xFFFFu)),
+                             e4m3x2_to_f16x2((uint16_t)(hi >> 16)));
+            }
+            proxy_fence();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(su32(&ctl.bar_v[a]));
+          }
+        }
+        continue;
+      }
       uint4 nxt[9];
-      if (t + 1 < ntiles) {
+      if (t + 1 < nmain) {
         load_row(t + 1, nxt);
       } else {
+        if (t + 1 < ntiles)  // the window follows: bring its rows into L2 meanwhile
+          if (const uint4* nx = swa_row(0))
+            for (int i = 0; i < 2; ++i) asm volatile("prefetch.global.L2 [%0];" ::"l"(nx + 8 * i));
 #pragma unroll
         for (int i = 0; i < 9; ++i) nxt[i] = make_uint4(0, 0, 0, 0);
       }
@@ -301,8 +369,14 @@ sparse_attn_tc_kernel(const uint16_t* __restrict__ q_bf16, const uint8_t* __rest
       tmem_wait_ld();
       {
         const int sl = t * kTileE + e;
-        const int32_t j = sl < cnt ? slot_at(sl) : -1;
-        if (!(j >= 0 && j < N)) {
+        bool valid;
+        if (t < nmain) {
+          const int32_t j = sl < cnt ? slot_at(sl) : -1;
+          valid = j >= 0 && j < N;
+        } else {
+          valid = (t - nmain) * kTileE + e < wcnt;  // a window row
+        }
+        if (!valid) {
 #pragma unroll
           for (int i = 0; i < 32; ++i) s[i] = -INFINITY;
         }
@@ -458,32 +532,34 @@ static cudaError_t launch_tc_t(const uint16_t* q_bf16, const uint8_t* kv_fp4, in
                                int64_t kv_seq_stride, int q_per_seq, const int32_t* idx, int k,
                                int nsplit, int chunk, float scale_log2, float* out, float* lse,
                                float* part_o, float* part_lse, int32_t* status,
-                               cudaStream_t stream, bool pdl) {
+                               const SwaArgs* swa, cudaStream_t stream, bool pdl) {
   using L = TcLayout;
   cudaError_t e = cudaFuncSetAttribute(sparse_attn_tc_kernel<H>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)L::alloc);
   if (e != cudaSuccess) return e;
   return launch_kernel(sparse_attn_tc_kernel<H>, dim3((unsigned)nsplit, (unsigned)B),
                        dim3(kThreadsTc), L::alloc, stream, pdl, q_bf16, kv_fp4, N, kv_seq_stride,
-                       q_per_seq, idx, k, chunk, scale_log2, out, lse, part_o, part_lse, status);
+                       q_per_seq, idx, k, chunk, scale_log2, out, lse, part_o, part_lse, status,
+                       swa ? swa->kv : nullptr, swa ? swa->ring : (int64_t)0, swa ? swa->n_win : 0,
+                       swa ? swa->q_pos : nullptr);
 }
 
 cudaError_t launch_sparse_attn_tc(const uint16_t* q_bf16, const uint8_t* kv_fp4, int B, int H,
                                   int64_t N, int64_t kv_seq_stride, int q_per_seq,
                                   const int32_t* idx, int k, int nsplit, int chunk,
                                   float scale_log2, float* out, float* lse, float* part_o,
-                                  float* part_lse, int32_t* status, cudaStream_t stream,
-                                  bool pdl) {
+                                  float* part_lse, int32_t* status, const SwaArgs* swa,
+                                  cudaStream_t stream, bool pdl) {
   switch (H) {
     case 16:
       return launch_tc_t<16>(q_bf16, kv_fp4, B, N, kv_seq_stride, q_per_seq, idx, k, nsplit,
-                             chunk, scale_log2, out, lse, part_o, part_lse, status, stream, pdl);
+                             chunk, scale_log2, out, lse, part_o, part_lse, status, swa, stream, pdl);
     case 32:
       return launch_tc_t<32>(q_bf16, kv_fp4, B, N, kv_seq_stride, q_per_seq, idx, k, nsplit,
-                             chunk, scale_log2, out, lse, part_o, part_lse, status, stream, pdl);
+                             chunk, scale_log2, out, lse, part_o, part_lse, status, swa, stream, pdl);
     default:
       return launch_tc_t<64>(q_bf16, kv_fp4, B, N, kv_seq_stride, q_per_seq, idx, k, nsplit,
-                             chunk, scale_log2, out, lse, part_o, part_lse, status, stream, pdl);
+                             chunk, scale_log2, out, lse, part_o, part_lse, status, swa, stream, pdl);
   }
 }
 

@@ -161,21 +161,31 @@ cudaError_t launch_block_pool(const float* scores, int B, int64_t N, const int32
                               int ratio, int block, int n_blocks, int32_t* pool, void* scratch,
                               cudaStream_t stream, bool pdl);
 
-// Sparse attention.  scratch: partial outputs when split over several CTAs.
+// The sliding window of a layer's SWA KV that a call also attends.
+struct SwaArgs {
+  const uint8_t* kv;     // E4M3 [S][ring][512]
+  int64_t ring;
+  int n_win;
+  const int32_t* q_pos;  // [B] query token positions
+};
+
+// Sparse attention (+ the SWA window when swa is non-null).  scratch:
+// attn_scratch_bytes(B, H, k) bytes (split-k partials).
 size_t attn_scratch_bytes(int B, int H, int k);
-int attn_launches(int B, int k);  // kernels one sparse-attention call launches
+int attn_launches(int B, int k);  // kernels one call launches
 cudaError_t launch_sparse_attn(const uint16_t* q_bf16, const uint8_t* kv_fp4, int B, int H,
                                int64_t N, int64_t kv_seq_stride, int q_per_seq, const int32_t* idx,
                                int k, float softmax_scale, float* out, float* lse, void* scratch,
-                               int32_t* status, cudaStream_t stream, bool pdl = false);
+                               int32_t* status, cudaStream_t stream, bool pdl = false,
+                               const SwaArgs* swa = nullptr);
 
 // tcgen05 kernel of one sparse-attention call (partials when nsplit > 1).
 cudaError_t launch_sparse_attn_tc(const uint16_t* q_bf16, const uint8_t* kv_fp4, int B, int H,
                                   int64_t N, int64_t kv_seq_stride, int q_per_seq,
                                   const int32_t* idx, int k, int nsplit, int chunk,
                                   float scale_log2, float* out, float* lse, float* part_o,
-                                  float* part_lse, int32_t* status, cudaStream_t stream,
-                                  bool pdl);
+                                  float* part_lse, int32_t* status, const SwaArgs* swa,
+                                  cudaStream_t stream, bool pdl);
 
 int device_sm_count();
 

@@ -43,6 +43,7 @@ TENSOR_KV = 1
 TENSOR_KI = 2
 TENSOR_QI = 3
 TENSOR_Q = 4
+TENSOR_SWA = 5
 
 
 def build(force: bool = False) -> str:
@@ -153,6 +154,8 @@ class Workload:
     pool: int = 0          # hierarchical candidate pool size (0 = flat indexer)
     pool_block: int = 0    # > 1: blockwise pool of pool / pool_block blocks (else top-pool)
     float_indexer: bool = False          # bf16 N(0,1) indexer inputs instead of integers
+    n_win: int = 0         # SWA window of every layer (0: no SWA branch)
+    swa_ring: int = 0      # rows of each sequence's SWA KV ring
 
     @property
     def n_seq(self) -> int:
@@ -208,6 +211,13 @@ class Workload:
         key = stream_key(self.workload_id, self.seed_of_seq(s), TENSOR_KI)
         vals = self._indexer_values(key, 0, self.N * self.D_I)
         return float_to_e4m3_bytes(vals).reshape(self.N, self.D_I)
+
+    def swa_kv(self, layer: int, s: int) -> np.ndarray:
+        """E4M3 bytes [swa_ring][D] of layer `layer`'s SWA KV ring of sequence s
+        (token t at row t mod swa_ring): N(0,1) latents cast to E4M3."""
+        key = stream_key(self.workload_id, self.seed_of_seq(s), TENSOR_SWA, layer)
+        vals = normal_f32(key, 0, self.swa_ring * self.D)
+        return float_to_e4m3_bytes(vals).reshape(self.swa_ring, self.D)
 
     # --- per-query, per-layer tensors --------------------------------------
     def qi_fp8(self, layer: int, qs: Optional[Sequence[int]] = None) -> np.ndarray:
@@ -265,8 +275,11 @@ HIER_1M = Workload("hier_pool8192_b16_ctx1m", 4, B=16, N=262144, H=64, H_I=8, k=
 HIER_BLOCK_1M = Workload("hier_block2048x8_b16_ctx1m", 6, B=16, N=262144, H=64, H_I=8, k=2048,
                          seeds=tuple(_seeds(6000, 16)), modes=(FULL, REINDEX, REINDEX, REINDEX),
                          pool=16384, pool_block=8)
+# Decode with every query's own 128-token SWA window in the same softmax.
+DECODE_64K_SWA = Workload("decode_swa128_b32_ctx64k", 7, B=32, N=16384, H=64, H_I=8, k=2048,
+                          seeds=tuple(_seeds(7000, 32)), n_win=128, swa_ring=128)
 PREFILL_128K = Workload("prefill_4096q_ctx128k", 5, B=4096, N=32768, H=64, H_I=8, k=2048,
                         q_per_seq=4096, seeds=(5000,), first_pos=126976, float_indexer=True)
 
 WORKLOADS = {w.name: w for w in (TINY_FULL, DECODE_64K, GROUP_128K, HIER_1M, PREFILL_128K,
-                                  HIER_BLOCK_1M)}
+                                  HIER_BLOCK_1M, DECODE_64K_SWA)}

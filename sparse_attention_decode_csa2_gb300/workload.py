@@ -24,6 +24,7 @@ class DeviceInputs:
     q: List[torch.Tensor]           # int16 (bf16 bits) [B][H][D] per layer
     qi: List[Optional[torch.Tensor]]  # uint8 [B][H_I][D_I] per layer (None for REUSE)
     q_pos: torch.Tensor             # int32 [B]
+    swa: Optional[List[torch.Tensor]] = None  # uint8 E4M3 [S][ring][D] per layer (n_win > 0)
 
     @property
     def scale(self) -> float:
@@ -33,7 +34,8 @@ class DeviceInputs:
         w = self.w
         return csa2.LayerGroup(w.modes, self.q, self.qi, self.kv_fp4, self.ki_fp8, w.N,
                                w.kv_seq_stride, w.q_per_seq, self.q_pos, w.ratio, w.k, w.pool,
-                               self.scale, pool_block=w.pool_block, **kw)
+                               self.scale, pool_block=w.pool_block, swa_kv=self.swa,
+                               n_win=w.n_win, **kw)
 
 
 def _to_dev(a: np.ndarray, device, dtype=None) -> torch.Tensor:
@@ -62,4 +64,7 @@ def prepare(w: Workload, device="cuda", layers: Optional[int] = None) -> DeviceI
     q = [_to_dev(w.q_bf16(l).view(np.int16), device) for l in range(L)]
     qi = [None if w.modes[l] == REUSE else _to_dev(w.qi_fp8(l), device) for l in range(L)]
     q_pos = _to_dev(w.q_pos(), device)
-    return DeviceInputs(w, kv, ki, q, qi, q_pos)
+    swa = None
+    if w.n_win > 0:
+        swa = [_to_dev(np.stack([w.swa_kv(l, s) for s in range(S)]), device) for l in range(L)]
+    return DeviceInputs(w, kv, ki, q, qi, q_pos, swa)

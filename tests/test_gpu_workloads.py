@@ -1,4 +1,4 @@
-"""Parity of the whole CSA2 path at the six workloads' full sizes, in the
+"""Parity of the whole CSA2 path at the seven workloads' full sizes, in the
 launch configuration the benchmark times (csa2_layer_group over the
 device-resident cache).  The oracle recomputes sampled queries one by one:
 their FP4 rows (from the same seeded latent), indexer scores, top-k / pool
@@ -13,7 +13,8 @@ from helpers import assert_attn_close, assert_float_selection_ok, assert_lse_clo
 pytestmark = pytest.mark.gpu
 
 NAMES = ["tiny_full_1q_ctx4k", "decode_b32_ctx64k", "group_full_reindex_reuse_b64_ctx128k",
-         "hier_pool8192_b16_ctx1m", "prefill_4096q_ctx128k", "hier_block2048x8_b16_ctx1m"]
+         "hier_pool8192_b16_ctx1m", "prefill_4096q_ctx128k", "hier_block2048x8_b16_ctx1m",
+         "decode_swa128_b32_ctx64k"]
 
 
 def _sample(B, n):
@@ -37,7 +38,7 @@ def test_workload_parity(name):
     code, bits = csa2.read_status(lg.ws)
     assert code == 0, bits
     pos = w.q_pos()
-    n_samples = {1: 1, 2: 4, 3: 3, 4: 3, 5: 6, 6: 3}[w.workload_id]
+    n_samples = {1: 1, 2: 4, 3: 3, 4: 3, 5: 6, 6: 3, 7: 4}[w.workload_id]
     for q in _sample(w.B, n_samples):
         s = q // w.q_per_seq
         ki = w.ki_fp8(s)
@@ -82,7 +83,12 @@ def test_workload_parity(name):
         kv_sparse[rows] = ref_rows
         for l in range(len(w.modes)):
             ql = w.q_bf16(l, [q])
-            ref_o, ref_l = oracle.sparse_attn(ql, kv_sparse, w.N, 0, 1, attended[l][None],
-                                              inp.scale)
+            if w.n_win:
+                ref_o, ref_l = oracle.sparse_attn_swa(ql, kv_sparse, w.N, 0, 1, attended[l][None],
+                                                      w.swa_kv(l, s)[None], w.swa_ring, w.n_win,
+                                                      qpos, inp.scale)
+            else:
+                ref_o, ref_l = oracle.sparse_attn(ql, kv_sparse, w.N, 0, 1, attended[l][None],
+                                                  inp.scale)
             assert_attn_close(outs[l][q].cpu().numpy(), ref_o[0], (name, q, l))
             assert_lse_close(lses[l][q].cpu().numpy(), ref_l[0], (name, q, l))
