@@ -278,8 +278,15 @@ HIER_BLOCK_1M = Workload("hier_block2048x8_b16_ctx1m", 6, B=16, N=262144, H=64, 
 # Decode with every query's own 128-token SWA window in the same softmax.
 DECODE_64K_SWA = Workload("decode_swa128_b32_ctx64k", 7, B=32, N=16384, H=64, H_I=8, k=2048,
                           seeds=tuple(_seeds(7000, 32)), n_win=128, swa_ring=128)
+# The pages' production decoder: 20 CSA2 layers at m = 1 in five groups of four
+# (Full + 3 Reuse, then Reindex + 3 Reuse four times), indexer 32 heads x 128,
+# top-k 512, blockwise pool of at most 2048 blocks x 8, SWA window 128.
+DECODER20 = Workload("decoder20_prod_b32_ctx64k", 8, B=32, N=65536, H=64, H_I=32, D_I=128, k=512,
+                     ratio=1, seeds=tuple(_seeds(8000, 32)),
+                     modes=(FULL, REUSE, REUSE, REUSE) + (REINDEX, REUSE, REUSE, REUSE) * 4,
+                     pool=16384, pool_block=8, n_win=128, swa_ring=128)
 PREFILL_128K = Workload("prefill_4096q_ctx128k", 5, B=4096, N=32768, H=64, H_I=8, k=2048,
                         q_per_seq=4096, seeds=(5000,), first_pos=126976, float_indexer=True)
 
 WORKLOADS = {w.name: w for w in (TINY_FULL, DECODE_64K, GROUP_128K, HIER_1M, PREFILL_128K,
-                                  HIER_BLOCK_1M, DECODE_64K_SWA)}
+                                  HIER_BLOCK_1M, DECODE_64K_SWA, DECODER20)}
