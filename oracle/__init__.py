@@ -63,11 +63,18 @@ def _load():
                 "orc_sparse_attn": (None, [vp, vp, i32, i32, i32, i64, i64, i32, vp, i32, dbl,
                                            vp, vp]),
                 "orc_block_pool": (None, [vp, i32, i64, vp, i32, i32, i32, vp]),
+                "orc_e8m0_value": (dbl, [i32]),
+                "orc_mxfp4_row_bytes": (i64, [i32]),
+                "orc_quantize_mxfp4": (None, [vp, i64, i32, vp]),
+                "orc_index_scores_fmt": (None, [vp, vp, i32, i32, i32, i64, i64, i32, vp, i32, i32,
+                                                vp]),
+                "orc_hier_pool_index_fmt": (None, [vp, vp, i32, i32, i32, i64, i64, i32, vp, i32,
+                                                   i32, i32, vp]),
                 "orc_sparse_attn_swa": (None, [vp, vp, i32, i32, i32, i64, i64, i32, vp, i32, vp,
                                                i64, i32, vp, dbl, vp, vp]),
                 "orc_layer_group": (i32, [i32, vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32,
                                           i32, i64, i64, i32, vp, i32, i32, i32, i32, vp, vp,
-                                          i64, i32, dbl]),
+                                          i64, i32, i32, dbl]),
             }
             for name, (res, args) in sig.items():
                 f = getattr(lib, name)
@@ -153,6 +160,52 @@ def topk(scores, k: int, q_pos=None, ratio: int = 1) -> np.ndarray:
     return out
 
 
+# --- MXFP4 indexer rows (walkthrough 1.(5).4: OCP MXFP4 indexer q and K) ---
+
+def e8m0_value(byte: int) -> float:
+    return _load().orc_e8m0_value(int(byte))
+
+
+def mxfp4_row_bytes(d: int) -> int:
+    return int(_load().orc_mxfp4_row_bytes(d))
+
+
+def quantize_mxfp4(x: np.ndarray) -> np.ndarray:
+    """fp32 [..., d] (d % 32 == 0) -> uint8 [..., d/2 + d/32] OCP MXFP4 rows."""
+    x = _c(x, np.float32)
+    d = x.shape[-1]
+    rows = x.reshape(-1, d)
+    out = np.empty((rows.shape[0], mxfp4_row_bytes(d)), dtype=np.uint8)
+    _load().orc_quantize_mxfp4(_ptr(rows), rows.shape[0], d, _ptr(out))
+    return out.reshape(x.shape[:-1] + (out.shape[-1],))
+
+
+def index_scores_mxfp4(q_mx, k_mx, D_I: int, N: int, kv_seq_stride: int, q_per_seq: int, q_pos,
+                       ratio: int):
+    """MXFP4 q [B][H_I][row], K [S*stride][row] -> fp64 scores [B][N] (R3 with R11)."""
+    q_mx = _c(q_mx, np.uint8)
+    k_mx = _c(k_mx, np.uint8)
+    B, H_I = q_mx.shape[0], q_mx.shape[1]
+    qp = None if q_pos is None else _c(q_pos, np.int32)
+    out = np.empty((B, N), dtype=np.float64)
+    _load().orc_index_scores_fmt(_ptr(q_mx), _ptr(k_mx), B, H_I, D_I, N, kv_seq_stride, q_per_seq,
+                                 _ptr(qp), ratio, 1, _ptr(out))
+    return out
+
+
+def hier_pool_index_mxfp4(q_mx, k_mx, D_I: int, N: int, kv_seq_stride: int, q_per_seq: int,
+                          pool, k: int):
+    q_mx = _c(q_mx, np.uint8)
+    k_mx = _c(k_mx, np.uint8)
+    pool = _c(pool, np.int32)
+    B, H_I = q_mx.shape[0], q_mx.shape[1]
+    P = pool.shape[1]
+    out = np.empty((B, k), dtype=np.int32)
+    _load().orc_hier_pool_index_fmt(_ptr(q_mx), _ptr(k_mx), B, H_I, D_I, N, kv_seq_stride,
+                                    q_per_seq, _ptr(pool), P, k, 1, _ptr(out))
+    return out
+
+
 def block_pool(scores, block: int, n_blocks: int, q_pos=None, ratio: int = 1) -> np.ndarray:
     """Blockwise candidate pool of the Hierarchical Sparse Indexer (walkthrough
     1.(4).2): scores [B][N] -> int32 pool [B][n_blocks * block]."""
@@ -214,7 +267,8 @@ def sparse_attn_swa(q_bf16, kv_fp4, N: int, kv_seq_stride: int, q_per_seq: int, 
 def layer_group(modes: Sequence[int], q_bf16: Sequence[np.ndarray], qi_fp8: Sequence[np.ndarray],
                 kv_fp4, ki_fp8, N: int, kv_seq_stride: int, q_per_seq: int, q_pos, ratio: int,
                 k: int, pool_size: int, scale: float, pool_block: int = 0,
-                swa_kv: Optional[Sequence[np.ndarray]] = None, swa_ring: int = 0, n_win: int = 0):
+                swa_kv: Optional[Sequence[np.ndarray]] = None, swa_ring: int = 0, n_win: int = 0,
+                indexer_fmt: int = 0, D_I: Optional[int] = None):
     """Runs the layer schedule (walkthrough 1.(4).1 and 1.(4).2).  pool_block > 0
     builds the blockwise pool (pool_size / pool_block blocks of pool_block entries).
 
@@ -222,7 +276,7 @@ def layer_group(modes: Sequence[int], q_bf16: Sequence[np.ndarray], qi_fp8: Sequ
     L = len(modes)
     q_bf16 = [_c(q, np.uint16) for q in q_bf16]
     B, H, D = q_bf16[0].shape
-    H_I, D_I = None, None
+    H_I = None
     qis = []
     for l in range(L):
         qi = qi_fp8[l]
@@ -230,7 +284,9 @@ def layer_group(modes: Sequence[int], q_bf16: Sequence[np.ndarray], qi_fp8: Sequ
             qis.append(None)
         else:
             qi = _c(qi, np.uint8)
-            H_I, D_I = qi.shape[1], qi.shape[2]
+            H_I = qi.shape[1]
+            if D_I is None:
+                D_I = qi.shape[2]
             qis.append(qi)
     kv_fp4 = _c(kv_fp4, np.uint8)
     ki_fp8 = _c(ki_fp8, np.uint8)
@@ -247,7 +303,7 @@ def layer_group(modes: Sequence[int], q_bf16: Sequence[np.ndarray], qi_fp8: Sequ
                                  arr(idxs), _ptr(kv_fp4), _ptr(ki_fp8), B, H, H_I, D, D_I, N,
                                  kv_seq_stride, q_per_seq, _ptr(qp), ratio, k, pool_size,
                                  pool_block, _ptr(pool), None if swas is None else arr(swas),
-                                 swa_ring, n_win, float(scale))
+                                 swa_ring, n_win, indexer_fmt, float(scale))
     if rc != 0:
         raise ValueError("invalid layer schedule")
     return outs, lses, idxs, (pool if pool_size > 0 else None)

@@ -26,6 +26,8 @@
  *        per 16 channels, no second-level global scale, largest magnitude
  *        448 x 6 = 2688, quantised after RoPE, dequantised before attention.
  *  [P4e] same page, 2.(2).1 "Model settings": 64 main query heads of 512 dims.
+ *  [P4f] same page, 1.(5).4: the indexer query and key are FP4 in the OCP
+ *        MXFP4 format.
  *
  * Readings where the pages are silent (each is also listed in the design doc):
  *  R1  scale byte = E4M3(absmax/6) rounded to nearest even, saturating at 448;
@@ -58,6 +60,13 @@
  *      The query at position pos attends tokens max(0, pos - n_win + 1) ..
  *      pos (its own token included) together with its selected entries, in
  *      one softmax; K = V = the decoded latent, same scale.
+ *  R11 MXFP4 indexer [P4d] (indexer q and K in OCP MXFP4): per block of 32
+ *      values, shared exponent = floor(log2(absmax)) - 2 (2 = the largest
+ *      E2M1 exponent), clamped to the E8M0 range, scale 2^shared; elements
+ *      E2M1 nearest to value / scale (an exact quotient), ties to the even
+ *      code, saturating at 6; sign bit = sign of the value; an all-zero block
+ *      takes scale byte 0.  Row: D/2 code bytes (element 2j in the low nibble
+ *      of byte j) then D/32 scale bytes (E8M0, 2^(byte - 127)).
  *  R9  blockwise candidate pool [P4c]: entries are cut into aligned blocks of
  *      `block` consecutive entries; a block's score is the largest score of
  *      its visible entries (a block without one is no candidate); the
@@ -181,6 +190,55 @@ void orc_dequantize_row(const uint8_t* row, int d, double* out) {
   }
 }
 
+/* ---------------------------------------------------------------------- */
+/* MXFP4 indexer rows [P4f], reading R11                                   */
+/* ---------------------------------------------------------------------- */
+
+/* E8M0 (OCP MX shared scale): 2^(byte - 127); 0xFF (NaN) is never written. */
+double orc_e8m0_value(int byte) { return ldexp(1.0, byte - 127); }
+
+int64_t orc_mxfp4_row_bytes(int d) { return d / 2 + d / 32; }
+
+/* x: fp32 [n_rows][d] -> out: [n_rows][d/2 + d/32].  d % 32 == 0. */
+void orc_quantize_mxfp4(const float* x, int64_t n_rows, int d, uint8_t* out) {
+  int64_t rb = orc_mxfp4_row_bytes(d);
+  for (int64_t r = 0; r < n_rows; ++r) {
+    const float* xr = x + r * d;
+    uint8_t* codes = out + r * rb;
+    uint8_t* scales = codes + d / 2;
+    memset(codes, 0, (size_t)(d / 2));
+    for (int b = 0; b < d / 32; ++b) {
+      double amax = 0.0;
+      for (int i = 0; i < 32; ++i) amax = fmax(amax, fabs((double)xr[32 * b + i]));
+      int shared = -127;
+      if (amax > 0.0) {
+        int e;
+        frexp(amax, &e);           /* amax = m 2^e, m in [0.5, 1): floor(log2 amax) = e - 1 */
+        shared = (e - 1) - 2;
+        if (shared < -127) shared = -127;
+        if (shared > 127) shared = 127;
+      }
+      scales[b] = (uint8_t)(shared + 127);
+      double X = ldexp(1.0, shared);
+      for (int i = 0; i < 32; ++i) {
+        int ch = 32 * b + i;
+        double xv = (double)xr[ch];
+        int mag = orc_e2m1_encode_magnitude(fabs(xv) / X); /* exact: X is a power of two */
+        int code = (signbit(xv) ? 8 : 0) | mag;
+        codes[ch / 2] |= (uint8_t)((ch & 1) ? (code << 4) : code);
+      }
+    }
+  }
+}
+
+void orc_dequantize_mxfp4_row(const uint8_t* row, int d, double* out) {
+  const uint8_t* scales = row + d / 2;
+  for (int ch = 0; ch < d; ++ch) {
+    int code = (ch & 1) ? (row[ch / 2] >> 4) : (row[ch / 2] & 15);
+    out[ch] = orc_e2m1_value(code) * orc_e8m0_value(scales[ch / 32]);
+  }
+}
+
 void orc_dequantize_kv_fp4(const uint8_t* rows, int64_t n_rows, int d, double* out) {
   int64_t rb = orc_fp4_row_bytes(d);
   for (int64_t r = 0; r < n_rows; ++r) orc_dequantize_row(rows + r * rb, d, out + r * d);
@@ -206,21 +264,35 @@ int64_t orc_n_visible(const int32_t* q_pos, int q, int ratio, int64_t N) {
 /* scores[q][j] = sum_h sum_d qI[q][h][d] * KI[seq(q)][j][d] for visible j,
  * -inf otherwise.  q_fp8 [B][H_I][D_I], k_fp8 [S][N][D_I] (sequence s at
  * offset s * kv_seq_stride entries), scores [B][N]. */
-void orc_index_scores(const uint8_t* q_fp8, const uint8_t* k_fp8, int B, int H_I, int D_I,
-                      int64_t N, int64_t kv_seq_stride, int q_per_seq, const int32_t* q_pos,
-                      int ratio, double* scores) {
+/* Indexer rows: fmt 0 = E4M3 [D_I] bytes, fmt 1 = MXFP4 (R11). */
+static int64_t idx_row_bytes(int D_I, int fmt) {
+  return fmt ? orc_mxfp4_row_bytes(D_I) : D_I;
+}
+static void idx_row_values(const uint8_t* row, int D_I, int fmt, double* out) {
+  if (fmt) {
+    orc_dequantize_mxfp4_row(row, D_I, out);
+  } else {
+    for (int d = 0; d < D_I; ++d) out[d] = orc_e4m3_value(row[d]);
+  }
+}
+
+void orc_index_scores_fmt(const uint8_t* q_fp8, const uint8_t* k_fp8, int B, int H_I, int D_I,
+                          int64_t N, int64_t kv_seq_stride, int q_per_seq, const int32_t* q_pos,
+                          int ratio, int fmt, double* scores) {
+  int64_t rb = idx_row_bytes(D_I, fmt);
   double* kj = (double*)malloc(sizeof(double) * D_I);
   double* qv = (double*)malloc(sizeof(double) * H_I * D_I);
   for (int q = 0; q < B; ++q) {
-    const uint8_t* kseq = k_fp8 + (int64_t)(q / q_per_seq) * kv_seq_stride * D_I;
+    const uint8_t* kseq = k_fp8 + (int64_t)(q / q_per_seq) * kv_seq_stride * rb;
     int64_t nv = orc_n_visible(q_pos, q, ratio, N);
-    for (int i = 0; i < H_I * D_I; ++i) qv[i] = orc_e4m3_value(q_fp8[(int64_t)q * H_I * D_I + i]);
+    for (int h = 0; h < H_I; ++h)
+      idx_row_values(q_fp8 + ((int64_t)q * H_I + h) * rb, D_I, fmt, qv + (int64_t)h * D_I);
     for (int64_t j = 0; j < N; ++j) {
       if (j >= nv) {
         scores[(int64_t)q * N + j] = -INFINITY;
         continue;
       }
-      for (int d = 0; d < D_I; ++d) kj[d] = orc_e4m3_value(kseq[j * D_I + d]);
+      idx_row_values(kseq + j * rb, D_I, fmt, kj);
       double s = 0.0;
       for (int h = 0; h < H_I; ++h) {
         double dot = 0.0;
@@ -232,6 +304,13 @@ void orc_index_scores(const uint8_t* q_fp8, const uint8_t* k_fp8, int B, int H_I
   }
   free(kj);
   free(qv);
+}
+
+void orc_index_scores(const uint8_t* q_fp8, const uint8_t* k_fp8, int B, int H_I, int D_I,
+                      int64_t N, int64_t kv_seq_stride, int q_per_seq, const int32_t* q_pos,
+                      int ratio, double* scores) {
+  orc_index_scores_fmt(q_fp8, k_fp8, B, H_I, D_I, N, kv_seq_stride, q_per_seq, q_pos, ratio, 0,
+                       scores);
 }
 
 /* ---------------------------------------------------------------------- */
@@ -323,23 +402,26 @@ void orc_block_pool(const double* scores, int B, int64_t N, const int32_t* q_pos
 
 /* For each query, score only the entries listed in pool[q][0..P) (-1 slots
  * skipped) and keep the top-k of them by (score desc, entry id asc). */
-void orc_hier_pool_index(const uint8_t* q_fp8, const uint8_t* k_fp8, int B, int H_I, int D_I,
-                         int64_t N, int64_t kv_seq_stride, int q_per_seq, const int32_t* pool,
-                         int P, int k, int32_t* idx) {
+void orc_hier_pool_index_fmt(const uint8_t* q_fp8, const uint8_t* k_fp8, int B, int H_I, int D_I,
+                             int64_t N, int64_t kv_seq_stride, int q_per_seq, const int32_t* pool,
+                             int P, int k, int fmt, int32_t* idx) {
+  int64_t rb = idx_row_bytes(D_I, fmt);
   cand_t* c = (cand_t*)malloc(sizeof(cand_t) * (P > 0 ? P : 1));
   double* qv = (double*)malloc(sizeof(double) * H_I * D_I);
+  double* kj = (double*)malloc(sizeof(double) * D_I);
   for (int q = 0; q < B; ++q) {
-    const uint8_t* kseq = k_fp8 + (int64_t)(q / q_per_seq) * kv_seq_stride * D_I;
-    for (int i = 0; i < H_I * D_I; ++i) qv[i] = orc_e4m3_value(q_fp8[(int64_t)q * H_I * D_I + i]);
+    const uint8_t* kseq = k_fp8 + (int64_t)(q / q_per_seq) * kv_seq_stride * rb;
+    for (int h = 0; h < H_I; ++h)
+      idx_row_values(q_fp8 + ((int64_t)q * H_I + h) * rb, D_I, fmt, qv + (int64_t)h * D_I);
     int64_t n = 0;
     for (int p = 0; p < P; ++p) {
       int32_t j = pool[(int64_t)q * P + p];
       if (j < 0 || j >= N) continue;
+      idx_row_values(kseq + (int64_t)j * rb, D_I, fmt, kj);
       double s = 0.0;
       for (int h = 0; h < H_I; ++h) {
         double dot = 0.0;
-        for (int d = 0; d < D_I; ++d)
-          dot += qv[h * D_I + d] * orc_e4m3_value(kseq[(int64_t)j * D_I + d]);
+        for (int d = 0; d < D_I; ++d) dot += qv[h * D_I + d] * kj[d];
         s += dot;
       }
       c[n].s = s;
@@ -350,6 +432,14 @@ void orc_hier_pool_index(const uint8_t* q_fp8, const uint8_t* k_fp8, int B, int 
   }
   free(c);
   free(qv);
+  free(kj);
+}
+
+void orc_hier_pool_index(const uint8_t* q_fp8, const uint8_t* k_fp8, int B, int H_I, int D_I,
+                         int64_t N, int64_t kv_seq_stride, int q_per_seq, const int32_t* pool,
+                         int P, int k, int32_t* idx) {
+  orc_hier_pool_index_fmt(q_fp8, k_fp8, B, H_I, D_I, N, kv_seq_stride, q_per_seq, pool, P, k, 0,
+                          idx);
 }
 
 /* ---------------------------------------------------------------------- */
@@ -450,6 +540,7 @@ enum { ORC_FULL = 0, ORC_REINDEX = 1, ORC_REUSE = 2 };
  *   qi_fp8[l]         [B][H_I][D_I] indexer query (ignored for REUSE)
  *   out[l], lse[l]    [B][H][D], [B][H] outputs (lse may be NULL)
  *   idx_out[l]        [B][k] indices layer l attended (written for every layer)
+ *   indexer_fmt       0: indexer q / K in E4M3 [D_I]; 1: in MXFP4 rows (R11)
  *   swa_kv[l]         E4M3 [S][swa_ring][D] SWA KV of layer l (R10), or NULL;
  *                     with n_win > 0 each layer also attends its window
  *   pool_out          [B][pool_size] when pool_size > 0 (built by FULL layers):
@@ -463,7 +554,7 @@ int orc_layer_group(int n_layers, const int* modes, const uint16_t* const* q_bf1
                     int H, int H_I, int D, int D_I, int64_t N, int64_t kv_seq_stride,
                     int q_per_seq, const int32_t* q_pos, int ratio, int k, int pool_size,
                     int pool_block, int32_t* pool_out, const uint8_t* const* swa_kv,
-                    int64_t swa_ring, int n_win, double scale) {
+                    int64_t swa_ring, int n_win, int indexer_fmt, double scale) {
   if (n_layers < 1 || modes[0] != ORC_FULL) return -1;
   if (pool_block < 0 || (pool_block > 0 && pool_size % pool_block != 0)) return -1;
   double* scores = (double*)malloc(sizeof(double) * (size_t)B * (size_t)(N > 0 ? N : 1));
@@ -471,8 +562,8 @@ int orc_layer_group(int n_layers, const int* modes, const uint16_t* const* q_bf1
   for (int l = 0; l < n_layers; ++l) {
     int32_t* idx = idx_out[l];
     if (modes[l] == ORC_FULL) {
-      orc_index_scores(qi_fp8[l], ki_fp8, B, H_I, D_I, N, kv_seq_stride, q_per_seq, q_pos, ratio,
-                       scores);
+      orc_index_scores_fmt(qi_fp8[l], ki_fp8, B, H_I, D_I, N, kv_seq_stride, q_per_seq, q_pos,
+                           ratio, indexer_fmt, scores);
       orc_topk(scores, B, N, k, q_pos, ratio, idx);
       if (pool_size > 0 && pool_block == 0)
         orc_topk(scores, B, N, pool_size, q_pos, ratio, pool_out);
@@ -481,11 +572,11 @@ int orc_layer_group(int n_layers, const int* modes, const uint16_t* const* q_bf1
       latest = idx;
     } else if (modes[l] == ORC_REINDEX) {
       if (pool_size > 0) {
-        orc_hier_pool_index(qi_fp8[l], ki_fp8, B, H_I, D_I, N, kv_seq_stride, q_per_seq, pool_out,
-                            pool_size, k, idx);
+        orc_hier_pool_index_fmt(qi_fp8[l], ki_fp8, B, H_I, D_I, N, kv_seq_stride, q_per_seq,
+                                pool_out, pool_size, k, indexer_fmt, idx);
       } else {
-        orc_index_scores(qi_fp8[l], ki_fp8, B, H_I, D_I, N, kv_seq_stride, q_per_seq, q_pos,
-                         ratio, scores);
+        orc_index_scores_fmt(qi_fp8[l], ki_fp8, B, H_I, D_I, N, kv_seq_stride, q_per_seq, q_pos,
+                             ratio, indexer_fmt, scores);
         orc_topk(scores, B, N, k, q_pos, ratio, idx);
       }
       latest = idx;
