@@ -62,6 +62,16 @@ typedef enum csa2_mode {
   CSA2_REUSE = 2     /* no indexer; reuses the latest FULL/REINDEX indices */
 } csa2_mode;
 
+/* Formats of the indexer query and key rows of a layer group. */
+typedef enum csa2_indexer_fmt {
+  CSA2_INDEXER_E4M3 = 0,   /* E4M3 [D_I] bytes per row */
+  CSA2_INDEXER_MXFP4 = 1   /* OCP MXFP4 rows of CSA2_MXFP4_ROW_BYTES(D_I) bytes */
+} csa2_indexer_fmt;
+
+/* Bytes of one MXFP4 indexer row of d elements: d/2 E2M1 code bytes then d/32
+ * E8M0 scale bytes (68 bytes at d = 128). */
+#define CSA2_MXFP4_ROW_BYTES(d) ((d) / 2 + (d) / 32)
+
 /* Bytes of one FP4 main-KV row of d channels: d/2 code bytes then d/16 scale bytes. */
 #define CSA2_FP4_ROW_BYTES(d) ((d) / 2 + (d) / 16)
 
@@ -108,6 +118,43 @@ csa2_status csa2_index_scores(const uint8_t* q_fp8, const uint8_t* k_fp8, int B,
                               int64_t N, int64_t kv_seq_stride, int q_per_seq,
                               const int32_t* q_pos, int ratio, float* scores,
                               cudaStream_t stream);
+
+/*
+ * csa2_quantize_mxfp4 -- writes MXFP4 indexer rows (walkthrough 1.(5).4: the
+ * indexer query and key are FP4 in the OCP MXFP4 format: blocks of 32 E2M1
+ * elements sharing one E8M0 power-of-two scale).
+ *   x      fp32 [n_rows][d], finite values; d a multiple of 32, <= 4096;
+ *          16-byte aligned
+ *   out    uint8 [n_rows][d/2 + d/32]: byte j of a row holds element 2j in its
+ *          low nibble and 2j+1 in its high nibble; then one E8M0 byte per
+ *          32-element block b (2^(byte - 127))
+ *   Per block: shared exponent e = floor(log2(absmax)) - 2 (2 is the largest
+ *   E2M1 exponent) clamped to >= -127, scale byte e + 127 (0 for an all-zero
+ *   block); each code = the E2M1 value nearest to the exact |x| / 2^e (ties to
+ *   the even code), saturating at 6; sign bit = sign bit of x.  Bit-exact.
+ */
+csa2_status csa2_quantize_mxfp4(const float* x, int64_t n_rows, int d, uint8_t* out,
+                                cudaStream_t stream);
+
+/*
+ * csa2_index_scores_mxfp4 -- the lightweight indexer with MXFP4 query and key
+ * (walkthrough 1.(4) "CSA2" and 1.(5).4).
+ *   q_mx     MXFP4 [B][H_I][68] indexer queries (D_I = 128)
+ *   k_mx     MXFP4 [S][N][68] indexer keys (sequence s at entry offset
+ *            s * kv_seq_stride); 16-byte aligned, and kv_seq_stride a multiple
+ *            of 4 when there is more than one sequence
+ *   scores   fp32 [B][N]: sum_h sum_d value(q[q][h][d]) * value(k[s][j][d]) for
+ *            visible j, -inf for invisible j
+ *   The head sum of the decoded query is formed first (compensated fp32
+ *   summation); the dot product with each key accumulates fp32 products of
+ *   exact decoded values, scaled per 32-element block.  Scores are therefore
+ *   fp32 approximations of the exact sum (relative error of the order of
+ *   2^-20 of the sum of absolute products).  D_I must be 128, 1 <= H_I <= 64.
+ */
+csa2_status csa2_index_scores_mxfp4(const uint8_t* q_mx, const uint8_t* k_mx, int B, int H_I,
+                                    int D_I, int64_t N, int64_t kv_seq_stride, int q_per_seq,
+                                    const int32_t* q_pos, int ratio, float* scores,
+                                    cudaStream_t stream);
 
 /*
  * csa2_topk -- per-query top-k selection (walkthrough 1.(4) "CSA2": the top-k
@@ -179,6 +226,16 @@ csa2_status csa2_hier_pool_index(const uint8_t* q_fp8, const uint8_t* k_fp8, int
  *   A row with no valid slot yields out = 0 and lse = -inf.
  *   ws       at least csa2_workspace_size(B, 0, k, H, 0) bytes.
  */
+/*
+ * csa2_hier_pool_index_mxfp4 -- csa2_hier_pool_index with MXFP4 indexer rows
+ * (q_mx, k_mx as in csa2_index_scores_mxfp4); same pool, idx and workspace
+ * rules.
+ */
+csa2_status csa2_hier_pool_index_mxfp4(const uint8_t* q_mx, const uint8_t* k_mx, int B, int H_I,
+                                       int D_I, int64_t N, int64_t kv_seq_stride, int q_per_seq,
+                                       const int32_t* pool, int P, int k, int32_t* idx, void* ws,
+                                       size_t ws_bytes, cudaStream_t stream);
+
 csa2_status csa2_sparse_attn_fp4(const uint16_t* q_bf16, const uint8_t* kv_fp4, int B, int H,
                                  int D, int64_t N, int64_t kv_seq_stride, int q_per_seq,
                                  const int32_t* idx, int k, float softmax_scale, float* out,
@@ -245,7 +302,8 @@ csa2_status csa2_sparse_attn_fp4_noalloc(const uint16_t* q_bf16, const uint8_t* 
 typedef struct csa2_layer {
   int mode;                /* csa2_mode */
   const uint16_t* q_bf16;  /* bf16 [B][H][D] this layer's main query */
-  const uint8_t* qi_fp8;   /* E4M3 [B][H_I][D_I] indexer query; NULL for REUSE */
+  const uint8_t* qi_fp8;   /* [B][H_I][row] indexer query in the group's indexer format
+                              (E4M3 [D_I] or MXFP4 rows); NULL for REUSE */
   float* out;              /* fp32 [B][H][D] */
   float* lse;              /* fp32 [B][H] or NULL */
   int32_t* idx_out;        /* int32 [B][k]: indices this layer attended.  Required for
@@ -258,7 +316,7 @@ typedef struct csa2_layer {
 /* What the layers of one group share (walkthrough 1.(4).1). */
 typedef struct csa2_group_args {
   const uint8_t* kv_fp4;   /* [S][N][D/2 + D/16] shared FP4 main KV */
-  const uint8_t* ki_fp8;   /* [S][N][D_I] shared indexer K */
+  const uint8_t* ki_fp8;   /* [S][N][row] shared indexer K in the indexer format */
   int B, H, H_I, D, D_I;
   int64_t N, kv_seq_stride;
   int q_per_seq;
@@ -276,6 +334,7 @@ typedef struct csa2_group_args {
   int n_win;               /* SWA window; 0: no layer attends a window.  With n_win > 0
                               each layer with swa_kv also attends its window (q_pos
                               required, swa_ring >= n_win) */
+  int indexer_fmt;         /* csa2_indexer_fmt of qi_fp8 and ki_fp8 */
 } csa2_group_args;
 
 /*

@@ -57,7 +57,22 @@ class Csa2GroupArgs(ctypes.Structure):
                 ("q_per_seq", ctypes.c_int), ("q_pos", _vp), ("ratio", ctypes.c_int),
                 ("k", ctypes.c_int), ("pool_size", ctypes.c_int), ("pool_out", _vp),
                 ("softmax_scale", ctypes.c_float), ("pool_block", ctypes.c_int),
-                ("swa_ring", ctypes.c_int64), ("n_win", ctypes.c_int)]
+                ("swa_ring", ctypes.c_int64), ("n_win", ctypes.c_int),
+                ("indexer_fmt", ctypes.c_int)]
+
+
+INDEXER_E4M3, INDEXER_MXFP4 = 0, 1
+
+
+def mxfp4_row_bytes(d: int) -> int:
+    return d // 2 + d // 32
+
+
+def _mx_dim(row_bytes: int) -> int:
+    # an MXFP4 row of d elements has 17 d / 32 bytes
+    if row_bytes % 17:
+        raise ValueError(f"{row_bytes} bytes is not an MXFP4 row")
+    return row_bytes * 32 // 17
 
 
 _SIGS = {
@@ -67,6 +82,11 @@ _SIGS = {
     "csa2_quantize_kv_fp4": (_i32, [_vp, _i64, _i32, _vp, _vp]),
     "csa2_index_scores": (_i32, [_vp, _vp, _i32, _i32, _i32, _i64, _i64, _i32, _vp, _i32, _vp,
                                  _vp]),
+    "csa2_quantize_mxfp4": (_i32, [_vp, _i64, _i32, _vp, _vp]),
+    "csa2_index_scores_mxfp4": (_i32, [_vp, _vp, _i32, _i32, _i32, _i64, _i64, _i32, _vp, _i32,
+                                       _vp, _vp]),
+    "csa2_hier_pool_index_mxfp4": (_i32, [_vp, _vp, _i32, _i32, _i32, _i64, _i64, _i32, _vp,
+                                          _i32, _i32, _vp, _vp, _sz, _vp]),
     "csa2_topk": (_i32, [_vp, _i32, _i64, _i32, _vp, _i32, _vp, _vp, _sz, _vp]),
     "csa2_block_pool": (_i32, [_vp, _i32, _i64, _vp, _i32, _i32, _i32, _vp, _vp, _sz, _vp]),
     "csa2_block_pool_workspace_size": (_sz, [_i32, _i64, _i32, _i32]),
@@ -183,6 +203,57 @@ def index_scores(q_fp8: torch.Tensor, k_fp8: torch.Tensor, N: int, kv_seq_stride
     _check(lib.csa2_index_scores(_ptr(q_fp8), _ptr(k_fp8), B, H_I, D_I, N, kv_seq_stride,
                                  q_per_seq, _ptr(qp), ratio, _ptr(out), _stream()),
            "csa2_index_scores")
+    return out
+
+
+def quantize_mxfp4(x: torch.Tensor, out: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """fp32 [..., d] -> uint8 [..., d/2 + d/32] MXFP4 rows."""
+    x = _dev(x, torch.float32, "x")
+    d = x.shape[-1]
+    n = x.numel() // d
+    if out is None:
+        out = torch.empty(x.shape[:-1] + (mxfp4_row_bytes(d),), dtype=torch.uint8,
+                          device=x.device)
+    _dev(out, torch.uint8, "out")
+    _check(lib.csa2_quantize_mxfp4(_ptr(x), n, d, _ptr(out), _stream()), "csa2_quantize_mxfp4")
+    return out
+
+
+def index_scores_mxfp4(q_mx: torch.Tensor, k_mx: torch.Tensor, N: int, kv_seq_stride: int,
+                       q_per_seq: int, q_pos: Optional[torch.Tensor], ratio: int,
+                       out: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """MXFP4 q [B][H_I][68], MXFP4 K [S*stride][68] -> fp32 scores [B][N]."""
+    q_mx = _dev(q_mx, torch.uint8, "q_mx")
+    k_mx = _dev(k_mx, torch.uint8, "k_mx")
+    B, H_I, rb = q_mx.shape
+    if out is None:
+        out = torch.empty((B, N), dtype=torch.float32, device=q_mx.device)
+    _dev(out, torch.float32, "scores")
+    qp = _opt_pos(q_pos)
+    _check(lib.csa2_index_scores_mxfp4(_ptr(q_mx), _ptr(k_mx), B, H_I, _mx_dim(rb), N,
+                                       kv_seq_stride, q_per_seq, _ptr(qp), ratio, _ptr(out),
+                                       _stream()), "csa2_index_scores_mxfp4")
+    return out
+
+
+def hier_pool_index_mxfp4(q_mx: torch.Tensor, k_mx: torch.Tensor, N: int, kv_seq_stride: int,
+                          q_per_seq: int, pool: torch.Tensor, k: int,
+                          ws: Optional[torch.Tensor] = None,
+                          out: Optional[torch.Tensor] = None) -> torch.Tensor:
+    q_mx = _dev(q_mx, torch.uint8, "q_mx")
+    k_mx = _dev(k_mx, torch.uint8, "k_mx")
+    pool = _dev(pool, torch.int32, "pool")
+    B, H_I, rb = q_mx.shape
+    P = pool.shape[1]
+    if ws is None:
+        ws = make_workspace(B, 0, k, 0, P, q_mx.device)
+    if out is None:
+        out = torch.empty((B, k), dtype=torch.int32, device=q_mx.device)
+    _dev(out, torch.int32, "idx")
+    _check(lib.csa2_hier_pool_index_mxfp4(_ptr(q_mx), _ptr(k_mx), B, H_I, _mx_dim(rb), N,
+                                          kv_seq_stride, q_per_seq, _ptr(pool), P, k, _ptr(out),
+                                          _ptr(ws), ws.numel(), _stream()),
+           "csa2_hier_pool_index_mxfp4")
     return out
 
 
@@ -305,7 +376,8 @@ class LayerGroup:
                  q_pos: Optional[torch.Tensor], ratio: int, k: int, pool_size: int = 0,
                  softmax_scale: Optional[float] = None, want_lse: bool = True,
                  reuse_idx_copy: bool = True, pool_block: int = 0,
-                 swa_kv: Optional[Sequence[Optional[torch.Tensor]]] = None, n_win: int = 0):
+                 swa_kv: Optional[Sequence[Optional[torch.Tensor]]] = None, n_win: int = 0,
+                 indexer_fmt: int = INDEXER_E4M3):
         L = len(modes)
         self.modes = list(modes)
         self.q = [_bits16(q, f"q_bf16[{l}]") for l, q in enumerate(q_bf16)]
@@ -320,6 +392,8 @@ class LayerGroup:
         for qi in self.qi:
             if qi is not None:
                 _, H_I, D_I = qi.shape
+                if indexer_fmt == INDEXER_MXFP4:
+                    D_I = _mx_dim(D_I)
         if softmax_scale is None:
             softmax_scale = 1.0 / math.sqrt(D)
         self.B, self.H, self.D, self.k, self.N = B, H, D, k, N
@@ -343,7 +417,7 @@ class LayerGroup:
         self._args = Csa2GroupArgs(_ptr(self.kv), _ptr(self.ki), B, H, H_I, D, D_I, N,
                                    kv_seq_stride, q_per_seq, _ptr(self.q_pos), ratio, k,
                                    pool_size, _ptr(self.pool), softmax_scale, pool_block, ring,
-                                   n_win)
+                                   n_win, indexer_fmt)
 
     def __call__(self):
         _check(lib.csa2_layer_group(self._layers, len(self.modes), ctypes.byref(self._args),
@@ -359,8 +433,9 @@ def group_launches(group: LayerGroup) -> int:
 
 
 def layer_group(modes, q_bf16, qi_fp8, kv_fp4, ki_fp8, N, kv_seq_stride, q_per_seq, q_pos, ratio,
-                k, pool_size=0, softmax_scale=None, pool_block=0, swa_kv=None, n_win=0):
+                k, pool_size=0, softmax_scale=None, pool_block=0, swa_kv=None, n_win=0,
+                indexer_fmt=INDEXER_E4M3):
     """One-shot csa2_layer_group; returns (outs, lses, idxs, pool)."""
     return LayerGroup(modes, q_bf16, qi_fp8, kv_fp4, ki_fp8, N, kv_seq_stride, q_per_seq, q_pos,
                       ratio, k, pool_size, softmax_scale, pool_block=pool_block, swa_kv=swa_kv,
-                      n_win=n_win)()
+                      n_win=n_win, indexer_fmt=indexer_fmt)()

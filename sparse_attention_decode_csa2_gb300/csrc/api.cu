@@ -75,6 +75,26 @@ csa2_status check_indexer(const uint8_t* q, const uint8_t* k, int B, int H_I, in
   return CSA2_OK;
 }
 
+// MXFP4 indexer rows (68 bytes at D_I = 128): a sequence's rows must start
+// on a 16-byte boundary for the bulk copies of the full scan.
+csa2_status check_indexer_mx(const uint8_t* q, const uint8_t* k, int B, int H_I, int D_I,
+                             int ratio, int64_t kv_seq_stride, int q_per_seq) {
+  if (B > 0 && (!q || !k)) return CSA2_ERR_INVALID_ARG;
+  if (ratio < 1 || H_I < 1) return CSA2_ERR_INVALID_ARG;
+  if (D_I != 128 || H_I > 64) return CSA2_ERR_UNSUPPORTED;
+  if (!aligned16(k)) return CSA2_ERR_INVALID_ARG;
+  if (B > q_per_seq && kv_seq_stride % 4 != 0) return CSA2_ERR_UNSUPPORTED;
+  return CSA2_OK;
+}
+
+csa2_status check_indexer_fmt(int fmt, const uint8_t* q, const uint8_t* k, int B, int H_I,
+                              int D_I, int ratio, int64_t kv_seq_stride, int q_per_seq) {
+  if (fmt == CSA2_INDEXER_E4M3) return check_indexer(q, k, B, H_I, D_I, ratio);
+  if (fmt == CSA2_INDEXER_MXFP4)
+    return check_indexer_mx(q, k, B, H_I, D_I, ratio, kv_seq_stride, q_per_seq);
+  return CSA2_ERR_INVALID_ARG;
+}
+
 csa2_status check_attn(const uint16_t* q, const uint8_t* kv, int B, int H, int D, int k,
                        float scale, const float* out) {
   if (B > 0 && (!q || !kv || !out)) return CSA2_ERR_INVALID_ARG;
@@ -156,6 +176,27 @@ csa2_status csa2_index_scores(const uint8_t* q_fp8, const uint8_t* k_fp8, int B,
                                           q_pos, ratio, scores, nullptr, stream));
 }
 
+csa2_status csa2_quantize_mxfp4(const float* x, int64_t n_rows, int d, uint8_t* out,
+                               cudaStream_t stream) {
+  if (n_rows < 0 || d < 32 || d % 32 != 0 || d > 4096) return CSA2_ERR_INVALID_ARG;
+  if (n_rows > 0 && (!x || !out)) return CSA2_ERR_INVALID_ARG;
+  if (!aligned16(x)) return CSA2_ERR_INVALID_ARG;
+  return check_launch(launch_quantize_mxfp4(x, n_rows, d, out, stream));
+}
+
+csa2_status csa2_index_scores_mxfp4(const uint8_t* q_mx, const uint8_t* k_mx, int B, int H_I,
+                                    int D_I, int64_t N, int64_t kv_seq_stride, int q_per_seq,
+                                    const int32_t* q_pos, int ratio, float* scores,
+                                    cudaStream_t stream) {
+  csa2_status s = check_seq(B, N, kv_seq_stride, q_per_seq);
+  if (s != CSA2_OK) return s;
+  if ((s = check_indexer_mx(q_mx, k_mx, B, H_I, D_I, ratio, kv_seq_stride, q_per_seq)) != CSA2_OK)
+    return s;
+  if (B > 0 && N > 0 && !scores) return CSA2_ERR_INVALID_ARG;
+  return check_launch(launch_index_scores_mxfp4(q_mx, k_mx, B, H_I, N, kv_seq_stride, q_per_seq,
+                                                q_pos, ratio, scores, nullptr, stream));
+}
+
 csa2_status csa2_topk(const float* scores, int B, int64_t N, int k, const int32_t* q_pos,
                       int ratio, int32_t* idx, void* ws, size_t ws_bytes, cudaStream_t stream) {
   if (B < 0 || N < 0 || N > INT32_MAX - 1 || k < 1 || ratio < 1) return CSA2_ERR_INVALID_ARG;
@@ -203,6 +244,27 @@ csa2_status csa2_hier_pool_index(const uint8_t* q_fp8, const uint8_t* k_fp8, int
   cudaError_t e = launch_pool_scores(q_fp8, k_fp8, B, H_I, D_I, N, kv_seq_stride, q_per_seq, pool,
                                      P, pscores, nullptr, status_ptr(ws), stream);
   if (e != cudaSuccess) return CSA2_ERR_CUDA;
+  return check_launch(
+      launch_topk(pscores, B, P, k, nullptr, 1, nullptr, pool, idx, stream, /*pdl=*/true));
+}
+
+csa2_status csa2_hier_pool_index_mxfp4(const uint8_t* q_mx, const uint8_t* k_mx, int B, int H_I,
+                                       int D_I, int64_t N, int64_t kv_seq_stride, int q_per_seq,
+                                       const int32_t* pool, int P, int k, int32_t* idx, void* ws,
+                                       size_t ws_bytes, cudaStream_t stream) {
+  csa2_status s = check_seq(B, N, kv_seq_stride, q_per_seq);
+  if (s != CSA2_OK) return s;
+  if ((s = check_indexer_mx(q_mx, k_mx, B, H_I, D_I, 1, kv_seq_stride, q_per_seq)) != CSA2_OK)
+    return s;
+  if (P < 1 || k < 1) return CSA2_ERR_INVALID_ARG;
+  if (B > 0 && (!pool || !idx)) return CSA2_ERR_INVALID_ARG;
+  WsLayout w = layout(B, 0, 0, 0, P);
+  if (!ws || ws_bytes < w.total) return CSA2_ERR_WORKSPACE;
+  uint8_t* wsb = reinterpret_cast<uint8_t*>(ws);
+  float* pscores = reinterpret_cast<float*>(wsb + w.pool_scores);
+  cudaError_t e = launch_pool_scores_mxfp4(q_mx, k_mx, B, H_I, N, kv_seq_stride, q_per_seq, pool,
+                                           P, pscores, status_ptr(ws), stream);
+  if (e != cudaSuccess) return check_launch(e);
   return check_launch(
       launch_topk(pscores, B, P, k, nullptr, 1, nullptr, pool, idx, stream, /*pdl=*/true));
 }
@@ -286,7 +348,8 @@ csa2_status csa2_layer_group(const csa2_layer* layers, int n_layers, const csa2_
     if (L.mode == CSA2_REUSE) {
       if (L.qi_fp8) return CSA2_ERR_INVALID_ARG;
     } else {
-      if ((s = check_indexer(L.qi_fp8, g->ki_fp8, g->B, g->H_I, g->D_I, g->ratio)) != CSA2_OK)
+      if ((s = check_indexer_fmt(g->indexer_fmt, L.qi_fp8, g->ki_fp8, g->B, g->H_I, g->D_I,
+                                 g->ratio, g->kv_seq_stride, g->q_per_seq)) != CSA2_OK)
         return s;
       if (g->B > 0 && !L.idx_out) return CSA2_ERR_INVALID_ARG;
     }
@@ -299,13 +362,18 @@ csa2_status csa2_layer_group(const csa2_layer* layers, int n_layers, const csa2_
   float* scores = reinterpret_cast<float*>(wsb + w.scores);
   float* pscores = reinterpret_cast<float*>(wsb + w.pool_scores);
   const int32_t* latest = nullptr;
+  const bool mx = g->indexer_fmt == CSA2_INDEXER_MXFP4;
   cudaError_t e = cudaSuccess;
   for (int l = 0; l < n_layers && e == cudaSuccess; ++l) {
     const csa2_layer& L = layers[l];
     const int32_t* use = nullptr;
     if (L.mode == CSA2_FULL || (L.mode == CSA2_REINDEX && g->pool_size == 0)) {
-      e = launch_index_scores(L.qi_fp8, g->ki_fp8, g->B, g->H_I, g->D_I, g->N, g->kv_seq_stride,
-                              g->q_per_seq, g->q_pos, g->ratio, scores, status, stream);
+      e = mx ? launch_index_scores_mxfp4(L.qi_fp8, g->ki_fp8, g->B, g->H_I, g->N,
+                                         g->kv_seq_stride, g->q_per_seq, g->q_pos, g->ratio,
+                                         scores, status, stream)
+             : launch_index_scores(L.qi_fp8, g->ki_fp8, g->B, g->H_I, g->D_I, g->N,
+                                   g->kv_seq_stride, g->q_per_seq, g->q_pos, g->ratio, scores,
+                                   status, stream);
       if (e == cudaSuccess && L.mode == CSA2_FULL && g->pool_size > 0) {
         if (g->pool_block > 1)  // blockwise pool (a one-entry block pool is the flat one)
           e = launch_block_pool(scores, g->B, g->N, g->q_pos, g->ratio, g->pool_block,
@@ -320,9 +388,12 @@ csa2_status csa2_layer_group(const csa2_layer* layers, int n_layers, const csa2_
                         stream, /*pdl=*/true, wsb + w.topk, w.topk_bytes);
       use = L.idx_out;
     } else if (L.mode == CSA2_REINDEX) {
-      e = launch_pool_scores(L.qi_fp8, g->ki_fp8, g->B, g->H_I, g->D_I, g->N, g->kv_seq_stride,
-                             g->q_per_seq, g->pool_out, g->pool_size, pscores, nullptr, status,
-                             stream);
+      e = mx ? launch_pool_scores_mxfp4(L.qi_fp8, g->ki_fp8, g->B, g->H_I, g->N,
+                                        g->kv_seq_stride, g->q_per_seq, g->pool_out,
+                                        g->pool_size, pscores, status, stream)
+             : launch_pool_scores(L.qi_fp8, g->ki_fp8, g->B, g->H_I, g->D_I, g->N,
+                                  g->kv_seq_stride, g->q_per_seq, g->pool_out, g->pool_size,
+                                  pscores, nullptr, status, stream);
       if (e == cudaSuccess)
         e = launch_topk(pscores, g->B, g->pool_size, g->k, nullptr, 1, nullptr, g->pool_out,
                         L.idx_out, stream, /*pdl=*/true);

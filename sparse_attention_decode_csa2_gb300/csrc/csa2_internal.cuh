@@ -132,6 +132,18 @@ cudaError_t launch_pool_scores(const uint8_t* q_fp8, const uint8_t* k_fp8, int B
                                const int32_t* pool, int P, float* pool_scores, int32_t* n_valid,
                                int32_t* status, cudaStream_t stream);
 
+// MXFP4 indexer (rows of D_I = 128: 64 code bytes + 4 E8M0 scale bytes).
+cudaError_t launch_quantize_mxfp4(const float* x, int64_t n_rows, int d, uint8_t* out,
+                                  cudaStream_t stream);
+cudaError_t launch_index_scores_mxfp4(const uint8_t* q_mx, const uint8_t* k_mx, int B, int H_I,
+                                      int64_t N, int64_t kv_seq_stride, int q_per_seq,
+                                      const int32_t* q_pos, int ratio, float* scores,
+                                      int32_t* status, cudaStream_t stream);
+cudaError_t launch_pool_scores_mxfp4(const uint8_t* q_mx, const uint8_t* k_mx, int B, int H_I,
+                                     int64_t N, int64_t kv_seq_stride, int q_per_seq,
+                                     const int32_t* pool, int P, float* pool_scores,
+                                     int32_t* status, cudaStream_t stream);
+
 // Top-k over rows of `scores` [B][N].  The number of candidates of row b is
 // n_visible(q_pos, b, ratio, N) when n_valid is null, else n_valid[b].  When
 // `map` is non-null the selected position p is written as map[b*N + p].
