@@ -170,12 +170,12 @@ def algorithmic_bytes(w):
         b = B * k * w.row_bytes + B * w.H * w.D * 2 + B * w.H * w.D * 4
         if m == FULL or (m == REINDEX and not w.pool):
             n_scored = sum(min(N, (int(p) + 1) // w.ratio) for p in w.q_pos())
-            b += n_scored * w.D_I + B * w.H_I * w.D_I
+            b += n_scored * w.idx_row_bytes + B * w.H_I * w.idx_row_bytes
             if w.q_per_seq > 1:   # one shared context: its K is read once
-                b -= n_scored * w.D_I
-                b += w.n_seq * N * w.D_I
+                b -= n_scored * w.idx_row_bytes
+                b += w.n_seq * N * w.idx_row_bytes
         elif m == REINDEX:
-            b += B * w.pool * (w.D_I + 4) + B * w.H_I * w.D_I
+            b += B * w.pool * (w.idx_row_bytes + 4) + B * w.H_I * w.idx_row_bytes
         if w.n_win:   # each query's SWA window (E4M3 rows of D bytes)
             b += sum(min(w.n_win, int(p) + 1) for p in w.q_pos() if p >= 0) * w.D
         per_layer.append(b)
@@ -189,7 +189,7 @@ def kernel_bytes(w):
     n_scored = sum(min(N, (int(p) + 1) // w.ratio) for p in w.q_pos())
     n_win = sum(min(w.n_win, int(p) + 1) for p in w.q_pos() if p >= 0) if w.n_win else 0
     return {
-        "index_scores": n_scored * w.D_I + B * w.H_I * w.D_I + B * N * 4,
+        "index_scores": n_scored * w.idx_row_bytes + B * w.H_I * w.idx_row_bytes + B * N * 4,
         "topk": n_scored * 4 + B * k * 4,
         "sparse_attn_fp4": B * k * (w.row_bytes + 4) + n_win * w.D + B * w.H * w.D * (2 + 4) +
                            B * w.H * 4,
@@ -268,8 +268,11 @@ def run_gpu(args, rank, world, local):
     lse = torch.empty((w.B, w.H), dtype=torch.float32, device=dev)
     ws = csa2.make_workspace(w.B, w.N, w.k, w.H, w.pool, dev)
     ops = {
-        "index_scores": lambda: csa2.index_scores(inp.qi[0], inp.ki_fp8, w.N, w.kv_seq_stride,
-                                                  w.q_per_seq, inp.q_pos, w.ratio, out=scores),
+        "index_scores": (lambda: csa2.index_scores_mxfp4(
+            inp.qi[0], inp.ki_fp8, w.N, w.kv_seq_stride, w.q_per_seq, inp.q_pos, w.ratio,
+            out=scores)) if w.indexer_fmt else
+        (lambda: csa2.index_scores(inp.qi[0], inp.ki_fp8, w.N, w.kv_seq_stride, w.q_per_seq,
+                                   inp.q_pos, w.ratio, out=scores)),
         "topk": lambda: csa2.topk(scores, w.k, inp.q_pos, w.ratio, ws, out=idx),
         "sparse_attn_fp4": (lambda: csa2.sparse_attn_fp4_swa(
             inp.q[0], inp.kv_fp4, w.N, w.kv_seq_stride, w.q_per_seq, idx, inp.swa[0], w.n_win,
@@ -417,12 +420,12 @@ class OracleSample:
         for q in queries:
             s = q // w.q_per_seq
             if s not in cache:
-                cache[s] = (oracle.quantize_kv_fp4(w.kv_latent(s)), w.ki_fp8(s))
+                cache[s] = (oracle.quantize_kv_fp4(w.kv_latent(s)), w.ki_rows(s))
             kv, ki = cache[s]
             L = len(w.modes)
             self.items.append(dict(q=q, kv=kv, ki=ki, qpos=w.q_pos()[q:q + 1],
                                    qb=[w.q_bf16(l, [q]) for l in range(L)],
-                                   qi=[w.qi_fp8(l, [q]) if w.modes[l] != 2 else None
+                                   qi=[w.qi_rows(l, [q]) if w.modes[l] != 2 else None
                                        for l in range(L)],
                                    swa=[w.swa_kv(l, s)[None] for l in range(L)]
                                    if w.n_win else None))
@@ -432,7 +435,7 @@ class OracleSample:
         o.layer_group(w.modes, item["qb"], item["qi"], item["kv"], item["ki"], w.N, 0, 1,
                       item["qpos"], w.ratio, w.k, w.pool, 1.0 / math.sqrt(w.D),
                       pool_block=w.pool_block, swa_kv=item["swa"], swa_ring=w.swa_ring,
-                      n_win=w.n_win)
+                      n_win=w.n_win, indexer_fmt=w.indexer_fmt, D_I=w.D_I)
 
 
 def cpu_baseline(w, budget_s=12.0):

@@ -9,18 +9,19 @@
 // Scoring.  The score is a sum over indexer heads of q_h . K_j, so the head
 // sum is formed first (qsum = sum_h q_h, compensated fp32 summation of exact
 // decoded values) and each entry costs one 128-long dot product: 68 bytes of
-// HBM for 128 multiply-adds.  That is a matrix-vector product bounded by HBM
-// bandwidth, so it runs on the CUDA cores, not the tensor cores:
+// HBM for 128 multiply-adds, a matrix-vector product bounded by HBM bandwidth.
+// What limits it on the SM is decoding: one E2M1 pair -> f16x2 conversion
+// per code byte is the only per-element instruction left; the multiply-adds
+// run as warp-level m16n8k16 MMAs (f16 operands, fp32 accumulation) that
+// take the decoded registers directly, 16 entries per MMA group, with the
+// head sum in B split into two f16 parts (22 significant bits).
 //  * full scan: a persistent grid (a multiple of the SM count) walks
 //    contiguous runs of 128-entry tiles (8704 bytes); one producer warp
 //    streams the tiles into a 4-stage shared-memory ring with 1D bulk
 //    copies (cp.async.bulk, mbarrier completion), four consumer warps score
-//    them.  Four lanes share an entry, one 32-element block each, and add
-//    their partial dot products with two shuffles.
-//  * pool scan (Reindex layers): the same per-entry arithmetic on gathered
-//    rows, one entry per four lanes.
-// Products are fp32 FMAs of exact decoded values; the per-block partial is
-// scaled by the entry's E8M0 scale.
+//    them, 32 entries each.
+//  * pool scan (Reindex layers): the same per-group arithmetic on gathered
+//    rows loaded straight from global memory.
 #include "csa2_internal.cuh"
 #include "tc_common.cuh"
 
@@ -92,46 +93,70 @@ quantize_mxfp4_kernel(const float* __restrict__ x, int64_t n_rows, int d,
   }
 }
 
-// fp32 pair FMA (Blackwell packed FP32 pipe): acc += a * b, element-wise.
-__device__ __forceinline__ void ffma2(float2& acc, float2 a, float2 b) {
-  uint64_t d;
-  asm("{\n\t.reg .b64 ra, rb, rc;\n\t"
-      "mov.b64 ra, {%1, %2};\n\tmov.b64 rb, {%3, %4};\n\tmov.b64 rc, {%5, %6};\n\t"
-      "fma.rn.f32x2 %0, ra, rb, rc;\n\t}"
-      : "=l"(d)
-      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(acc.x), "f"(acc.y));
-  acc.x = __uint_as_float((uint32_t)d);
-  acc.y = __uint_as_float((uint32_t)(d >> 32));
+// ---------------------------------------------------------------------------
+// Dot products of 16 entries with one query on the warp's tensor cores.
+//
+// mma.sync m16n8k16 (f16 in, fp32 accumulate) with A = 16 entries x 16
+// elements and B = 16 elements x 8 columns.  Lane (g, t) (g = lane / 4,
+// t = lane % 4) supplies entries g and g + 8 of the group; of each entry it
+// decodes code word 4b + t of every 32-element block b: 8 elements, i.e. the
+// four A registers of two k16 steps.  The k order inside a step is therefore
+// a permutation of the elements, and B follows the same permutation: in step
+// (b, cc), k = 2t + {0,1} is element 32b + 8t + 4cc + {0,1} and k = 2t + 8 +
+// {0,1} is element 32b + 8t + 4cc + 2 + {0,1}.
+// Column n = 2b + p of B holds part p (p = 0: f16 rounding, p = 1: f16
+// rounding of the remainder) of the query's head sum, scaled by 2^-e_b, on
+// the rows of block b and zero elsewhere.  After the 8 steps lane (g, t)
+// holds the block-t partials of entries g and g + 8 in accumulator columns
+// 2t (part 0) and 2t + 1 (part 1); it scales them by the entry's E8M0 scale
+// and 2^e_t and four lanes add them.  Products of two f16 values are exact in
+// fp32.
+// ---------------------------------------------------------------------------
+
+// code word (8 E2M1 elements) -> 4 f16x2 registers (byte j -> register j,
+// low nibble in the low half).  The byte unpack costs no instruction.
+__device__ __forceinline__ void e2m1_word_to_f16x2(uint32_t w, uint32_t h[4]) {
+  asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\tmov.b32 {b0, b1, b2, b3}, %4;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %0, b0;\n\tcvt.rn.f16x2.e2m1x2 %1, b1;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %2, b2;\n\tcvt.rn.f16x2.e2m1x2 %3, b3;\n\t}"
+      : "=r"(h[0]), "=r"(h[1]), "=r"(h[2]), "=r"(h[3])
+      : "r"(w));
 }
 
-// Dot product of one 32-element block (16 code bytes in w[0..3]) with the
-// matching 32 qsum values (in registers), unscaled.
-__device__ __forceinline__ float block_dot(const uint32_t w[4], const float* qs) {
-  float2 acc0 = make_float2(0.f, 0.f), acc1 = make_float2(0.f, 0.f);
+__device__ __forceinline__ void mma_16816(float c[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                          uint32_t a3, uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+      "{%8,%9}, {%0,%1,%2,%3};"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// wA[b], wB[b]: code word 4b + t of entries g and g + 8; bq[b]: the lane's B
+// registers of steps (b, 0) and (b, 1).
+__device__ __forceinline__ void mx16_dot(const uint32_t wA[4], const uint32_t wB[4],
+                                         const uint4 bq[4], float c[4]) {
+  c[0] = c[1] = c[2] = c[3] = 0.0f;
 #pragma unroll
-  for (int c = 0; c < 4; ++c) {
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const float2 f = half2_bits_to_float2(e2m1x2_to_f16x2((w[c] >> (8 * j)) & 0xFFu));
-      const float2 q = make_float2(qs[8 * c + 2 * j], qs[8 * c + 2 * j + 1]);
-      if (j & 1) ffma2(acc1, f, q);
-      else ffma2(acc0, f, q);
-    }
+  for (int b = 0; b < 4; ++b) {
+    uint32_t hA[4], hB[4];
+    e2m1_word_to_f16x2(wA[b], hA);
+    e2m1_word_to_f16x2(wB[b], hB);
+    mma_16816(c, hA[0], hB[0], hA[1], hB[1], bq[b].x, bq[b].y);
+    mma_16816(c, hA[2], hB[2], hA[3], hB[3], bq[b].z, bq[b].w);
   }
-  return (acc0.x + acc0.y) + (acc1.x + acc1.y);
 }
 
 // qsum[d] = sum_h value(q[h][d]) for one query (MXFP4 rows of kMxDI), by
-// compensated (Neumaier) fp32 summation of the exact decoded values; thread t
-// of `nthreads` computes dims t, t + nthreads, ...
+// compensated (Neumaier) fp32 summation of the exact decoded values.
 __device__ __forceinline__ float mx_qsum_dim(const uint8_t* __restrict__ q, int H_I, int d) {
   float s = 0.0f, comp = 0.0f;
   for (int h = 0; h < H_I; ++h) {
     const uint8_t* row = q + (int64_t)h * kMxRow;
     const uint32_t byte = __ldg(row + d / 2);
     const uint32_t code = (d & 1) ? (byte >> 4) : (byte & 15u);
-    const float v =
-        half2_bits_to_float2(e2m1x2_to_f16x2(code)).x * e8m0_to_float(__ldg(row + kMxCodes + d / 32));
+    const float v = half2_bits_to_float2(e2m1x2_to_f16x2(code)).x *
+                    e8m0_to_float(__ldg(row + kMxCodes + d / 32));
     const float t = s + v;
     comp += (fabsf(s) >= fabsf(v)) ? ((s - t) + v) : ((v - t) + s);
     s = t;
@@ -139,9 +164,64 @@ __device__ __forceinline__ float mx_qsum_dim(const uint8_t* __restrict__ q, int 
   return s + comp;
 }
 
+// The B registers of up to kQChunk queries, built by `nthreads` threads
+// (>= 128, a multiple of 32): qsum of each dim, a power-of-two scale 2^e_b per
+// 32-dim block putting the block's largest |qsum| in [2^14, 2^15), then the
+// f16 parts.  qfrag[ql][b][lane] holds lane's registers of steps (b, 0),
+// (b, 1); qscale[ql][b] = 2^e_b.  Ends with a barrier of the `bar` group.
+struct QFrag {
+  float qs[kQChunk][kMxDI];
+  uint4 frag[kQChunk][4][32];
+  float qscale[kQChunk][4];
+};
+
+__device__ __forceinline__ uint32_t f16_part_pair(float x0, float x1, int p) {
+  __half h0 = __float2half_rn(x0), h1 = __float2half_rn(x1);
+  if (p) {
+    h0 = __float2half_rn(x0 - __half2float(h0));
+    h1 = __float2half_rn(x1 - __half2float(h1));
+  }
+  return (uint32_t)__half_as_ushort(h0) | ((uint32_t)__half_as_ushort(h1) << 16);
+}
+
+template <int kThreads, int kBarId>
+__device__ __forceinline__ void build_qfrag(QFrag& f, const uint8_t* __restrict__ q_mx, int H_I,
+                                            int q0, int nq) {
+  const int tid = threadIdx.x;
+  const int lane = tid & 31;
+  for (int i = tid; i < nq * kMxDI; i += kThreads) {  // thread i % 128 always takes dim i % 128
+    const int ql = i / kMxDI, d = i % kMxDI;
+    const float v = mx_qsum_dim(q_mx + (int64_t)(q0 + ql) * H_I * kMxRow, H_I, d);
+    float a = fabsf(v);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, o));
+    int e = 0;
+    if (a > 0.0f) {
+      int ex;
+      frexpf(a, &ex);  // a = m 2^ex, m in [0.5, 1): floor(log2 a) = ex - 1
+      e = ex - 1 - 14;
+    }
+    f.qs[ql][d] = ldexpf(v, -e);
+    if (lane == 0) f.qscale[ql][d / 32] = ldexpf(1.0f, e);
+  }
+  asm volatile("bar.sync %0, %1;" ::"n"(kBarId), "n"(kThreads) : "memory");
+  uint32_t* words = reinterpret_cast<uint32_t*>(&f.frag[0][0][0]);
+  for (int i = tid; i < nq * 4 * 32 * 4; i += kThreads) {
+    const int ql = i / 512, b = (i / 128) % 4, ln = (i / 4) % 32, w = i % 4;
+    const int g = ln >> 2, t = ln & 3, cc = w >> 1, h = w & 1;
+    uint32_t val = 0;
+    if ((g >> 1) == b) {
+      const int e = 32 * b + 8 * t + 4 * cc + 2 * h;
+      val = f16_part_pair(f.qs[ql][e], f.qs[ql][e + 1], g & 1);
+    }
+    words[i] = val;
+  }
+  asm volatile("bar.sync %0, %1;" ::"n"(kBarId), "n"(kThreads) : "memory");
+}
+
 struct ScanSmem {
   uint8_t tiles[kStages][kTileBytes];
-  float qsum[kQChunk][kMxDI];
+  QFrag qf;
   uint64_t full[kStages];
   uint64_t empty[kStages];
 };
@@ -175,7 +255,7 @@ __device__ __forceinline__ void bulk_copy(uint32_t dst, const void* src, uint32_
 
 // Full scan.  Tiles are numbered (sequence, tile) row-major, T tiles of 128
 // entries per sequence; CTA c takes the contiguous run [c*total/C, (c+1)*total/C),
-// so it meets few sequence changes (each recomputes the staged qsum).
+// so it meets few sequence changes (each rebuilds the staged query registers).
 __global__ void __launch_bounds__(kScanThreads, 3)
 mx_scores_kernel(const uint8_t* __restrict__ q_mx, const uint8_t* __restrict__ k_mx, int B,
                  int H_I, int64_t N, int64_t kv_seq_stride, int q_per_seq,
@@ -237,10 +317,9 @@ mx_scores_kernel(const uint8_t* __restrict__ q_mx, const uint8_t* __restrict__ k
     return;
   }
 
-  // ---------------- consumers ----------------
-  const int blk = lane & 3;                 // 32-element block of this lane
-  const int rsub = tid >> 2;                // 0..31: rows rsub + 32 i
-  int64_t n = 0;                            // loads consumed
+  // ---------------- consumers: warp w scores entries 32w .. 32w + 31 of a tile ----------------
+  const int g = lane >> 2, t = lane & 3;
+  int64_t n = 0;  // loads consumed
   int cur_s = -1, cur_chunk = -1;
   int64_t vis = 0;
   for (int64_t tile = t_begin; tile < t_end; ++tile) {
@@ -258,46 +337,48 @@ mx_scores_kernel(const uint8_t* __restrict__ q_mx, const uint8_t* __restrict__ k
         !tc::mbar_wait(tc::su32(&sm.full[st]), (uint32_t)((n / kStages) & 1), status))
       return;
     const uint8_t* tileb = sm.tiles[st];
+    const uint32_t* tw = reinterpret_cast<const uint32_t*>(tileb);
     const int q_first = s * q_per_seq;
     const int q_last = min(B, q_first + q_per_seq);
     for (int qc = q_first; qc < q_last; qc += kQChunk) {
       const int nq = min(kQChunk, q_last - qc);
       if (qc != cur_chunk) {
         asm volatile("bar.sync 1, %0;" ::"n"(kConsumers) : "memory");
-        for (int i = tid; i < nq * kMxDI; i += kConsumers)
-          sm.qsum[i / kMxDI][i % kMxDI] =
-              mx_qsum_dim(q_mx + (int64_t)(qc + i / kMxDI) * H_I * kMxRow, H_I, i % kMxDI);
-        asm volatile("bar.sync 1, %0;" ::"n"(kConsumers) : "memory");
+        build_qfrag<kConsumers, 1>(sm.qf, q_mx, H_I, qc, nq);
         cur_chunk = qc;
       }
       for (int ql = 0; ql < nq; ++ql) {
         const int q = qc + ql;
         const int64_t nv = n_visible(q_pos, q, ratio, N);
-        float qs[32];
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          const float4 v4 = *reinterpret_cast<const float4*>(&sm.qsum[ql][32 * blk + 4 * i]);
-          qs[4 * i] = v4.x;
-          qs[4 * i + 1] = v4.y;
-          qs[4 * i + 2] = v4.z;
-          qs[4 * i + 3] = v4.w;
-        }
         float* srow = scores + (int64_t)q * N + row0;
+        uint4 bq[4];
 #pragma unroll
-        for (int i = 0; i < kTileRows / 32; ++i) {
-          const int r = rsub + 32 * i;
-          float part = 0.0f;
-          if (r < rows) {
-            const uint32_t* rw = reinterpret_cast<const uint32_t*>(tileb + r * kMxRow);
-            uint32_t w[4];
+        for (int b = 0; b < 4; ++b) bq[b] = sm.qf.frag[ql][b][lane];
+        const float qs_t = sm.qf.qscale[ql][t];
 #pragma unroll
-            for (int c = 0; c < 4; ++c) w[c] = rw[4 * blk + c];
-            const uint32_t sb = (rw[kMxCodes / 4] >> (8 * blk)) & 0xFFu;
-            part = block_dot(w, qs) * e8m0_to_float(sb);
+        for (int grp = 0; grp < 2; ++grp) {
+          const int rA = warp * 32 + grp * 16 + g, rB = rA + 8;
+          float pA = 0.0f, pB = 0.0f;
+          if (rows > 0) {  // tile-uniform
+            uint32_t wA[4], wB[4];
+#pragma unroll
+            for (int b = 0; b < 4; ++b) {
+              wA[b] = rA < rows ? tw[rA * (kMxRow / 4) + 4 * b + t] : 0u;
+              wB[b] = rB < rows ? tw[rB * (kMxRow / 4) + 4 * b + t] : 0u;
+            }
+            float c[4];
+            mx16_dot(wA, wB, bq, c);
+            const float ksA = rA < rows ? e8m0_to_float(tileb[rA * kMxRow + kMxCodes + t]) : 0.0f;
+            const float ksB = rB < rows ? e8m0_to_float(tileb[rB * kMxRow + kMxCodes + t]) : 0.0f;
+            pA = (c[0] + c[1]) * (ksA * qs_t);
+            pB = (c[2] + c[3]) * (ksB * qs_t);
+            pA += __shfl_xor_sync(0xffffffffu, pA, 1);
+            pB += __shfl_xor_sync(0xffffffffu, pB, 1);
+            pA += __shfl_xor_sync(0xffffffffu, pA, 2);
+            pB += __shfl_xor_sync(0xffffffffu, pB, 2);
           }
-          part += __shfl_xor_sync(0xffffffffu, part, 1);
-          part += __shfl_xor_sync(0xffffffffu, part, 2);
-          if (blk == 0 && r < rows_in_tile) srow[r] = (row0 + r < nv) ? part : -INFINITY;
+          if (t == 0 && rA < rows_in_tile) srow[rA] = (row0 + rA < nv) ? pA : -INFINITY;
+          if (t == 1 && rB < rows_in_tile) srow[rB] = (row0 + rB < nv) ? pB : -INFINITY;
         }
       }
     }
@@ -309,56 +390,75 @@ mx_scores_kernel(const uint8_t* __restrict__ q_mx, const uint8_t* __restrict__ k
   }
 }
 
-// Pool scan: CTA (x, q) scores pool slots [1024 x, 1024 x + 1024) of query q.
+// Pool scan: CTA (x, q) scores pool slots [1024 x, 1024 x + 1024) of query q,
+// each warp 16 gathered entries at a time.
 constexpr int kPoolThreads = 256;
 constexpr int kPoolSlots = 1024;
+
+struct PoolSmem {
+  QFrag qf;
+};
 
 __global__ void __launch_bounds__(kPoolThreads)
 mx_pool_scores_kernel(const uint8_t* __restrict__ q_mx, const uint8_t* __restrict__ k_mx, int H_I,
                       int64_t N, int64_t kv_seq_stride, int q_per_seq,
                       const int32_t* __restrict__ pool, int P, float* __restrict__ pool_scores,
                       int32_t* status) {
-  __shared__ __align__(16) float qsum[kMxDI];
+  extern __shared__ __align__(128) uint8_t smem_raw[];
+  PoolSmem& sm = *reinterpret_cast<PoolSmem*>(smem_raw);
   pdl_trigger();
   pdl_wait();
   const int q = blockIdx.y;
-  for (int d = threadIdx.x; d < kMxDI; d += kPoolThreads)
-    qsum[d] = mx_qsum_dim(q_mx + (int64_t)q * H_I * kMxRow, H_I, d);
-  __syncthreads();
-  const int blk = threadIdx.x & 3;
-  float qs[32];
+  build_qfrag<kPoolThreads, 1>(sm.qf, q_mx, H_I, q, 1);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int g = lane >> 2, t = lane & 3;
+  uint4 bq[4];
 #pragma unroll
-  for (int i = 0; i < 32; ++i) qs[i] = qsum[32 * blk + i];
+  for (int b = 0; b < 4; ++b) bq[b] = sm.qf.frag[0][b][lane];
+  const float qs_t = sm.qf.qscale[0][t];
   const uint8_t* kseq = k_mx + (int64_t)(q / q_per_seq) * kv_seq_stride * kMxRow;
   const int32_t* prow = pool + (int64_t)q * P;
-  for (int it = 0; it < kPoolSlots / (kPoolThreads / 4); ++it) {
-    const int p = blockIdx.x * kPoolSlots + it * (kPoolThreads / 4) + (threadIdx.x >> 2);
-    int32_t j = -1;
-    bool ok = false;
-    if (p < P) {
-      j = prow[p];
-      ok = (j >= 0 && j < N);
-      if (blk == 0) {
+  constexpr int kGroups = kPoolSlots / 16 / (kPoolThreads / 32);  // per warp
+  for (int it = 0; it < kGroups; ++it) {
+    const int p0 = blockIdx.x * kPoolSlots + (it * (kPoolThreads / 32) + warp) * 16;
+    const int pA = p0 + g, pB = pA + 8;
+    int32_t jA = -1, jB = -1;
+    if (pA < P) jA = __ldg(prow + pA);
+    if (pB < P) jB = __ldg(prow + pB);
+    // lanes t = 0 / 1 check slots g / g + 8: in range, ascending, -1 only at the tail
+    if (t < 2) {
+      const int p = t == 0 ? pA : pB;
+      const int32_t j = t == 0 ? jA : jB;
+      if (p < P) {
         bool bad = (j >= N) || (j < -1);
         if (p > 0) {
-          const int32_t prev = prow[p - 1];
-          if (j >= 0 && (prev < 0 || prev >= j)) bad = true;  // not ascending / -1 not at tail
+          const int32_t prev = __ldg(prow + p - 1);
+          if (j >= 0 && (prev < 0 || prev >= j)) bad = true;
         }
         if (bad) set_status(status, kStatusBadIndex);
       }
     }
-    float part = 0.0f;
-    if (ok) {
-      const uint32_t* rw = reinterpret_cast<const uint32_t*>(kseq + (int64_t)j * kMxRow);
-      uint32_t w[4];
+    const bool okA = jA >= 0 && jA < N, okB = jB >= 0 && jB < N;
+    const uint32_t* rwA = reinterpret_cast<const uint32_t*>(kseq + (int64_t)(okA ? jA : 0) * kMxRow);
+    const uint32_t* rwB = reinterpret_cast<const uint32_t*>(kseq + (int64_t)(okB ? jB : 0) * kMxRow);
+    uint32_t wA[4], wB[4];
 #pragma unroll
-      for (int c = 0; c < 4; ++c) w[c] = __ldg(rw + 4 * blk + c);
-      const uint32_t sb = (__ldg(rw + kMxCodes / 4) >> (8 * blk)) & 0xFFu;
-      part = block_dot(w, qs) * e8m0_to_float(sb);
+    for (int b = 0; b < 4; ++b) {
+      wA[b] = okA ? __ldg(rwA + 4 * b + t) : 0u;
+      wB[b] = okB ? __ldg(rwB + 4 * b + t) : 0u;
     }
-    part += __shfl_xor_sync(0xffffffffu, part, 1);
-    part += __shfl_xor_sync(0xffffffffu, part, 2);
-    if (blk == 0 && p < P) pool_scores[(int64_t)q * P + p] = ok ? part : -INFINITY;
+    const uint32_t sA = okA ? __ldg(reinterpret_cast<const uint8_t*>(rwA) + kMxCodes + t) : 0u;
+    const uint32_t sB = okB ? __ldg(reinterpret_cast<const uint8_t*>(rwB) + kMxCodes + t) : 0u;
+    float c[4];
+    mx16_dot(wA, wB, bq, c);
+    float vA = (c[0] + c[1]) * (e8m0_to_float(sA) * qs_t);
+    float vB = (c[2] + c[3]) * (e8m0_to_float(sB) * qs_t);
+    vA += __shfl_xor_sync(0xffffffffu, vA, 1);
+    vB += __shfl_xor_sync(0xffffffffu, vB, 1);
+    vA += __shfl_xor_sync(0xffffffffu, vA, 2);
+    vB += __shfl_xor_sync(0xffffffffu, vB, 2);
+    if (t == 0 && pA < P) pool_scores[(int64_t)q * P + pA] = okA ? vA : -INFINITY;
+    if (t == 1 && pB < P) pool_scores[(int64_t)q * P + pB] = okB ? vB : -INFINITY;
   }
 }
 
@@ -394,7 +494,7 @@ cudaError_t launch_index_scores_mxfp4(const uint8_t* q_mx, const uint8_t* k_mx, 
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&smem_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev);
   int per_sm = smem_sm > 0 ? smem_sm / (int)(smem + 1024) : 1;
-  per_sm = per_sm < 1 ? 1 : (per_sm > 3 ? 3 : per_sm);
+  per_sm = per_sm < 1 ? 1 : (per_sm > 4 ? 4 : per_sm);
   int64_t grid = (int64_t)per_sm * device_sm_count();
   if (grid > total) grid = total;
   return launch_kernel(mx_scores_kernel, dim3((unsigned)grid), dim3(kScanThreads), smem, stream,
@@ -407,8 +507,16 @@ cudaError_t launch_pool_scores_mxfp4(const uint8_t* q_mx, const uint8_t* k_mx, i
                                      const int32_t* pool, int P, float* pool_scores,
                                      int32_t* status, cudaStream_t stream) {
   if (B == 0 || P == 0) return cudaSuccess;
+  const size_t smem = sizeof(PoolSmem);
+  static bool attr_set = false;  // per process; the attribute is per kernel
+  if (!attr_set) {
+    cudaError_t e = cudaFuncSetAttribute(mx_pool_scores_kernel,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
   dim3 grid((unsigned)((P + kPoolSlots - 1) / kPoolSlots), (unsigned)B);
-  return launch_kernel(mx_pool_scores_kernel, grid, dim3(kPoolThreads), 0, stream, false, q_mx,
+  return launch_kernel(mx_pool_scores_kernel, grid, dim3(kPoolThreads), smem, stream, false, q_mx,
                        k_mx, H_I, N, kv_seq_stride, q_per_seq, pool, P, pool_scores, status);
 }
 

@@ -11,6 +11,12 @@ defined in ``gen.c``):
 * indexer K       : integers U{-8..8} (or N(0,1) rounded to bf16 for the float workload),
                     stored as FP8 E4M3 with unit scale, [N][D_I] per sequence
 * indexer q       : same distribution as indexer K, [H_I][D_I] per query and layer
+* MXFP4 indexer   : (workloads with the MXFP4 indexer format) rows of D_I / 2 code bytes
+                    and D_I / 32 E8M0 scale bytes drawn directly in that format: every
+                    4-bit E2M1 code uniform over its 16 values (counter = element), every
+                    scale byte uniform over {126, 127} (counter = 2^40 + block), for K and q
+                    alike.  Values are then multiples of 1/4 and every score is a multiple
+                    of 1/16 below 2^20, which fp32 holds exactly.
 * main query      : bf16 N(0,1) (fp64 -> fp32 -> bf16, round-to-nearest-even), [H][512]
                     per query and layer
 * query positions : the last token of each decode context, or consecutive tokens
@@ -156,6 +162,7 @@ class Workload:
     float_indexer: bool = False          # bf16 N(0,1) indexer inputs instead of integers
     n_win: int = 0         # SWA window of every layer (0: no SWA branch)
     swa_ring: int = 0      # rows of each sequence's SWA KV ring
+    indexer_fmt: int = 0   # 0: E4M3 indexer rows of D_I bytes; 1: MXFP4 rows
 
     @property
     def n_seq(self) -> int:
@@ -168,6 +175,11 @@ class Workload:
     @property
     def kv_seq_stride(self) -> int:
         return self.N
+
+    @property
+    def idx_row_bytes(self) -> int:
+        """Bytes of one indexer q or K row in the workload's indexer format."""
+        return self.D_I // 2 + self.D_I // 32 if self.indexer_fmt else self.D_I
 
     def seed_of_seq(self, s: int) -> int:
         return int(self.seeds[s])
@@ -211,6 +223,37 @@ class Workload:
         key = stream_key(self.workload_id, self.seed_of_seq(s), TENSOR_KI)
         vals = self._indexer_values(key, 0, self.N * self.D_I)
         return float_to_e4m3_bytes(vals).reshape(self.N, self.D_I)
+
+    def _mx_rows(self, key: int, row0: int, n_rows: int) -> np.ndarray:
+        """MXFP4 rows [n_rows][D_I/2 + D_I/32] drawn in the format (see the recipe)."""
+        d = self.D_I
+        nib = uniform_int8(key, row0 * d, n_rows * d, 0, 15).astype(np.uint8).reshape(n_rows, d)
+        sc = uniform_int8(key, (1 << 40) + row0 * (d // 32), n_rows * (d // 32), 126, 127)
+        out = np.empty((n_rows, d // 2 + d // 32), dtype=np.uint8)
+        out[:, :d // 2] = nib[:, 0::2] | (nib[:, 1::2] << 4)
+        out[:, d // 2:] = sc.astype(np.uint8).reshape(n_rows, d // 32)
+        return out
+
+    def ki_rows(self, s: int) -> np.ndarray:
+        """Indexer K [N][idx_row_bytes] of sequence s in the workload's indexer format."""
+        if not self.indexer_fmt:
+            return self.ki_fp8(s)
+        key = stream_key(self.workload_id, self.seed_of_seq(s), TENSOR_KI)
+        return self._mx_rows(key, 0, self.N)
+
+    def qi_rows(self, layer: int, qs: Optional[Sequence[int]] = None) -> np.ndarray:
+        """Indexer queries [len(qs)][H_I][idx_row_bytes] of one layer in the indexer format."""
+        if not self.indexer_fmt:
+            return self.qi_fp8(layer, qs)
+        qs = range(self.B) if qs is None else qs
+        out = []
+        for q in qs:
+            s, j = divmod(q, self.q_per_seq)
+            key = stream_key(self.workload_id, self.seed_of_seq(s), TENSOR_QI, layer)
+            out.append(self._mx_rows(key, j * self.H_I, self.H_I))
+        if not out:
+            return np.zeros((0, self.H_I, self.idx_row_bytes), np.uint8)
+        return np.stack(out)
 
     def swa_kv(self, layer: int, s: int) -> np.ndarray:
         """E4M3 bytes [swa_ring][D] of layer `layer`'s SWA KV ring of sequence s
@@ -285,8 +328,13 @@ DECODER20 = Workload("decoder20_prod_b32_ctx64k", 8, B=32, N=65536, H=64, H_I=32
                      ratio=1, seeds=tuple(_seeds(8000, 32)),
                      modes=(FULL, REUSE, REUSE, REUSE) + (REINDEX, REUSE, REUSE, REUSE) * 4,
                      pool=16384, pool_block=8, n_win=128, swa_ring=128)
+# The production decoder with the indexer query and key in MXFP4 (68-byte rows).
+DECODER20_MX = Workload("decoder20_mxfp4_b32_ctx64k", 9, B=32, N=65536, H=64, H_I=32, D_I=128,
+                        k=512, ratio=1, seeds=tuple(_seeds(9000, 32)),
+                        modes=(FULL, REUSE, REUSE, REUSE) + (REINDEX, REUSE, REUSE, REUSE) * 4,
+                        pool=16384, pool_block=8, n_win=128, swa_ring=128, indexer_fmt=1)
 PREFILL_128K = Workload("prefill_4096q_ctx128k", 5, B=4096, N=32768, H=64, H_I=8, k=2048,
                         q_per_seq=4096, seeds=(5000,), first_pos=126976, float_indexer=True)
 
 WORKLOADS = {w.name: w for w in (TINY_FULL, DECODE_64K, GROUP_128K, HIER_1M, PREFILL_128K,
-                                  HIER_BLOCK_1M, DECODE_64K_SWA, DECODER20)}
+                                  HIER_BLOCK_1M, DECODE_64K_SWA, DECODER20, DECODER20_MX)}

@@ -20,9 +20,9 @@ from .synthetic import FULL, REINDEX, REUSE, Workload
 class DeviceInputs:
     w: Workload
     kv_fp4: torch.Tensor            # uint8 [S*N][288]
-    ki_fp8: torch.Tensor            # uint8 [S*N][D_I]
+    ki_fp8: torch.Tensor            # uint8 [S*N][idx_row_bytes] indexer K (E4M3 or MXFP4)
     q: List[torch.Tensor]           # int16 (bf16 bits) [B][H][D] per layer
-    qi: List[Optional[torch.Tensor]]  # uint8 [B][H_I][D_I] per layer (None for REUSE)
+    qi: List[Optional[torch.Tensor]]  # uint8 [B][H_I][idx_row_bytes] per layer (None: REUSE)
     q_pos: torch.Tensor             # int32 [B]
     swa: Optional[List[torch.Tensor]] = None  # uint8 E4M3 [S][ring][D] per layer (n_win > 0)
 
@@ -35,7 +35,7 @@ class DeviceInputs:
         return csa2.LayerGroup(w.modes, self.q, self.qi, self.kv_fp4, self.ki_fp8, w.N,
                                w.kv_seq_stride, w.q_per_seq, self.q_pos, w.ratio, w.k, w.pool,
                                self.scale, pool_block=w.pool_block, swa_kv=self.swa,
-                               n_win=w.n_win, **kw)
+                               n_win=w.n_win, indexer_fmt=w.indexer_fmt, **kw)
 
 
 def _to_dev(a: np.ndarray, device, dtype=None) -> torch.Tensor:
@@ -48,7 +48,7 @@ def _to_dev(a: np.ndarray, device, dtype=None) -> torch.Tensor:
 def prepare(w: Workload, device="cuda", layers: Optional[int] = None) -> DeviceInputs:
     S, N = w.n_seq, w.N
     kv = torch.empty((S * N, w.row_bytes), dtype=torch.uint8, device=device)
-    ki = torch.empty((S * N, w.D_I), dtype=torch.uint8, device=device)
+    ki = torch.empty((S * N, w.idx_row_bytes), dtype=torch.uint8, device=device)
     rows_per_chunk = max(1, min(N, (256 << 20) // (w.D * 4)))
     host = torch.empty((rows_per_chunk, w.D), dtype=torch.float32).pin_memory()
     dev_chunk = torch.empty((rows_per_chunk, w.D), dtype=torch.float32, device=device)
@@ -58,11 +58,11 @@ def prepare(w: Workload, device="cuda", layers: Optional[int] = None) -> DeviceI
             w.kv_latent(s, r0, n, out=host.numpy()[:n])
             dev_chunk[:n].copy_(host[:n], non_blocking=False)
             csa2.quantize_kv_fp4(dev_chunk[:n], out=kv[s * N + r0:s * N + r0 + n])
-        ki[s * N:(s + 1) * N].copy_(torch.from_numpy(w.ki_fp8(s)))
+        ki[s * N:(s + 1) * N].copy_(torch.from_numpy(w.ki_rows(s)))
     torch.cuda.synchronize()
     L = len(w.modes) if layers is None else layers
     q = [_to_dev(w.q_bf16(l).view(np.int16), device) for l in range(L)]
-    qi = [None if w.modes[l] == REUSE else _to_dev(w.qi_fp8(l), device) for l in range(L)]
+    qi = [None if w.modes[l] == REUSE else _to_dev(w.qi_rows(l), device) for l in range(L)]
     q_pos = _to_dev(w.q_pos(), device)
     swa = None
     if w.n_win > 0:
