@@ -81,7 +81,7 @@ csa2_status check_indexer_mx(const uint8_t* q, const uint8_t* k, int B, int H_I,
                              int ratio, int64_t kv_seq_stride, int q_per_seq) {
   if (B > 0 && (!q || !k)) return CSA2_ERR_INVALID_ARG;
   if (ratio < 1 || H_I < 1) return CSA2_ERR_INVALID_ARG;
-  if (D_I != 128 || H_I > 64) return CSA2_ERR_UNSUPPORTED;
+  if (D_I != 128 || H_I > 64) return CSA2_ERR_UNSUPPORTED;  // the kernels stage <= 64 rows
   if (!aligned16(k)) return CSA2_ERR_INVALID_ARG;
   if (B > q_per_seq && kv_seq_stride % 4 != 0) return CSA2_ERR_UNSUPPORTED;
   return CSA2_OK;

@@ -133,9 +133,11 @@ __device__ __forceinline__ void mma_16816(float c[4], uint32_t a0, uint32_t a1, 
 }
 
 // wA[b], wB[b]: code word 4b + t of entries g and g + 8; bq[b]: the lane's B
-// registers of steps (b, 0) and (b, 1).
+// registers of steps (b, 0) and (b, 1).  The two steps of a block go to
+// separate accumulators (two independent MMA chains), added at the end.
 __device__ __forceinline__ void mx16_dot(const uint32_t wA[4], const uint32_t wB[4],
                                          const uint4 bq[4], float c[4]) {
+  float d[4] = {0.f, 0.f, 0.f, 0.f};
   c[0] = c[1] = c[2] = c[3] = 0.0f;
 #pragma unroll
   for (int b = 0; b < 4; ++b) {
@@ -143,20 +145,48 @@ __device__ __forceinline__ void mx16_dot(const uint32_t wA[4], const uint32_t wB
     e2m1_word_to_f16x2(wA[b], hA);
     e2m1_word_to_f16x2(wB[b], hB);
     mma_16816(c, hA[0], hB[0], hA[1], hB[1], bq[b].x, bq[b].y);
-    mma_16816(c, hA[2], hB[2], hA[3], hB[3], bq[b].z, bq[b].w);
+    mma_16816(d, hA[2], hB[2], hA[3], hB[3], bq[b].z, bq[b].w);
   }
+#pragma unroll
+  for (int i = 0; i < 4; ++i) c[i] += d[i];
 }
 
-// qsum[d] = sum_h value(q[h][d]) for one query (MXFP4 rows of kMxDI), by
-// compensated (Neumaier) fp32 summation of the exact decoded values.
-__device__ __forceinline__ float mx_qsum_dim(const uint8_t* __restrict__ q, int H_I, int d) {
+// Two groups of 16 entries (32 entries) at once: four independent MMA chains.
+__device__ __forceinline__ void mx32_dot(const uint32_t w[2][2][4], const uint4 bq[4],
+                                         float c[2][4]) {
+  float d[2][4];
+#pragma unroll
+  for (int x = 0; x < 2; ++x)
+#pragma unroll
+    for (int i = 0; i < 4; ++i) c[x][i] = d[x][i] = 0.0f;
+#pragma unroll
+  for (int b = 0; b < 4; ++b) {
+#pragma unroll
+    for (int x = 0; x < 2; ++x) {
+      uint32_t hA[4], hB[4];
+      e2m1_word_to_f16x2(w[x][0][b], hA);
+      e2m1_word_to_f16x2(w[x][1][b], hB);
+      mma_16816(c[x], hA[0], hB[0], hA[1], hB[1], bq[b].x, bq[b].y);
+      mma_16816(d[x], hA[2], hB[2], hA[3], hB[3], bq[b].z, bq[b].w);
+    }
+  }
+#pragma unroll
+  for (int x = 0; x < 2; ++x)
+#pragma unroll
+    for (int i = 0; i < 4; ++i) c[x][i] += d[x][i];
+}
+
+// qsum[d] = sum_h value(q[h][d]) of one query from its H_I rows staged in
+// shared memory, by compensated (Neumaier) fp32 summation of the exact
+// decoded values.
+__device__ __forceinline__ float mx_qsum_dim(const uint8_t* q, int H_I, int d) {
   float s = 0.0f, comp = 0.0f;
   for (int h = 0; h < H_I; ++h) {
-    const uint8_t* row = q + (int64_t)h * kMxRow;
-    const uint32_t byte = __ldg(row + d / 2);
+    const uint8_t* row = q + h * kMxRow;
+    const uint32_t byte = row[d / 2];
     const uint32_t code = (d & 1) ? (byte >> 4) : (byte & 15u);
-    const float v = half2_bits_to_float2(e2m1x2_to_f16x2(code)).x *
-                    e8m0_to_float(__ldg(row + kMxCodes + d / 32));
+    const float v =
+        half2_bits_to_float2(e2m1x2_to_f16x2(code)).x * e8m0_to_float(row[kMxCodes + d / 32]);
     const float t = s + v;
     comp += (fabsf(s) >= fabsf(v)) ? ((s - t) + v) : ((v - t) + s);
     s = t;
@@ -164,12 +194,16 @@ __device__ __forceinline__ float mx_qsum_dim(const uint8_t* __restrict__ q, int 
   return s + comp;
 }
 
-// The B registers of up to kQChunk queries, built by `nthreads` threads
-// (>= 128, a multiple of 32): qsum of each dim, a power-of-two scale 2^e_b per
+constexpr int kMaxHI = 64;
+
+// The B registers of up to kQChunk queries, built by kThreads threads (a
+// multiple of 32, >= 64): qsum of each dim, a power-of-two scale 2^e_b per
 // 32-dim block putting the block's largest |qsum| in [2^14, 2^15), then the
-// f16 parts.  qfrag[ql][b][lane] holds lane's registers of steps (b, 0),
-// (b, 1); qscale[ql][b] = 2^e_b.  Ends with a barrier of the `bar` group.
+// f16 parts.  frag[ql][b][lane] holds lane's registers of steps (b, 0),
+// (b, 1); qscale[ql][b] = 2^e_b.  Each query's H_I rows are first copied to
+// shared memory with independent loads (one memory latency, not H_I).
 struct QFrag {
+  __align__(16) uint8_t qraw[kMaxHI * kMxRow];
   float qs[kQChunk][kMxDI];
   uint4 frag[kQChunk][4][32];
   float qscale[kQChunk][4];
@@ -189,20 +223,43 @@ __device__ __forceinline__ void build_qfrag(QFrag& f, const uint8_t* __restrict_
                                             int q0, int nq) {
   const int tid = threadIdx.x;
   const int lane = tid & 31;
-  for (int i = tid; i < nq * kMxDI; i += kThreads) {  // thread i % 128 always takes dim i % 128
-    const int ql = i / kMxDI, d = i % kMxDI;
-    const float v = mx_qsum_dim(q_mx + (int64_t)(q0 + ql) * H_I * kMxRow, H_I, d);
-    float a = fabsf(v);
+  const int nbytes = H_I * kMxRow;
+  for (int ql = 0; ql < nq; ++ql) {
+    const uint8_t* src = q_mx + (int64_t)(q0 + ql) * nbytes;
+    if ((reinterpret_cast<uintptr_t>(src) & 3u) == 0) {  // rows are 68 bytes: words
+      constexpr int kPer = (kMaxHI * kMxRow / 4 + kThreads - 1) / kThreads;
+      const uint32_t* s4 = reinterpret_cast<const uint32_t*>(src);
+      uint32_t* d4 = reinterpret_cast<uint32_t*>(f.qraw);
+      uint32_t v[kPer];
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, o));
-    int e = 0;
-    if (a > 0.0f) {
-      int ex;
-      frexpf(a, &ex);  // a = m 2^ex, m in [0.5, 1): floor(log2 a) = ex - 1
-      e = ex - 1 - 14;
+      for (int i = 0; i < kPer; ++i) {
+        const int o = tid + i * kThreads;
+        v[i] = o < nbytes / 4 ? __ldg(s4 + o) : 0u;
+      }
+#pragma unroll
+      for (int i = 0; i < kPer; ++i) {
+        const int o = tid + i * kThreads;
+        if (o < nbytes / 4) d4[o] = v[i];
+      }
+    } else {
+      for (int o = tid; o < nbytes; o += kThreads) f.qraw[o] = __ldg(src + o);
     }
-    f.qs[ql][d] = ldexpf(v, -e);
-    if (lane == 0) f.qscale[ql][d / 32] = ldexpf(1.0f, e);
+    asm volatile("bar.sync %0, %1;" ::"n"(kBarId), "n"(kThreads) : "memory");
+    for (int d = tid; d < kMxDI; d += kThreads) {  // whole warps: a warp's dims form one block
+      const float x = mx_qsum_dim(f.qraw, H_I, d);
+      float a = fabsf(x);
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, o));
+      int e = 0;
+      if (a > 0.0f) {
+        int ex;
+        frexpf(a, &ex);  // a = m 2^ex, m in [0.5, 1): floor(log2 a) = ex - 1
+        e = ex - 1 - 14;
+      }
+      f.qs[ql][d] = ldexpf(x, -e);
+      if (lane == 0) f.qscale[ql][d / 32] = ldexpf(1.0f, e);
+    }
+    asm volatile("bar.sync %0, %1;" ::"n"(kBarId), "n"(kThreads) : "memory");
   }
   asm volatile("bar.sync %0, %1;" ::"n"(kBarId), "n"(kThreads) : "memory");
   uint32_t* words = reinterpret_cast<uint32_t*>(&f.frag[0][0][0]);
@@ -288,9 +345,14 @@ mx_scores_kernel(const uint8_t* __restrict__ q_mx, const uint8_t* __restrict__ k
     int64_t n = 0;  // loads issued
     int cur_s = -1;
     int64_t vis = 0;
-    for (int64_t tile = t_begin; tile < t_end; ++tile) {
-      const int s = (int)(tile / T);
-      const int64_t row0 = (tile - (int64_t)s * T) * kTileRows;
+    int s = (int)(t_begin / T);
+    int64_t tt = t_begin - (int64_t)s * T;
+    for (int64_t tile = t_begin; tile < t_end; ++tile, ++tt) {
+      if (tt == T) {
+        tt = 0;
+        ++s;
+      }
+      const int64_t row0 = tt * kTileRows;
       if (s != cur_s) {
         cur_s = s;
         vis = seq_vis_max(q_pos, s, q_per_seq, B, ratio, N);
@@ -318,13 +380,23 @@ mx_scores_kernel(const uint8_t* __restrict__ q_mx, const uint8_t* __restrict__ k
   }
 
   // ---------------- consumers: warp w scores entries 32w .. 32w + 31 of a tile ----------------
+  // Entries past the loaded rows of a ragged tile read stale (or never
+  // written) shared memory: any byte is a valid pair of E2M1 codes, so the
+  // products stay finite, and their scale is taken as 0.
   const int g = lane >> 2, t = lane & 3;
   int64_t n = 0;  // loads consumed
-  int cur_s = -1, cur_chunk = -1;
+  int cur_s = -1, cur_chunk = -1, reg_q = -1;
   int64_t vis = 0;
-  for (int64_t tile = t_begin; tile < t_end; ++tile) {
-    const int s = (int)(tile / T);
-    const int64_t row0 = (tile - (int64_t)s * T) * kTileRows;
+  uint4 bq[4];
+  float qs_t = 0.0f;
+  int s = (int)(t_begin / T);
+  int64_t tt = t_begin - (int64_t)s * T;
+  for (int64_t tile = t_begin; tile < t_end; ++tile, ++tt) {
+    if (tt == T) {
+      tt = 0;
+      ++s;
+    }
+    const int64_t row0 = tt * kTileRows;
     if (s != cur_s) {
       cur_s = s;
       cur_chunk = -1;
@@ -340,46 +412,54 @@ mx_scores_kernel(const uint8_t* __restrict__ q_mx, const uint8_t* __restrict__ k
     const uint32_t* tw = reinterpret_cast<const uint32_t*>(tileb);
     const int q_first = s * q_per_seq;
     const int q_last = min(B, q_first + q_per_seq);
+    const int r0 = warp * 32 + g;  // entries r0, r0 + 8, r0 + 16, r0 + 24
     for (int qc = q_first; qc < q_last; qc += kQChunk) {
       const int nq = min(kQChunk, q_last - qc);
       if (qc != cur_chunk) {
         asm volatile("bar.sync 1, %0;" ::"n"(kConsumers) : "memory");
         build_qfrag<kConsumers, 1>(sm.qf, q_mx, H_I, qc, nq);
         cur_chunk = qc;
+        reg_q = -1;
       }
       for (int ql = 0; ql < nq; ++ql) {
         const int q = qc + ql;
+        if (q != reg_q) {
+#pragma unroll
+          for (int b = 0; b < 4; ++b) bq[b] = sm.qf.frag[ql][b][lane];
+          qs_t = sm.qf.qscale[ql][t];
+          reg_q = q;
+        }
         const int64_t nv = n_visible(q_pos, q, ratio, N);
         float* srow = scores + (int64_t)q * N + row0;
-        uint4 bq[4];
+        float p[4] = {0.f, 0.f, 0.f, 0.f};  // entries r0 + 8 i
+        if (rows > 0) {  // tile-uniform
+          uint32_t w[2][2][4];
 #pragma unroll
-        for (int b = 0; b < 4; ++b) bq[b] = sm.qf.frag[ql][b][lane];
-        const float qs_t = sm.qf.qscale[ql][t];
+          for (int x = 0; x < 2; ++x)
 #pragma unroll
-        for (int grp = 0; grp < 2; ++grp) {
-          const int rA = warp * 32 + grp * 16 + g, rB = rA + 8;
-          float pA = 0.0f, pB = 0.0f;
-          if (rows > 0) {  // tile-uniform
-            uint32_t wA[4], wB[4];
+            for (int y = 0; y < 2; ++y)
 #pragma unroll
-            for (int b = 0; b < 4; ++b) {
-              wA[b] = rA < rows ? tw[rA * (kMxRow / 4) + 4 * b + t] : 0u;
-              wB[b] = rB < rows ? tw[rB * (kMxRow / 4) + 4 * b + t] : 0u;
+              for (int b = 0; b < 4; ++b)
+                w[x][y][b] = tw[(r0 + 16 * x + 8 * y) * (kMxRow / 4) + 4 * b + t];
+          float c[2][4];
+          mx32_dot(w, bq, c);
+#pragma unroll
+          for (int x = 0; x < 2; ++x)
+#pragma unroll
+            for (int y = 0; y < 2; ++y) {
+              const int r = r0 + 16 * x + 8 * y;
+              const float ks = r < rows ? e8m0_to_float(tileb[r * kMxRow + kMxCodes + t]) : 0.0f;
+              p[2 * x + y] = (c[x][2 * y] + c[x][2 * y + 1]) * (ks * qs_t);
             }
-            float c[4];
-            mx16_dot(wA, wB, bq, c);
-            const float ksA = rA < rows ? e8m0_to_float(tileb[rA * kMxRow + kMxCodes + t]) : 0.0f;
-            const float ksB = rB < rows ? e8m0_to_float(tileb[rB * kMxRow + kMxCodes + t]) : 0.0f;
-            pA = (c[0] + c[1]) * (ksA * qs_t);
-            pB = (c[2] + c[3]) * (ksB * qs_t);
-            pA += __shfl_xor_sync(0xffffffffu, pA, 1);
-            pB += __shfl_xor_sync(0xffffffffu, pB, 1);
-            pA += __shfl_xor_sync(0xffffffffu, pA, 2);
-            pB += __shfl_xor_sync(0xffffffffu, pB, 2);
-          }
-          if (t == 0 && rA < rows_in_tile) srow[rA] = (row0 + rA < nv) ? pA : -INFINITY;
-          if (t == 1 && rB < rows_in_tile) srow[rB] = (row0 + rB < nv) ? pB : -INFINITY;
+#pragma unroll
+          for (int i = 0; i < 4; ++i) p[i] += __shfl_xor_sync(0xffffffffu, p[i], 1);
+#pragma unroll
+          for (int i = 0; i < 4; ++i) p[i] += __shfl_xor_sync(0xffffffffu, p[i], 2);
         }
+        // lane t of the quad stores entry r0 + 8 t
+        const float v = t == 0 ? p[0] : (t == 1 ? p[1] : (t == 2 ? p[2] : p[3]));
+        const int r = r0 + 8 * t;
+        if (r < rows_in_tile) srow[r] = (row0 + r < nv) ? v : -INFINITY;
       }
     }
     if (rows > 0) {
