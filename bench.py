@@ -371,12 +371,17 @@ def run_gpu(args, rank, world, local):
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
-        "dtype": "fp16-mma/fp32-acc (fp4 KV, e4m3 indexer)",
-        "data": "synthetic (seeded SplitMix64: N(0,1) latent -> FP4, integer E4M3 indexer, "
-                "bf16 N(0,1) queries)",
+        "dtype": ("fp16-mma/fp32-acc (fp4 KV, mxfp4 indexer)" if w.indexer_fmt else
+                  "fp16-mma/fp32-acc (fp4 KV, e4m3 indexer)"),
+        "data": ("synthetic (seeded SplitMix64: N(0,1) latent -> FP4, MXFP4 indexer rows drawn "
+                 "in format, bf16 N(0,1) queries)" if w.indexer_fmt else
+                 "synthetic (seeded SplitMix64: N(0,1) latent -> FP4, "
+                 + ("bf16 N(0,1)" if w.float_indexer else "integer") + " E4M3 indexer, "
+                 "bf16 N(0,1) queries)"),
         "config": {"workload": w.name, "queries": w.B, "entries_per_seq": w.N,
                    "ctx_tokens": w.N * w.ratio, "heads": w.H, "indexer_heads": w.H_I,
                    "top_k": w.k, "modes": [["FULL", "REINDEX", "REUSE"][m] for m in w.modes],
+                   "indexer": "mxfp4" if w.indexer_fmt else "e4m3",
                    "l2": "flushed before every timed step (512 MiB write, then 256 MiB read)",
                    "cuda_graph": True, "parallelism": f"replicas x{world}"},
         "step_bytes": step_bytes,
