@@ -9,7 +9,9 @@
 // and the first `need` members of the class, in ascending position.
 //
 // Rows of up to 32768 candidates (topk_reg_kernel, one 512-thread CTA per
-// row): each thread holds KPT consecutive keys in registers.  The radix
+// row; topk_cluster_kernel, a cluster of 4 or 8 such CTAs per row when the
+// batch alone would leave most SMs idle): each thread holds KPT consecutive
+// keys in registers.  The radix
 // passes take 8-bit digits from the highest bit where the row's min and max
 // keys differ down to the lowest bit that differs between two keys of the
 // selected sign (OR ^ AND per sign; integer-valued scores skip their zero
@@ -359,6 +361,251 @@ topk_reg_kernel(const float* __restrict__ scores, int64_t N, int k,
   }
 }
 
+// ---------------------------------------------------------------------------
+// Cluster variant for batches too small to fill the GPU one row per CTA: a
+// cluster of CL CTAs shares a row, CTA r holding the KPT * kRegThreads keys
+// from position r * KPT * kRegThreads on.  Every step that needs the whole row
+// (OR / AND of the keys, each pass's digit counts, the counts of keys above
+// and inside the threshold class before each CTA) is exchanged through
+// distributed shared memory: a CTA publishes its values in its own shared
+// memory, one cluster barrier (release / acquire) makes them visible, and
+// every CTA reads all CL copies, so all of them take the same decisions.  The
+// per-pass counts are double-buffered: a buffer is rewritten two passes
+// later, after the next barrier has shown that every peer has read it.  A
+// final barrier keeps every CTA's shared memory alive until its peers' last
+// reads are done.
+// ---------------------------------------------------------------------------
+
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+
+__device__ __forceinline__ void cluster_barrier() {
+  asm volatile(
+      "barrier.cluster.arrive.release.aligned;\n\t"
+      "barrier.cluster.wait.acquire.aligned;" ::
+          : "memory");
+}
+
+// The shared-memory word at `p` (this CTA's address) in cluster CTA `rank`.
+__device__ __forceinline__ uint32_t ld_peer(const void* p, uint32_t rank) {
+  uint32_t a = static_cast<uint32_t>(__cvta_generic_to_shared(p)), ra, v;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(ra) : "r"(a), "r"(rank));
+  asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(ra) : "memory");
+  return v;
+}
+
+template <int KPT, int CL>
+__global__ void __launch_bounds__(kRegThreads, 1)
+topk_cluster_kernel(const float* __restrict__ scores, int64_t N, int k,
+                    const int32_t* __restrict__ q_pos, int ratio,
+                    const int32_t* __restrict__ n_valid, const int32_t* __restrict__ map,
+                    int32_t* __restrict__ idx) {
+  __shared__ __align__(16) int32_t whist[2][kRegWarps * 256];
+  __shared__ __align__(16) int32_t csum[256];
+  __shared__ __align__(16) int32_t pub[2][256];  // this CTA's digit counts (descending digits)
+  __shared__ uint32_t pub_bits[4];               // this CTA's OR / AND per sign
+  __shared__ int32_t pub_cnt[2];                 // keys above / inside the class in this CTA
+  __shared__ uint32_t all_bits[4 * CL];
+  __shared__ int32_t all_cnt[2 * CL];
+  __shared__ int32_t tot[kRegWarps + 1];
+  __shared__ uint32_t red[4][kRegWarps];
+
+  pdl_trigger();
+  pdl_wait();  // scores, n_valid and map come from the kernel before
+  const int b = blockIdx.y;
+  const uint32_t rank = cluster_ctarank();
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const float* row = scores + (int64_t)b * N;
+  const int32_t* mrow = map ? map + (int64_t)b * N : nullptr;
+  int32_t* out = idx + (int64_t)b * k;
+
+  int n;  // candidates of the row, the same in every CTA of the cluster
+  if (map) {
+    int c = 0;
+    for (int64_t j = tid; j < N; j += kRegThreads) c += (mrow[j] >= 0);
+    int t;
+    reg_block_scan(c, tot, &t);
+    n = t;
+  } else if (n_valid) {
+    n = n_valid[b];
+  } else {
+    n = (int)n_visible(q_pos, b, ratio, N);
+  }
+  if (n <= k) {  // the whole cluster leaves here together
+    if (rank == 0)
+      for (int j = tid; j < k; j += kRegThreads) out[j] = (j < n) ? (mrow ? mrow[j] : j) : -1;
+    return;
+  }
+
+  const int base = (int)rank * (KPT * kRegThreads) + tid * KPT;  // row position of key[0]
+  uint32_t key[KPT];
+  const bool vec = ((N & 3) == 0) && ((reinterpret_cast<uintptr_t>(scores) & 15u) == 0);
+#pragma unroll
+  for (int i = 0; i < KPT; i += 4) {
+    const int j = base + i;
+    float v[4];
+    if (vec && j + 3 < n) {
+      const float4 f = *reinterpret_cast<const float4*>(row + j);
+      v[0] = f.x; v[1] = f.y; v[2] = f.z; v[3] = f.w;
+    } else {
+#pragma unroll
+      for (int e = 0; e < 4; ++e) v[e] = (j + e < n) ? row[j + e] : 0.0f;
+    }
+#pragma unroll
+    for (int e = 0; e < 4; ++e) key[i + e] = float_to_ordered(v[e]);
+  }
+
+  // OR / AND of the keys per sign (see topk_reg_kernel), over the cluster
+  uint32_t por = 0u, pand = 0xFFFFFFFFu, nor = 0u, nand = 0xFFFFFFFFu;
+#pragma unroll
+  for (int i = 0; i < KPT; ++i) {
+    const uint32_t valid = base + i < n ? 0xFFFFFFFFu : 0u;
+    const uint32_t pos = valid & (0u - (key[i] >> 31));
+    const uint32_t neg = valid & ~pos;
+    por |= key[i] & pos;
+    pand &= key[i] | ~pos;
+    nor |= key[i] & neg;
+    nand &= key[i] | ~neg;
+  }
+  por = __reduce_or_sync(0xffffffffu, por);
+  pand = __reduce_and_sync(0xffffffffu, pand);
+  nor = __reduce_or_sync(0xffffffffu, nor);
+  nand = __reduce_and_sync(0xffffffffu, nand);
+  if (lane == 0) {
+    red[0][warp] = por;
+    red[1][warp] = pand;
+    red[2][warp] = nor;
+    red[3][warp] = nand;
+  }
+  for (int i = tid; i < kRegWarps * 256; i += kRegThreads) whist[0][i] = 0;
+  __syncthreads();
+  if (tid < 4) {
+    uint32_t v = (tid & 1) ? 0xFFFFFFFFu : 0u;
+#pragma unroll
+    for (int w = 0; w < kRegWarps; ++w) v = (tid & 1) ? (v & red[tid][w]) : (v | red[tid][w]);
+    pub_bits[tid] = v;
+  }
+  cluster_barrier();
+  if (tid < 4 * CL) all_bits[tid] = ld_peer(&pub_bits[tid & 3], (uint32_t)(tid >> 2));
+  __syncthreads();
+  por = 0u; pand = 0xFFFFFFFFu; nor = 0u; nand = 0xFFFFFFFFu;
+#pragma unroll
+  for (int r = 0; r < CL; ++r) {
+    por |= all_bits[4 * r];
+    pand &= all_bits[4 * r + 1];
+    nor |= all_bits[4 * r + 2];
+    nand &= all_bits[4 * r + 3];
+  }
+  const int lo_pos = (por ^ pand) ? __ffs(por ^ pand) - 1 : 32;
+  const int lo_neg = (nor ^ nand) ? __ffs(nor ^ nand) - 1 : 32;
+  const uint32_t kor = por | nor, kand = pand & nand;
+
+  uint32_t prefix = kand, mask = 0xFFFFFFFFu;
+  int cur_hi = -1, lo = 0;
+  if (kor != kand) {
+    cur_hi = 31 - __clz(kor ^ kand);
+    mask = ~((2u << cur_hi) - 1u);
+    prefix = kand & mask;
+    lo = min(cur_hi, cur_hi == 31 ? min(lo_pos, lo_neg) : ((kor >> 31) ? lo_pos : lo_neg));
+  }
+  int need = k;
+  for (int pass = 0; cur_hi >= lo; ++pass) {
+    const int nbits = min(8, cur_hi + 1 - lo);
+    const int shift = cur_hi + 1 - nbits;
+    const uint32_t dmask = (1u << nbits) - 1u;
+    int32_t* hist = whist[pass & 1];
+    int32_t* my_hist = hist + warp * 256;
+#pragma unroll
+    for (int i = 0; i < KPT; ++i) {
+      if (base + i < n && (key[i] & mask) == prefix)
+        atomicAdd(&my_hist[(key[i] >> shift) & dmask], 1);
+    }
+    __syncthreads();
+    if (tid < 256) {
+      const int d = 255 - tid;
+      int c = 0;
+#pragma unroll
+      for (int w = 0; w < kRegWarps; ++w) c += hist[w * 256 + d];
+      pub[pass & 1][tid] = c;
+    } else {
+      int32_t* next = whist[(pass + 1) & 1];
+      for (int i = tid - 256; i < kRegWarps * 256; i += kRegThreads - 256) next[i] = 0;
+    }
+    cluster_barrier();
+    if (tid < 256) {
+      int c = 0;
+#pragma unroll
+      for (int r = 0; r < CL; ++r) c += (int)ld_peer(&pub[pass & 1][tid], (uint32_t)r);
+      csum[tid] = c;
+    }
+    __syncthreads();
+    int above, cnt;
+    const int digit = select_digit(csum, need, &above, &cnt);
+    need -= above;
+    prefix |= (uint32_t)digit << shift;
+    mask |= dmask << shift;
+    cur_hi = shift - 1;
+    lo = (prefix >> 31) ? lo_pos : lo_neg;
+    if (cnt == need) break;
+  }
+
+  // ordered write (see topk_reg_kernel), offset by the keys above / inside
+  // the class held by the lower-ranked CTAs of the cluster
+  uint32_t gtm[(KPT + 31) / 32], eqm[(KPT + 31) / 32];
+  int gt = 0, eq = 0;
+#pragma unroll
+  for (int w = 0; w < (KPT + 31) / 32; ++w) {
+    uint32_t g = 0u, e = 0u;
+#pragma unroll
+    for (int i = 0; i < 32 && 32 * w + i < KPT; ++i) {
+      const int ii = 32 * w + i;
+      const uint32_t km = key[ii] & mask;
+      const bool valid = base + ii < n;
+      g |= (uint32_t)(valid && km > prefix) << i;
+      e |= (uint32_t)(valid && km == prefix) << i;
+    }
+    gtm[w] = g;
+    eqm[w] = e;
+    gt += __popc(g);
+    eq += __popc(e);
+  }
+  int tot_packed;
+  const int before = reg_block_scan((gt << 16) | eq, tot, &tot_packed);
+  if (tid == 0) {
+    pub_cnt[0] = tot_packed >> 16;
+    pub_cnt[1] = tot_packed & 0xFFFF;
+  }
+  cluster_barrier();
+  if (tid < 2 * CL) all_cnt[tid] = (int32_t)ld_peer(&pub_cnt[tid & 1], (uint32_t)(tid >> 1));
+  __syncthreads();
+  cluster_barrier();  // every peer has read this CTA's counts: its shared memory may go
+  int gt_lower = 0, eq_lower = 0;
+  for (int r = 0; r < (int)rank; ++r) {
+    gt_lower += all_cnt[2 * r];
+    eq_lower += all_cnt[2 * r + 1];
+  }
+  const int eq_before = eq_lower + (before & 0xFFFF);
+  int take = max(0, min(eq, need - eq_before));
+  int off = gt_lower + (before >> 16) + min(eq_before, need);
+#pragma unroll
+  for (int w = 0; w < (KPT + 31) / 32; ++w) {
+    uint32_t sel = gtm[w];
+    for (uint32_t c = eqm[w]; take > 0 && c != 0u; --take) {
+      sel |= c & (~c + 1u);
+      c &= c - 1u;
+    }
+    while (sel != 0u && off < k) {
+      const int p = base + 32 * w + __ffs(sel) - 1;
+      sel &= sel - 1u;
+      out[off] = mrow ? mrow[p] : p;
+      ++off;
+    }
+  }
+}
+
 template <bool kSmem>
 __global__ void __launch_bounds__(kThreads, 1)
 topk_long_kernel(const float* __restrict__ scores, int64_t N, int k, const int32_t* __restrict__ q_pos,
@@ -569,6 +816,52 @@ cudaError_t launch_reg(dim3 grid, const float* scores, int64_t N, int k, const i
                        q_pos, ratio, n_valid, map, idx, chunk);
 }
 
+template <int KPT, int CL>
+cudaError_t launch_cluster(int B, const float* scores, int64_t N, int k, const int32_t* q_pos,
+                           int ratio, const int32_t* n_valid, const int32_t* map, int32_t* idx,
+                           cudaStream_t stream, bool pdl) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(CL, (unsigned)B);
+  cfg.blockDim = dim3(kRegThreads);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = CL;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 2 : 1;
+  return cudaLaunchKernelEx(&cfg, topk_cluster_kernel<KPT, CL>, scores, N, k, q_pos, ratio,
+                            n_valid, map, idx);
+}
+
+// Rows of <= 32768 candidates when one CTA per row leaves most SMs idle: a
+// cluster of 8 (B <= SMs / 8) or 4 (B <= SMs / 4) CTAs per row, each holding
+// at least 4 keys per thread.  Returns false when the shape does not qualify.
+bool cluster_launch(int B, const float* scores, int64_t N, int k, const int32_t* q_pos,
+                    int ratio, const int32_t* n_valid, const int32_t* map, int32_t* idx,
+                    cudaStream_t stream, bool pdl, cudaError_t* err) {
+  const int sms = device_sm_count();
+  const int CL = (B * 8 <= sms) ? 8 : ((B * 4 <= sms) ? 4 : 0);
+  if (CL == 0 || N > kRegMaxKeys) return false;
+  const int64_t per = (N + CL - 1) / CL;  // keys per CTA
+  const int kpt = per <= 4 * kRegThreads ? 4 : (per <= 8 * kRegThreads ? 8 : 16);
+  if ((int64_t)kpt * kRegThreads * CL < N) return false;
+  if (CL == 8) {
+    *err = kpt == 4 ? launch_cluster<4, 8>(B, scores, N, k, q_pos, ratio, n_valid, map, idx, stream, pdl)
+         : kpt == 8 ? launch_cluster<8, 8>(B, scores, N, k, q_pos, ratio, n_valid, map, idx, stream, pdl)
+                    : launch_cluster<16, 8>(B, scores, N, k, q_pos, ratio, n_valid, map, idx, stream, pdl);
+  } else {
+    *err = kpt == 4 ? launch_cluster<4, 4>(B, scores, N, k, q_pos, ratio, n_valid, map, idx, stream, pdl)
+         : kpt == 8 ? launch_cluster<8, 4>(B, scores, N, k, q_pos, ratio, n_valid, map, idx, stream, pdl)
+                    : launch_cluster<16, 4>(B, scores, N, k, q_pos, ratio, n_valid, map, idx, stream, pdl);
+  }
+  return true;
+}
+
 cudaError_t launch_reg_any(dim3 grid, const float* scores, int64_t N, int64_t keys, int k,
                            const int32_t* q_pos, int ratio, const int32_t* n_valid,
                            const int32_t* map, int32_t* idx, int chunk, cudaStream_t stream,
@@ -624,9 +917,12 @@ cudaError_t launch_topk(const float* scores, int B, int64_t N, int k, const int3
                         int ratio, const int32_t* n_valid, const int32_t* map, int32_t* idx,
                         cudaStream_t stream, bool pdl, void* scratch, size_t scratch_bytes) {
   if (B == 0) return cudaSuccess;
-  if (N <= kRegMaxKeys)
+  if (N <= kRegMaxKeys) {
+    cudaError_t e;
+    if (cluster_launch(B, scores, N, k, q_pos, ratio, n_valid, map, idx, stream, pdl, &e)) return e;
     return launch_reg_any(dim3((unsigned)B), scores, N, N, k, q_pos, ratio, n_valid, map, idx, 0,
                           stream, pdl);
+  }
   const size_t need = topk_scratch_bytes(B, N, k);
   if (!map && need > 0 && scratch && scratch_bytes >= need) {
     LongScratch ls;
