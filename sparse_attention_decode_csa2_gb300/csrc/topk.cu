@@ -371,9 +371,12 @@ topk_reg_kernel(const float* __restrict__ scores, int64_t N, int k,
 // memory, one cluster barrier (release / acquire) makes them visible, and
 // every CTA reads all CL copies, so all of them take the same decisions.  The
 // per-pass counts are double-buffered: a buffer is rewritten two passes
-// later, after the next barrier has shown that every peer has read it.  A
-// final barrier keeps every CTA's shared memory alive until its peers' last
-// reads are done.
+// later, after the next barrier has shown that every peer has read it.  From
+// the same per-peer counts each CTA also accumulates how many keys above the
+// class, and inside it, its lower-ranked peers hold: its output offsets.  The
+// last barrier is split: a CTA arrives once it has read its peers for the
+// last time and waits (so that its own shared memory outlives their reads)
+// only after writing its output.
 // ---------------------------------------------------------------------------
 
 __device__ __forceinline__ uint32_t cluster_ctarank() {
@@ -387,6 +390,27 @@ __device__ __forceinline__ void cluster_barrier() {
       "barrier.cluster.arrive.release.aligned;\n\t"
       "barrier.cluster.wait.acquire.aligned;" ::
           : "memory");
+}
+__device__ __forceinline__ void cluster_arrive_relaxed() {
+  asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait() {
+  asm volatile("barrier.cluster.wait.aligned;" ::: "memory");
+}
+
+// Sum of one int per thread over the first 256 threads (8 warps) of the
+// block; `scratch` holds 8 ints.  Every thread gets the total.  Ends with a
+// barrier of the whole block.
+__device__ __forceinline__ int sum256(int v, int32_t* scratch) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  v = __reduce_add_sync(0xffffffffu, v);
+  if (warp < 8 && lane == 0) scratch[warp] = v;
+  __syncthreads();
+  int t = 0;
+#pragma unroll
+  for (int w = 0; w < 8; ++w) t += scratch[w];
+  __syncthreads();
+  return t;
 }
 
 // The shared-memory word at `p` (this CTA's address) in cluster CTA `rank`.
@@ -407,9 +431,8 @@ topk_cluster_kernel(const float* __restrict__ scores, int64_t N, int k,
   __shared__ __align__(16) int32_t csum[256];
   __shared__ __align__(16) int32_t pub[2][256];  // this CTA's digit counts (descending digits)
   __shared__ uint32_t pub_bits[4];               // this CTA's OR / AND per sign
-  __shared__ int32_t pub_cnt[2];                 // keys above / inside the class in this CTA
   __shared__ uint32_t all_bits[4 * CL];
-  __shared__ int32_t all_cnt[2 * CL];
+  __shared__ int32_t red8[2][8];
   __shared__ int32_t tot[kRegWarps + 1];
   __shared__ uint32_t red[4][kRegWarps];
 
@@ -512,6 +535,10 @@ topk_cluster_kernel(const float* __restrict__ scores, int64_t N, int k,
     lo = min(cur_hi, cur_hi == 31 ? min(lo_pos, lo_neg) : ((kor >> 31) ? lo_pos : lo_neg));
   }
   int need = k;
+  // keys above the class / inside it held by the lower-ranked CTAs; with no
+  // pass (all keys equal) the class is every valid key
+  int gt_lower = 0;
+  int eq_lower = (int)min((int64_t)n, (int64_t)rank * (KPT * kRegThreads));
   for (int pass = 0; cur_hi >= lo; ++pass) {
     const int nbits = min(8, cur_hi + 1 - lo);
     const int shift = cur_hi + 1 - nbits;
@@ -535,15 +562,23 @@ topk_cluster_kernel(const float* __restrict__ scores, int64_t N, int k,
       for (int i = tid - 256; i < kRegWarps * 256; i += kRegThreads - 256) next[i] = 0;
     }
     cluster_barrier();
+    int lower = 0;  // this digit's count in the lower-ranked CTAs
     if (tid < 256) {
       int c = 0;
 #pragma unroll
-      for (int r = 0; r < CL; ++r) c += (int)ld_peer(&pub[pass & 1][tid], (uint32_t)r);
+      for (int r = 0; r < CL; ++r) {
+        const int v = (int)ld_peer(&pub[pass & 1][tid], (uint32_t)r);
+        c += v;
+        if (r < (int)rank) lower += v;
+      }
       csum[tid] = c;
     }
     __syncthreads();
     int above, cnt;
     const int digit = select_digit(csum, need, &above, &cnt);
+    const int tsel = 255 - digit;
+    gt_lower += sum256(tid < tsel ? lower : 0, red8[0]);
+    eq_lower = sum256(tid == tsel ? lower : 0, red8[1]);
     need -= above;
     prefix |= (uint32_t)digit << shift;
     mask |= dmask << shift;
@@ -551,6 +586,7 @@ topk_cluster_kernel(const float* __restrict__ scores, int64_t N, int k,
     lo = (prefix >> 31) ? lo_pos : lo_neg;
     if (cnt == need) break;
   }
+  cluster_arrive_relaxed();  // this CTA reads no peer any more
 
   // ordered write (see topk_reg_kernel), offset by the keys above / inside
   // the class held by the lower-ranked CTAs of the cluster
@@ -574,19 +610,6 @@ topk_cluster_kernel(const float* __restrict__ scores, int64_t N, int k,
   }
   int tot_packed;
   const int before = reg_block_scan((gt << 16) | eq, tot, &tot_packed);
-  if (tid == 0) {
-    pub_cnt[0] = tot_packed >> 16;
-    pub_cnt[1] = tot_packed & 0xFFFF;
-  }
-  cluster_barrier();
-  if (tid < 2 * CL) all_cnt[tid] = (int32_t)ld_peer(&pub_cnt[tid & 1], (uint32_t)(tid >> 1));
-  __syncthreads();
-  cluster_barrier();  // every peer has read this CTA's counts: its shared memory may go
-  int gt_lower = 0, eq_lower = 0;
-  for (int r = 0; r < (int)rank; ++r) {
-    gt_lower += all_cnt[2 * r];
-    eq_lower += all_cnt[2 * r + 1];
-  }
   const int eq_before = eq_lower + (before & 0xFFFF);
   int take = max(0, min(eq, need - eq_before));
   int off = gt_lower + (before >> 16) + min(eq_before, need);
@@ -604,6 +627,7 @@ topk_cluster_kernel(const float* __restrict__ scores, int64_t N, int k,
       ++off;
     }
   }
+  cluster_wait();  // the peers' last reads of this CTA's shared memory are done
 }
 
 template <bool kSmem>
