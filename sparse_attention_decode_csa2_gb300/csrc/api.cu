@@ -398,21 +398,20 @@ csa2_status csa2_layer_group(const csa2_layer* layers, int n_layers, const csa2_
         e = launch_topk(pscores, g->B, g->pool_size, g->k, nullptr, 1, nullptr, g->pool_out,
                         L.idx_out, stream, /*pdl=*/true);
       use = L.idx_out;
-    } else {  // REUSE
+    } else {  // REUSE: the attention kernel writes the copy of the reused indices
       use = latest;
-      if (L.idx_out)
-        e = cudaMemcpyAsync(L.idx_out, latest, (size_t)g->B * g->k * 4, cudaMemcpyDeviceToDevice,
-                            stream);
     }
     if (e != cudaSuccess) break;
     latest = use;
-    // After a top-k of this layer the attention starts early (programmatic
-    // dependent launch): it loads Q and sets up while the selection finishes.
+    // The attention starts early (programmatic dependent launch): it loads Q
+    // and sets up while the kernel before it (this layer's top-k, or the
+    // previous layer's merge) finishes.
     const SwaArgs swa{L.swa_kv, g->swa_ring, g->n_win, g->q_pos};
     const bool with_swa = g->n_win > 0 && L.swa_kv;
     e = launch_sparse_attn(L.q_bf16, g->kv_fp4, g->B, g->H, g->N, g->kv_seq_stride, g->q_per_seq,
                            use, g->k, g->softmax_scale, L.out, L.lse, wsb + w.attn, status,
-                           stream, /*pdl=*/L.mode != CSA2_REUSE, with_swa ? &swa : nullptr);
+                           stream, /*pdl=*/true, with_swa ? &swa : nullptr,
+                           L.mode == CSA2_REUSE ? L.idx_out : nullptr);
   }
   return check_launch(e);
 }

@@ -14,7 +14,8 @@ namespace {
 __global__ void __launch_bounds__(128)
 attn_combine_kernel(const float* __restrict__ part_o, const float* __restrict__ part_lse, int H,
                     int nsplit, float* __restrict__ out, float* __restrict__ lse) {
-  pdl_wait();  // the partials come from the attention kernel before
+  pdl_trigger();  // the next layer's attention may start its query prologue
+  pdl_wait();     // the partials come from the attention kernel before
   const int h = blockIdx.x, b = blockIdx.y;
   float M = -INFINITY;
   for (int s = 0; s < nsplit; ++s) M = fmaxf(M, part_lse[((int64_t)b * nsplit + s) * H + h]);
@@ -60,7 +61,8 @@ size_t partial_bytes(int B, int H, int nsplit) {
 cudaError_t launch_attn(const uint16_t* q_bf16, const uint8_t* kv_fp4, int B, int H, int64_t N,
                         int64_t kv_seq_stride, int q_per_seq, const int32_t* idx, int k,
                         float softmax_scale, float* out, float* lse, void* scratch,
-                        int32_t* status, cudaStream_t stream, bool pdl, const SwaArgs* swa) {
+                        int32_t* status, cudaStream_t stream, bool pdl, const SwaArgs* swa,
+                        int32_t* idx_copy) {
   const int nsplit = choose_splits(B, k);
   const int chunk = ((k + nsplit - 1) / nsplit + kSplitTile - 1) / kSplitTile * kSplitTile;
   float* part_o = nullptr;
@@ -72,7 +74,7 @@ cudaError_t launch_attn(const uint16_t* q_bf16, const uint8_t* kv_fp4, int B, in
   const float scale_log2 = softmax_scale * 1.4426950408889634f;
   cudaError_t e = launch_sparse_attn_tc(q_bf16, kv_fp4, B, H, N, kv_seq_stride, q_per_seq, idx, k,
                                         nsplit, chunk, scale_log2, out, lse, part_o, part_lse,
-                                        status, swa, stream, pdl);
+                                        status, swa, idx_copy, stream, pdl);
   if (e != cudaSuccess || nsplit == 1) return e;
   return launch_kernel(attn_combine_kernel, dim3((unsigned)H, (unsigned)B), dim3(128), 0, stream,
                        true, part_o, part_lse, H, nsplit, out, lse);
@@ -93,10 +95,11 @@ size_t attn_scratch_bytes(int B, int H, int k) {
 cudaError_t launch_sparse_attn(const uint16_t* q_bf16, const uint8_t* kv_fp4, int B, int H,
                                int64_t N, int64_t kv_seq_stride, int q_per_seq, const int32_t* idx,
                                int k, float softmax_scale, float* out, float* lse, void* scratch,
-                               int32_t* status, cudaStream_t stream, bool pdl, const SwaArgs* swa) {
+                               int32_t* status, cudaStream_t stream, bool pdl, const SwaArgs* swa,
+                               int32_t* idx_copy) {
   if (B == 0) return cudaSuccess;
   return launch_attn(q_bf16, kv_fp4, B, H, N, kv_seq_stride, q_per_seq, idx, k, softmax_scale, out,
-                     lse, scratch, status, stream, pdl, swa);
+                     lse, scratch, status, stream, pdl, swa, idx_copy);
 }
 
 }  // namespace csa2

@@ -113,7 +113,7 @@ sparse_attn_tc_kernel(const uint16_t* __restrict__ q_bf16, const uint8_t* __rest
                       float* __restrict__ out, float* __restrict__ lse, float* __restrict__ part_o,
                       float* __restrict__ part_lse, int32_t* status,
                       const uint8_t* __restrict__ swa_kv, int64_t swa_ring, int n_win,
-                      const int32_t* __restrict__ q_pos) {
+                      const int32_t* __restrict__ q_pos, int32_t* __restrict__ idx_copy) {
   using L = TcLayout;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_s = su32(smem_raw);
@@ -192,6 +192,10 @@ sparse_attn_tc_kernel(const uint16_t* __restrict__ q_bf16, const uint8_t* __rest
   if (tid < kHN) ctl.mref[tid] = -INFINITY;
   pdl_wait();
   for (int i = tid; i < min(cnt, kIdxCache); i += kThreadsTc) idx_s[i] = slots[i];
+  if (idx_copy) {  // the caller's copy of the slots this CTA reads
+    int32_t* dst = idx_copy + (int64_t)b * k + s0;
+    for (int i = tid; i < cnt; i += kThreadsTc) dst[i] = slots[i];
+  }
   proxy_fence();
   tc_fence_before();
   __syncthreads();
@@ -532,7 +536,8 @@ static cudaError_t launch_tc_t(const uint16_t* q_bf16, const uint8_t* kv_fp4, in
                                int64_t kv_seq_stride, int q_per_seq, const int32_t* idx, int k,
                                int nsplit, int chunk, float scale_log2, float* out, float* lse,
                                float* part_o, float* part_lse, int32_t* status,
-                               const SwaArgs* swa, cudaStream_t stream, bool pdl) {
+                               const SwaArgs* swa, int32_t* idx_copy, cudaStream_t stream,
+                               bool pdl) {
   using L = TcLayout;
   cudaError_t e = cudaFuncSetAttribute(sparse_attn_tc_kernel<H>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)L::alloc);
@@ -541,7 +546,7 @@ static cudaError_t launch_tc_t(const uint16_t* q_bf16, const uint8_t* kv_fp4, in
                        dim3(kThreadsTc), L::alloc, stream, pdl, q_bf16, kv_fp4, N, kv_seq_stride,
                        q_per_seq, idx, k, chunk, scale_log2, out, lse, part_o, part_lse, status,
                        swa ? swa->kv : nullptr, swa ? swa->ring : (int64_t)0, swa ? swa->n_win : 0,
-                       swa ? swa->q_pos : nullptr);
+                       swa ? swa->q_pos : nullptr, idx_copy);
 }
 
 cudaError_t launch_sparse_attn_tc(const uint16_t* q_bf16, const uint8_t* kv_fp4, int B, int H,
@@ -549,17 +554,20 @@ cudaError_t launch_sparse_attn_tc(const uint16_t* q_bf16, const uint8_t* kv_fp4,
                                   const int32_t* idx, int k, int nsplit, int chunk,
                                   float scale_log2, float* out, float* lse, float* part_o,
                                   float* part_lse, int32_t* status, const SwaArgs* swa,
-                                  cudaStream_t stream, bool pdl) {
+                                  int32_t* idx_copy, cudaStream_t stream, bool pdl) {
   switch (H) {
     case 16:
       return launch_tc_t<16>(q_bf16, kv_fp4, B, N, kv_seq_stride, q_per_seq, idx, k, nsplit,
-                             chunk, scale_log2, out, lse, part_o, part_lse, status, swa, stream, pdl);
+                             chunk, scale_log2, out, lse, part_o, part_lse, status, swa, idx_copy,
+                             stream, pdl);
     case 32:
       return launch_tc_t<32>(q_bf16, kv_fp4, B, N, kv_seq_stride, q_per_seq, idx, k, nsplit,
-                             chunk, scale_log2, out, lse, part_o, part_lse, status, swa, stream, pdl);
+                             chunk, scale_log2, out, lse, part_o, part_lse, status, swa, idx_copy,
+                             stream, pdl);
     default:
       return launch_tc_t<64>(q_bf16, kv_fp4, B, N, kv_seq_stride, q_per_seq, idx, k, nsplit,
-                             chunk, scale_log2, out, lse, part_o, part_lse, status, swa, stream, pdl);
+                             chunk, scale_log2, out, lse, part_o, part_lse, status, swa, idx_copy,
+                             stream, pdl);
   }
 }
 

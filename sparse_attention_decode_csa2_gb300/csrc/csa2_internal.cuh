@@ -182,14 +182,17 @@ struct SwaArgs {
 };
 
 // Sparse attention (+ the SWA window when swa is non-null).  scratch:
-// attn_scratch_bytes(B, H, k) bytes (split-k partials).
+// attn_scratch_bytes(B, H, k) bytes (split-k partials).  idx_copy non-null:
+// the kernel also writes the slots it reads to idx_copy [B][k].  Before
+// waiting on the previous kernel (programmatic dependent launch) the kernel
+// reads only q_bf16, so every launch of it may be a dependent one.
 size_t attn_scratch_bytes(int B, int H, int k);
 int attn_launches(int B, int k);  // kernels one call launches
 cudaError_t launch_sparse_attn(const uint16_t* q_bf16, const uint8_t* kv_fp4, int B, int H,
                                int64_t N, int64_t kv_seq_stride, int q_per_seq, const int32_t* idx,
                                int k, float softmax_scale, float* out, float* lse, void* scratch,
                                int32_t* status, cudaStream_t stream, bool pdl = false,
-                               const SwaArgs* swa = nullptr);
+                               const SwaArgs* swa = nullptr, int32_t* idx_copy = nullptr);
 
 // tcgen05 kernel of one sparse-attention call (partials when nsplit > 1).
 cudaError_t launch_sparse_attn_tc(const uint16_t* q_bf16, const uint8_t* kv_fp4, int B, int H,
@@ -197,7 +200,7 @@ cudaError_t launch_sparse_attn_tc(const uint16_t* q_bf16, const uint8_t* kv_fp4,
                                   const int32_t* idx, int k, int nsplit, int chunk,
                                   float scale_log2, float* out, float* lse, float* part_o,
                                   float* part_lse, int32_t* status, const SwaArgs* swa,
-                                  cudaStream_t stream, bool pdl);
+                                  int32_t* idx_copy, cudaStream_t stream, bool pdl);
 
 int device_sm_count();
 
