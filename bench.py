@@ -317,9 +317,12 @@ def run_gpu(args, rank, world, local):
             "q_pos": inp.q_pos.cpu().pin_memory(),
         }
         swa_rows = []
-        if w.n_win and w.q_per_seq == 1:
-            r = int(pos.max()) % w.swa_ring   # every sequence's newest token shares it here
-            swa_rows = [(t[:, r], t[:, r].cpu().pin_memory()) for t in inp.swa]
+        if w.n_win:
+            # ring rows of the step's tokens (one run of rows for every sequence here)
+            r_lo, r_hi = int(pos.min()) % w.swa_ring, int(pos.max()) % w.swa_ring
+            if r_hi - r_lo == int(pos.max() - pos.min()):
+                swa_rows = [(t[:, r_lo:r_hi + 1], t[:, r_lo:r_hi + 1].cpu().pin_memory())
+                            for t in inp.swa]
         host_out = [torch.empty_like(o, device="cpu").pin_memory() for o in lg.out]
         h2d = (host_in["kv_new"].numel() + host_in["ki_new"].numel()
                + host_in["q_pos"].numel() * 4

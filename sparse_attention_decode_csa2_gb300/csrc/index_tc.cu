@@ -5,9 +5,9 @@
 //                                         fp32 accumulate, M = 128 entries)
 //   score[q][e] = sum_h D[e][(q - q0) * H_I + h]
 // B holds the indexer heads of QG queries that share one context (QG = 1 for
-// decode: the heads padded to N = 16 or 32; QG = 16 for the prefill-shaped
-// case: N = 16 * H_I), so one pass over the K tile scores every head of every
-// query in the group.  FP8 products are exact; each head's 64-term sum and
+// decode: the heads padded to N = 16 or 32; up to QG = 16 for the prefill-shaped
+// case: N = QG * H_I <= 256), so one pass over the K tile scores every head of
+// every query in the group.  FP8 products are exact; each head's 64-term sum and
 // the head sum accumulate in fp32 (exact for integer-valued inputs).
 //
 // Work split: the (query group, 128-entry tile) items of the whole call are
@@ -363,10 +363,13 @@ cudaError_t launch_index_scores_tc(const uint8_t* q_fp8, const uint8_t* k_fp8, i
                                    int D_I, int64_t N, int64_t kv_seq_stride, int q_per_seq,
                                    const int32_t* q_pos, int ratio, float* scores,
                                    int32_t* status, cudaStream_t stream) {
-  int QG, NB;
-  if (q_per_seq >= 16 && q_per_seq % 16 == 0 && 16 * H_I <= 256 && (H_I % 4) == 0) {
-    QG = 16;
-    NB = 16 * H_I;  // multiple of 64
+  // queries sharing a context share each K tile: the largest group of
+  // QG <= 16 queries whose QG * H_I heads fit one MMA (N <= 256, a multiple of 16)
+  int QG = 0, NB = 0;
+  for (int qg = 16; qg >= 2 && QG == 0; qg >>= 1)
+    if (q_per_seq % qg == 0 && qg * H_I <= 256 && (qg * H_I) % 16 == 0) QG = qg;
+  if (QG > 0) {
+    NB = QG * H_I;
   } else if (H_I <= 32) {
     QG = 1;
     NB = H_I <= 16 ? 16 : 32;

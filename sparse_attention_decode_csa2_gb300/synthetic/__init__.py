@@ -333,8 +333,17 @@ DECODER20_MX = Workload("decoder20_mxfp4_b32_ctx64k", 9, B=32, N=65536, H=64, H_
                         k=512, ratio=1, seeds=tuple(_seeds(9000, 32)),
                         modes=(FULL, REUSE, REUSE, REUSE) + (REINDEX, REUSE, REUSE, REUSE) * 4,
                         pool=16384, pool_block=8, n_win=128, swa_ring=128, indexer_fmt=1)
+# The pages' production encoder: 18 CSA2 layers at m = 2 in three groups of six
+# (Full + 5 Reuse), indexer 32 heads x 128, top-k 512, SWA window 128; a chunk of
+# the last 512 prompt tokens of a 64K-token prompt (ring of 1024 SWA rows holds
+# every window the chunk reads).
+ENCODER18 = Workload("encoder18_chunk512_ctx64k", 10, B=512, N=32768, H=64, H_I=32, D_I=128,
+                     k=512, ratio=2, q_per_seq=512, seeds=(10000,), first_pos=65536 - 512,
+                     modes=(FULL,) + (REUSE,) * 5 + (FULL,) + (REUSE,) * 5 + (FULL,) + (REUSE,) * 5,
+                     n_win=128, swa_ring=1024)
 PREFILL_128K = Workload("prefill_4096q_ctx128k", 5, B=4096, N=32768, H=64, H_I=8, k=2048,
                         q_per_seq=4096, seeds=(5000,), first_pos=126976, float_indexer=True)
 
 WORKLOADS = {w.name: w for w in (TINY_FULL, DECODE_64K, GROUP_128K, HIER_1M, PREFILL_128K,
-                                  HIER_BLOCK_1M, DECODE_64K_SWA, DECODER20, DECODER20_MX)}
+                                  HIER_BLOCK_1M, DECODE_64K_SWA, DECODER20, DECODER20_MX,
+                                  ENCODER18)}

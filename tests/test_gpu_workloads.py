@@ -1,4 +1,4 @@
-"""Parity of the whole CSA2 path at the nine workloads' full sizes, in the
+"""Parity of the whole CSA2 path at the ten workloads' full sizes, in the
 launch configuration the benchmark times (csa2_layer_group over the
 device-resident cache).  The oracle recomputes sampled queries one by one:
 their FP4 rows (from the same seeded latent), indexer scores, top-k / pool
@@ -14,7 +14,8 @@ pytestmark = pytest.mark.gpu
 
 NAMES = ["tiny_full_1q_ctx4k", "decode_b32_ctx64k", "group_full_reindex_reuse_b64_ctx128k",
          "hier_pool8192_b16_ctx1m", "prefill_4096q_ctx128k", "hier_block2048x8_b16_ctx1m",
-         "decode_swa128_b32_ctx64k", "decoder20_prod_b32_ctx64k", "decoder20_mxfp4_b32_ctx64k"]
+         "decode_swa128_b32_ctx64k", "decoder20_prod_b32_ctx64k", "decoder20_mxfp4_b32_ctx64k",
+         "encoder18_chunk512_ctx64k"]
 
 
 def _sample(B, n):
@@ -38,7 +39,7 @@ def test_workload_parity(name):
     code, bits = csa2.read_status(lg.ws)
     assert code == 0, bits
     pos = w.q_pos()
-    n_samples = {1: 1, 2: 4, 3: 3, 4: 3, 5: 6, 6: 3, 7: 4, 8: 2, 9: 2}[w.workload_id]
+    n_samples = {1: 1, 2: 4, 3: 3, 4: 3, 5: 6, 6: 3, 7: 4, 8: 2, 9: 2, 10: 3}[w.workload_id]
     if w.indexer_fmt:
         def scores_of(qi, ki, qpos):
             return oracle.index_scores_mxfp4(qi, ki, w.D_I, w.N, 0, 1, qpos, w.ratio)
