@@ -432,7 +432,7 @@ topk_cluster_kernel(const float* __restrict__ scores, int64_t N, int k,
   __shared__ __align__(16) int32_t pub[2][256];  // this CTA's digit counts (descending digits)
   __shared__ uint32_t pub_bits[4];               // this CTA's OR / AND per sign
   __shared__ uint32_t all_bits[4 * CL];
-  __shared__ int32_t red8[2][8];
+  __shared__ int32_t red8[1][8];
   __shared__ int32_t tot[kRegWarps + 1];
   __shared__ uint32_t red[4][kRegWarps];
 
@@ -535,10 +535,10 @@ topk_cluster_kernel(const float* __restrict__ scores, int64_t N, int k,
     lo = min(cur_hi, cur_hi == 31 ? min(lo_pos, lo_neg) : ((kor >> 31) ? lo_pos : lo_neg));
   }
   int need = k;
-  // keys above the class / inside it held by the lower-ranked CTAs; with no
-  // pass (all keys equal) the class is every valid key
-  int gt_lower = 0;
-  int eq_lower = (int)min((int64_t)n, (int64_t)rank * (KPT * kRegThreads));
+  // this thread's share (digit 255 - tid) of the keys above the class / inside
+  // it held by the lower-ranked CTAs, summed over the block after the passes
+  int gt_part = 0, eq_part = 0;
+  bool any_pass = false;
   for (int pass = 0; cur_hi >= lo; ++pass) {
     const int nbits = min(8, cur_hi + 1 - lo);
     const int shift = cur_hi + 1 - nbits;
@@ -577,8 +577,9 @@ topk_cluster_kernel(const float* __restrict__ scores, int64_t N, int k,
     int above, cnt;
     const int digit = select_digit(csum, need, &above, &cnt);
     const int tsel = 255 - digit;
-    gt_lower += sum256(tid < tsel ? lower : 0, red8[0]);
-    eq_lower = sum256(tid == tsel ? lower : 0, red8[1]);
+    gt_part += tid < tsel ? lower : 0;
+    eq_part = tid == tsel ? lower : 0;
+    any_pass = true;
     need -= above;
     prefix |= (uint32_t)digit << shift;
     mask |= dmask << shift;
@@ -587,6 +588,13 @@ topk_cluster_kernel(const float* __restrict__ scores, int64_t N, int k,
     if (cnt == need) break;
   }
   cluster_arrive_relaxed();  // this CTA reads no peer any more
+  // both sums are below 2^15 (the lower ranks hold fewer than 32768 keys),
+  // so one packed reduction carries them; with no pass (all keys equal) the
+  // class is every valid key
+  const int packed = sum256((gt_part << 16) | eq_part, red8[0]);
+  const int gt_lower = packed >> 16;
+  const int eq_lower =
+      any_pass ? (packed & 0xFFFF) : (int)min((int64_t)n, (int64_t)rank * (KPT * kRegThreads));
 
   // ordered write (see topk_reg_kernel), offset by the keys above / inside
   // the class held by the lower-ranked CTAs of the cluster
