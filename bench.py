@@ -96,6 +96,12 @@ def allreduce_max(x: float, world: int) -> float:
     return float(t.item())
 
 
+def step_throughput(B: int, steps: int, world: int, total_s: float, n_layers: int) -> float:
+    """Whole-job query-tokens/s per layer: every rank runs `steps` steps of B queries
+    through n_layers layers; total_s is the slowest rank's time (max over ranks)."""
+    return B * steps * world * n_layers / total_s
+
+
 def measured_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -358,18 +364,14 @@ def run_gpu(args, rank, world, local):
         e1.record(cur)
         torch.cuda.synchronize()
         e2e_s = allreduce_max(e0.elapsed_time(e1) / 1e3, world)
-        e2e_v = w.B * Ke * world / e2e_s
-        if len(w.modes) > 1:
-            e2e_v *= len(w.modes)   # per layer, as `value`
+        e2e_v = step_throughput(w.B, Ke, world, e2e_s, len(w.modes))
         e2e = {"value": e2e_v, "unit": UNIT, "h2d_bytes_per_step": int(h2d),
                "d2h_bytes_per_step": int(d2h),
                "inputs": "queries, positions and the appended cache entries; cache resident"}
 
     total_s = allreduce_max(sum(step_ms) / 1e3, world)
     ms_per_step = total_s * 1e3 / K
-    value = w.B * K * world / total_s   # query tokens through one layer
-    if len(w.modes) > 1:
-        value = value * len(w.modes)    # per layer: every layer processes the batch
+    value = step_throughput(w.B, K, world, total_s, len(w.modes))
 
     hbm_peak, bf16_peak, peak_src = measured_peaks()
     step_bytes, _ = algorithmic_bytes(w)
