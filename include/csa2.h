@@ -32,7 +32,8 @@
  *    workspace.
  *  - Supported shapes on the GPU path: D = 512, D_I in {32, 64, 128},
  *    H in {16, 32, 64}, 1 <= H_I <= 32, 1 <= k <= 16384,
- *    N < 2^31.  Other shapes return CSA2_ERR_UNSUPPORTED.
+ *    N < 2^31; MXFP4 indexer rows: D_I = 128, 1 <= H_I <= 64.  Other shapes
+ *    return CSA2_ERR_UNSUPPORTED.
  */
 #ifndef CSA2_H_
 #define CSA2_H_
@@ -205,6 +206,9 @@ size_t csa2_block_pool_workspace_size(int B, int64_t N, int block, int n_blocks)
  *            CSA2_ERR_BAD_INDEX status and the row's result is unspecified
  *   idx      int32 [B][k] selected entry ids, ascending, -1 padded; ranking
  *            by (score desc, entry id asc).  Bit-exact given exact scores.
+ *   Scores: the head sum of the query (exact in fp32 for H_I <= 32) is split
+ *   into two f16 parts (22 significant bits: exact for integer inputs) and
+ *   dotted with the gathered rows on tensor cores in fp32.
  *   ws       at least csa2_workspace_size(B, N, k, 0, P) bytes.
  */
 csa2_status csa2_hier_pool_index(const uint8_t* q_fp8, const uint8_t* k_fp8, int B, int H_I,
