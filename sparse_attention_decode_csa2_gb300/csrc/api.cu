@@ -242,7 +242,7 @@ csa2_status csa2_hier_pool_index(const uint8_t* q_fp8, const uint8_t* k_fp8, int
   uint8_t* wsb = reinterpret_cast<uint8_t*>(ws);
   float* pscores = reinterpret_cast<float*>(wsb + w.pool_scores);
   cudaError_t e = launch_pool_scores(q_fp8, k_fp8, B, H_I, D_I, N, kv_seq_stride, q_per_seq, pool,
-                                     P, pscores, nullptr, status_ptr(ws), stream);
+                                     P, pscores, status_ptr(ws), stream);
   if (e != cudaSuccess) return CSA2_ERR_CUDA;
   return check_launch(
       launch_topk(pscores, B, P, k, nullptr, 1, nullptr, pool, idx, stream, /*pdl=*/true));
@@ -393,7 +393,7 @@ csa2_status csa2_layer_group(const csa2_layer* layers, int n_layers, const csa2_
                                         g->pool_size, pscores, status, stream)
              : launch_pool_scores(L.qi_fp8, g->ki_fp8, g->B, g->H_I, g->D_I, g->N,
                                   g->kv_seq_stride, g->q_per_seq, g->pool_out, g->pool_size,
-                                  pscores, nullptr, status, stream);
+                                  pscores, status, stream);
       if (e == cudaSuccess)
         e = launch_topk(pscores, g->B, g->pool_size, g->k, nullptr, 1, nullptr, g->pool_out,
                         L.idx_out, stream, /*pdl=*/true);

@@ -124,13 +124,12 @@ cudaError_t launch_index_scores_tc(const uint8_t* q_fp8, const uint8_t* k_fp8, i
                                    const int32_t* q_pos, int ratio, float* scores,
                                    int32_t* status, cudaStream_t stream);
 
-// Scores pool entries: pool_scores[b][p] for valid pool[b][p], -inf for -1 padding;
-// n_valid[b] = number of valid leading entries.  Flags a pool that is not strictly
-// ascending with -1 only at the tail.
+// Scores pool entries: pool_scores[b][p] for valid pool[b][p], -inf for -1 padding.
+// Flags a pool that is not strictly ascending with -1 only at the tail.
 cudaError_t launch_pool_scores(const uint8_t* q_fp8, const uint8_t* k_fp8, int B, int H_I,
                                int D_I, int64_t N, int64_t kv_seq_stride, int q_per_seq,
-                               const int32_t* pool, int P, float* pool_scores, int32_t* n_valid,
-                               int32_t* status, cudaStream_t stream);
+                               const int32_t* pool, int P, float* pool_scores, int32_t* status,
+                               cudaStream_t stream);
 
 // MXFP4 indexer (rows of D_I = 128: 64 code bytes + 4 E8M0 scale bytes).
 cudaError_t launch_quantize_mxfp4(const float* x, int64_t n_rows, int d, uint8_t* out,

@@ -159,9 +159,8 @@ cudaError_t launch_index_scores(const uint8_t* q_fp8, const uint8_t* k_fp8, int 
 
 cudaError_t launch_pool_scores(const uint8_t* q_fp8, const uint8_t* k_fp8, int B, int H_I,
                                int D_I, int64_t N, int64_t kv_seq_stride, int q_per_seq,
-                               const int32_t* pool, int P, float* pool_scores, int32_t* n_valid,
-                               int32_t* status, cudaStream_t stream) {
-  (void)n_valid;
+                               const int32_t* pool, int P, float* pool_scores, int32_t* status,
+                               cudaStream_t stream) {
   if (B == 0 || P == 0) return cudaSuccess;
   dim3 grid((unsigned)((P + 1023) / 1024), (unsigned)B);
   switch (D_I) {
