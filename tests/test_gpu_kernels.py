@@ -385,6 +385,24 @@ def test_layer_group_matches_oracle(C, modes, pool):
         assert (gpool.cpu().numpy() == r_pool).all()
 
 
+def test_layer_group_with_one_split_per_query_matches_oracle(C):
+    # B >= the SM count: every query's attention is one CTA (no merge kernel), so a Reuse
+    # layer follows another attention directly and writes its index copy itself
+    rng = np.random.default_rng(160)
+    B, N, H, H_I, k = 160, 600, 16, 8, 64
+    modes = (0, 2, 2, 1, 2)
+    kv, ki, qs, qis, pos = _group(rng, B, N, H, H_I, k, modes, 0)
+    outs, lses, idxs, _ = C.layer_group(modes, [cuda(q, torch.int16) for q in qs],
+                                        [None if qi is None else cuda(qi) for qi in qis],
+                                        cuda(kv), cuda(ki), N, N, 1, cuda(pos), 4, k, 0, SCALE)
+    r_outs, r_lses, r_idxs, _ = oracle.layer_group(modes, qs, qis, kv, ki, N, N, 1, pos, 4, k,
+                                                   0, SCALE)
+    for l in range(len(modes)):
+        assert (idxs[l].cpu().numpy() == r_idxs[l]).all(), l
+        assert_attn_close(outs[l].cpu().numpy(), r_outs[l], l)
+        assert_lse_close(lses[l].cpu().numpy(), r_lses[l])
+
+
 def test_layer_group_rejects_bad_schedules(C):
     rng = np.random.default_rng(0)
     B, N, H, k = 2, 500, 64, 64

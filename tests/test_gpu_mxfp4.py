@@ -177,23 +177,31 @@ def test_hier_pool_index_mxfp4_float_rows_follow_the_selection_rule(C):
         assert_float_selection_ok(got[b], ref[b], s1[b], b)
 
 
-@pytest.mark.parametrize("modes,pool,pool_block", [((0, 2, 1, 2), 0, 0), ((0, 1, 2, 1), 1024, 0),
-                                                   ((0, 2, 1, 1), 1024, 8)])
-def test_layer_group_with_mxfp4_indexer_matches_oracle(C, modes, pool, pool_block):
-    rng = np.random.default_rng(len(modes) + pool + pool_block)
+@pytest.mark.parametrize("modes,pool,pool_block,n_win", [((0, 2, 1, 2), 0, 0, 0),
+                                                         ((0, 1, 2, 1), 1024, 0, 0),
+                                                         ((0, 2, 1, 1), 1024, 8, 0),
+                                                         ((0, 2, 1, 2), 512, 8, 128)])
+def test_layer_group_with_mxfp4_indexer_matches_oracle(C, modes, pool, pool_block, n_win):
+    rng = np.random.default_rng(len(modes) + pool + pool_block + n_win)
     B, N, H, H_I, k = 3, 4000, 64, 32, 256
     kv = oracle.quantize_kv_fp4(rng.standard_normal((B * N, 512)).astype(np.float32))
     ki = _mx_int(rng, (B * N, D_I))
     qs = [bf16_bits(rng.standard_normal((B, H, 512))) for _ in modes]
     qis = [None if m == 2 else _mx_int(rng, (B, H_I, D_I)) for m in modes]
     pos = rng.integers(4 * k, N + 3, B).astype(np.int32)
+    ring = 256
+    swa = None
+    if n_win:  # each layer's SWA ring: E4M3 rows of N(0,1) latents
+        swa = [torch.from_numpy(rng.standard_normal((B, ring, 512)).astype(np.float32))
+               .to(torch.float8_e4m3fn).view(torch.uint8).numpy() for _ in modes]
     outs, lses, idxs, gpool = C.layer_group(
         modes, [cuda(q, torch.int16) for q in qs], [None if qi is None else cuda(qi) for qi in qis],
         cuda(kv), cuda(ki), N, N, 1, cuda(pos), 1, k, pool, SCALE, pool_block=pool_block,
+        swa_kv=None if swa is None else [cuda(x) for x in swa], n_win=n_win,
         indexer_fmt=C.INDEXER_MXFP4)
     r_outs, r_lses, r_idxs, r_pool = oracle.layer_group(
         modes, qs, qis, kv, ki, N, N, 1, pos, 1, k, pool, SCALE, pool_block=pool_block,
-        indexer_fmt=1, D_I=D_I)
+        swa_kv=swa, swa_ring=ring if n_win else 0, n_win=n_win, indexer_fmt=1, D_I=D_I)
     for l in range(len(modes)):
         assert (idxs[l].cpu().numpy() == r_idxs[l]).all(), l
         assert_attn_close(outs[l].cpu().numpy(), r_outs[l], l)
