@@ -872,12 +872,14 @@ cudaError_t launch_cluster(int B, const float* scores, int64_t N, int k, const i
 
 // Rows of <= 32768 candidates when one CTA per row leaves most SMs idle: a
 // cluster of 8 (B <= SMs / 8) or 4 (B <= SMs / 4) CTAs per row, each holding
-// at least 4 keys per thread.  Returns false when the shape does not qualify.
+// at least 4 keys per thread.  Shorter rows stay on one CTA: below 2048 keys
+// per CTA the cluster barriers cost more than the split saves.  Returns false
+// when the shape does not qualify.
 bool cluster_launch(int B, const float* scores, int64_t N, int k, const int32_t* q_pos,
                     int ratio, const int32_t* n_valid, const int32_t* map, int32_t* idx,
                     cudaStream_t stream, bool pdl, cudaError_t* err) {
   const int sms = device_sm_count();
-  const int CL = (B * 8 <= sms) ? 8 : ((B * 4 <= sms) ? 4 : 0);
+  int CL = (B * 8 <= sms && N >= 8 * 2048) ? 8 : ((B * 4 <= sms && N >= 4 * 2048) ? 4 : 0);
   if (CL == 0 || N > kRegMaxKeys) return false;
   const int64_t per = (N + CL - 1) / CL;  // keys per CTA
   const int kpt = per <= 4 * kRegThreads ? 4 : (per <= 8 * kRegThreads ? 8 : 16);
