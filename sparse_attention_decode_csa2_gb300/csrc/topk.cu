@@ -9,8 +9,8 @@
 // and the first `need` members of the class, in ascending position.
 //
 // Rows of up to 32768 candidates (topk_reg_kernel, one 512-thread CTA per
-// row; topk_cluster_kernel, a cluster of 4 or 8 such CTAs per row when the
-// batch alone would leave most SMs idle): each thread holds KPT consecutive
+// row; topk_cluster_kernel, a cluster of 2, 4 or 8 such CTAs per row when the
+// batch alone would leave SMs idle): each thread holds KPT consecutive
 // keys in registers.  The radix
 // passes take 8-bit digits from the highest bit where the row's min and max
 // keys differ down to the lowest bit that differs between two keys of the
@@ -870,29 +870,41 @@ cudaError_t launch_cluster(int B, const float* scores, int64_t N, int k, const i
                             n_valid, map, idx);
 }
 
-// Rows of <= 32768 candidates when one CTA per row leaves most SMs idle: a
-// cluster of 8 (B <= SMs / 8) or 4 (B <= SMs / 4) CTAs per row, each holding
-// at least 4 keys per thread.  Shorter rows stay on one CTA: below 2048 keys
-// per CTA the cluster barriers cost more than the split saves.  Returns false
+template <int CL>
+cudaError_t launch_cluster_kpt(int kpt, int B, const float* scores, int64_t N, int k,
+                               const int32_t* q_pos, int ratio, const int32_t* n_valid,
+                               const int32_t* map, int32_t* idx, cudaStream_t stream, bool pdl) {
+  switch (kpt) {
+    case 4: return launch_cluster<4, CL>(B, scores, N, k, q_pos, ratio, n_valid, map, idx, stream, pdl);
+    case 8: return launch_cluster<8, CL>(B, scores, N, k, q_pos, ratio, n_valid, map, idx, stream, pdl);
+    case 16: return launch_cluster<16, CL>(B, scores, N, k, q_pos, ratio, n_valid, map, idx, stream, pdl);
+    default: return launch_cluster<32, CL>(B, scores, N, k, q_pos, ratio, n_valid, map, idx, stream, pdl);
+  }
+}
+
+// Rows of <= 32768 candidates when one CTA per row leaves SMs idle: a cluster
+// of 8 (B <= SMs / 8), 4 (B <= SMs / 4) or 2 (B <= SMs / 2) CTAs per row.
+// Rows too short to give every CTA 2048 keys use fewer CTAs (or one): below
+// that the cluster barriers cost more than the split saves.  Returns false
 // when the shape does not qualify.
 bool cluster_launch(int B, const float* scores, int64_t N, int k, const int32_t* q_pos,
                     int ratio, const int32_t* n_valid, const int32_t* map, int32_t* idx,
                     cudaStream_t stream, bool pdl, cudaError_t* err) {
   const int sms = device_sm_count();
-  int CL = (B * 8 <= sms && N >= 8 * 2048) ? 8 : ((B * 4 <= sms && N >= 4 * 2048) ? 4 : 0);
+  int CL = 0;
+  for (int c = 8; c >= 2 && CL == 0; c >>= 1)
+    if (B * c <= sms && N >= (int64_t)c * 2048) CL = c;
   if (CL == 0 || N > kRegMaxKeys) return false;
   const int64_t per = (N + CL - 1) / CL;  // keys per CTA
-  const int kpt = per <= 4 * kRegThreads ? 4 : (per <= 8 * kRegThreads ? 8 : 16);
-  if ((int64_t)kpt * kRegThreads * CL < N) return false;
-  if (CL == 8) {
-    *err = kpt == 4 ? launch_cluster<4, 8>(B, scores, N, k, q_pos, ratio, n_valid, map, idx, stream, pdl)
-         : kpt == 8 ? launch_cluster<8, 8>(B, scores, N, k, q_pos, ratio, n_valid, map, idx, stream, pdl)
-                    : launch_cluster<16, 8>(B, scores, N, k, q_pos, ratio, n_valid, map, idx, stream, pdl);
-  } else {
-    *err = kpt == 4 ? launch_cluster<4, 4>(B, scores, N, k, q_pos, ratio, n_valid, map, idx, stream, pdl)
-         : kpt == 8 ? launch_cluster<8, 4>(B, scores, N, k, q_pos, ratio, n_valid, map, idx, stream, pdl)
-                    : launch_cluster<16, 4>(B, scores, N, k, q_pos, ratio, n_valid, map, idx, stream, pdl);
-  }
+  int kpt = 4;
+  while ((int64_t)kpt * kRegThreads < per) kpt *= 2;
+  if (kpt > 32) return false;
+  *err = CL == 8 ? launch_cluster_kpt<8>(kpt, B, scores, N, k, q_pos, ratio, n_valid, map, idx,
+                                          stream, pdl)
+       : CL == 4 ? launch_cluster_kpt<4>(kpt, B, scores, N, k, q_pos, ratio, n_valid, map, idx,
+                                          stream, pdl)
+                 : launch_cluster_kpt<2>(kpt, B, scores, N, k, q_pos, ratio, n_valid, map, idx,
+                                          stream, pdl);
   return true;
 }
 
@@ -986,6 +998,8 @@ cudaError_t launch_topk(const float* scores, int B, int64_t N, int k, const int3
       M = (int64_t)C * k;
     }
     // the packed ids serve as the map: the selected candidates' entry ids
+    if (cluster_launch(B, cur_score, M, k, nullptr, 1, nullptr, cur_id, idx, stream, true, &e))
+      return e;
     return launch_reg_any(dim3((unsigned)B), cur_score, M, M, k, nullptr, 1, nullptr, cur_id, idx,
                           0, stream, true);
   }

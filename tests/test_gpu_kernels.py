@@ -125,12 +125,15 @@ def test_index_scores_float_inputs_within_fp32_rounding(C, q_per_seq):
     (2, 2048, 2048, "normal"), (2, 1000, 128, "equal"), (2, 70000, 100, "signed_zero"),
     (16, 8192, 2048, "ties"), (2, 262144, 8192, "ties"), (3, 300001, 2048, "normal"),
     (2, 262144, 16384, "ties"), (2, 1 << 21, 2048, "ties"),
-    # dispatch boundaries: clusters of 8 (B <= 19, N >= 16384) and 4 (B <= 38, N >= 8192)
-    # CTAs per row, one CTA per row from B = 39 on or for shorter rows; a row length that is
-    # no multiple of 4
+    # dispatch boundaries: clusters of 8 (B <= 19, N >= 16384), 4 (B <= 38, N >= 8192) and
+    # 2 (B <= 76, N >= 4096) CTAs per row, one CTA per row beyond or for shorter rows; a row
+    # length that is no multiple of 4
     (19, 32768, 2048, "ties"), (38, 20001, 1000, "normal"), (40, 5000, 300, "ties"),
     (2, 32768, 16384, "ties"), (7, 32767, 4095, "equal"), (4, 8192, 700, "normal"),
-    (4, 16383, 2048, "ties")])
+    (4, 16383, 2048, "ties"),
+    # clusters of 2 (39 <= B <= 76), and the last level of a long row on a cluster
+    (64, 32768, 2048, "ties"), (76, 4096, 100, "normal"), (50, 20001, 3000, "normal"),
+    (16, 262144, 2048, "ties")])
 def test_topk_bit_exact(C, B, N, k, kind):
     rng = np.random.default_rng(N + k)
     if kind == "ties":
