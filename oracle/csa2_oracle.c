@@ -29,7 +29,7 @@
  *  [P4f] same page, 1.(5).4: the indexer query and key are FP4 in the OCP
  *        MXFP4 format.
  *
- * Readings where the pages are silent (each is also listed in the design doc):
+ * Readings where the pages are silent:
  *  R1  scale byte = E4M3(absmax/6) rounded to nearest even, saturating at 448;
  *      code = E2M1 value nearest to the exact quotient |x|/scale, ties to the
  *      even code; sign bit = sign bit of x; scale 0 gives magnitude code 0.
