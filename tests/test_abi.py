@@ -65,3 +65,70 @@ def test_binding_refuses_cpu_tensors(libpath):
     from sparse_attention_decode_csa2_gb300 import csa2
     with pytest.raises(ValueError):
         csa2.quantize_kv_fp4(torch.zeros(4, 512))
+
+
+def test_mxfp4_argument_validation_before_any_device_work(libpath):
+    from sparse_attention_decode_csa2_gb300 import csa2
+    lib = csa2.lib
+    # quantiser: null pointers, d not a multiple of 32, d too wide
+    assert lib.csa2_quantize_mxfp4(None, 4, 128, None, None) == 1
+    assert lib.csa2_quantize_mxfp4(16, 4, 48, 16, None) == 1
+    assert lib.csa2_quantize_mxfp4(16, 4, 8192, 16, None) == 1
+    assert lib.csa2_quantize_mxfp4(8, 4, 128, 16, None) == 1          # x not 16-byte aligned
+    # scorer: (q, k, B, H_I, D_I, N, stride, q_per_seq, q_pos, ratio, scores, stream)
+    args = lambda **kw: [kw.get("q", 64), kw.get("k", 64), kw.get("B", 4), kw.get("H_I", 32),
+                         kw.get("D_I", 128), kw.get("N", 100), kw.get("stride", 100),
+                         kw.get("qps", 1), None, kw.get("ratio", 1), kw.get("scores", 64), None]
+    assert lib.csa2_index_scores_mxfp4(*args(q=None)) == 1             # null query
+    assert lib.csa2_index_scores_mxfp4(*args(D_I=64)) == 2             # only D_I = 128
+    assert lib.csa2_index_scores_mxfp4(*args(H_I=65)) == 2             # H_I <= 64
+    assert lib.csa2_index_scores_mxfp4(*args(stride=102)) == 2         # 68 * stride % 16 != 0
+    assert lib.csa2_index_scores_mxfp4(*args(k=72)) == 1               # K not 16-byte aligned
+    assert lib.csa2_index_scores_mxfp4(*args(stride=50)) == 1          # stride < N
+    assert lib.csa2_index_scores_mxfp4(*args(ratio=0)) == 1
+    assert lib.csa2_index_scores_mxfp4(*args(scores=None)) == 1
+    # pool re-index: P < 1, k < 1
+    pargs = [64, 64, 4, 32, 128, 100, 100, 1, 64, 0, 8, 64, 64, 1 << 20, None]
+    assert lib.csa2_hier_pool_index_mxfp4(*pargs) == 1
+
+
+def _group(csa2, modes, B=32, N=16384, k=2048, pool=0, pool_block=0, fmt=0):
+    L = len(modes)
+    layers = (csa2.Csa2Layer * L)()
+    for l, m in enumerate(modes):
+        layers[l] = csa2.Csa2Layer(m, 64, None if m == 2 else 64, 64, 64, 64, None)
+    g = csa2.Csa2GroupArgs(64, 64, B, 64, 8, 512, 64, N, N, 1, None, 4, k, pool, 64 if pool else None,
+                           1.0 / 512 ** 0.5, pool_block, 0, 0, fmt)
+    return layers, g
+
+
+def test_layer_group_launch_counts(libpath):
+    import ctypes
+    from sparse_attention_decode_csa2_gb300 import csa2
+    count = lambda layers, g: csa2.lib.csa2_layer_group_launches(layers, len(layers),
+                                                                  ctypes.byref(g))
+    # without a device the SM count defaults to 148: 4 splits of 512 slots for 32 queries,
+    # so every attention is a kernel plus its merge
+    layers, g = _group(csa2, [0])
+    assert count(layers, g) == 1 + 1 + 2                  # indexer, top-k, attention + merge
+    layers, g = _group(csa2, [0, 2, 1, 2])
+    assert count(layers, g) == 4 + 2 + (2 + 2) + 2        # Reindex: scores + top-k
+    layers, g = _group(csa2, [0, 1], pool=8192)
+    assert count(layers, g) == (1 + 1 + 1 + 2) + (2 + 2)  # Full also selects the pool
+    layers, g = _group(csa2, [0, 1], pool=16384, pool_block=8)
+    assert count(layers, g) == (1 + 3 + 1 + 2) + (2 + 2)  # blockwise pool: three kernels
+    layers, g = _group(csa2, [2, 0])                      # no Full layer first
+    assert count(layers, g) == -1
+    layers, g = _group(csa2, [0], B=0)
+    assert count(layers, g) == 0
+
+
+def test_workspace_sizes_grow_with_the_problem(libpath):
+    from sparse_attention_decode_csa2_gb300 import csa2
+    ws = csa2.lib.csa2_workspace_size
+    base = ws(32, 16384, 2048, 64, 0)
+    assert base >= 256 + 32 * 16384 * 4                    # status word + scores
+    assert ws(32, 16384, 2048, 64, 16384) > base           # pool scores and pool scratch
+    assert ws(64, 16384, 2048, 64, 0) > base
+    assert ws(0, 0, 0, 0, 0) == 256                        # the status word alone
+    assert csa2.lib.csa2_block_pool_workspace_size(16, 262144, 8, 2048) > 0
