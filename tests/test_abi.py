@@ -132,3 +132,19 @@ def test_workspace_sizes_grow_with_the_problem(libpath):
     assert ws(64, 16384, 2048, 64, 0) > base
     assert ws(0, 0, 0, 0, 0) == 256                        # the status word alone
     assert csa2.lib.csa2_block_pool_workspace_size(16, 262144, 8, 2048) > 0
+
+
+def test_empty_batches_and_contexts_return_ok_without_device_work(libpath):
+    from sparse_attention_decode_csa2_gb300 import csa2
+    lib = csa2.lib
+    # B = 0: nothing to score, no pointer needed
+    assert lib.csa2_index_scores_mxfp4(None, None, 0, 32, 128, 100, 100, 1, None, 1, None,
+                                       None) == 0
+    assert lib.csa2_index_scores(None, None, 0, 8, 64, 100, 100, 1, None, 1, None, None) == 0
+    # N = 0: an empty context
+    assert lib.csa2_index_scores_mxfp4(64, 64, 4, 32, 128, 0, 0, 1, None, 1, 64, None) == 0
+    # top-k of an empty batch still needs the status word
+    assert lib.csa2_topk(None, 0, 100, 8, None, 1, None, None, 0, None) == 3
+    assert lib.csa2_topk(None, 0, 100, 8, None, 1, None, 64, 256, None) == 0
+    assert lib.csa2_quantize_mxfp4(None, 0, 128, None, None) == 0   # empty: a no-op
+    assert lib.csa2_quantize_kv_fp4(None, 0, 512, None, None) == 0
