@@ -216,7 +216,10 @@ def _attn_case(rng, B, H, N, k, pad=0, dup=False, q_per_seq=1):
 @pytest.mark.parametrize("B,H,N,k,pad,dup", [
     (2, 64, 3000, 2048, 0, False), (3, 64, 900, 333, 40, True), (1, 16, 1024, 128, 0, False),
     (5, 32, 600, 257, 3, False), (4, 64, 70, 1, 0, False), (2, 16, 5000, 4096, 100, False),
-    (40, 64, 2200, 2048, 0, False)])
+    (40, 64, 2200, 2048, 0, False),
+    # a query's slots split over 4, 8 and 2 CTAs, then merged
+    (32, 64, 3000, 2048, 0, False), (16, 16, 3000, 2048, 7, False),
+    (64, 32, 1500, 1024, 0, False)])
 def test_attention_matches_oracle(C, B, H, N, k, pad, dup):
     rng = np.random.default_rng(B * 7 + H + k)
     kv, q, idx = _attn_case(rng, B, H, N, k, pad, dup)
