@@ -307,7 +307,10 @@ def run_gpu(args, rank, world, local):
     # append (the entries holding the queries' positions, and each layer's SWA
     # ring row of the newest token).  Those are copied from pinned host memory
     # into the resident buffers every step, then the layer group runs and every
-    # layer's output is copied back.
+    # layer's output is copied back.  The step is timed twice: issued call by
+    # call, and as a serving loop runs it, one CUDA graph per step that holds
+    # the copies in, the layer group and the copies out (the graph's copy nodes
+    # read and write the pinned host buffers on every replay).
     e2e = None
     if not args.no_e2e:
         S, N = w.n_seq, w.N
@@ -356,18 +359,38 @@ def run_gpu(args, rank, world, local):
             e2e_step()
         torch.cuda.synchronize()
         Ke = max(3, min(K, 10))
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        barrier(world)
-        e0.record(cur)
-        for _ in range(Ke):
-            e2e_step()
-        e1.record(cur)
-        torch.cuda.synchronize()
-        e2e_s = allreduce_max(e0.elapsed_time(e1) / 1e3, world)
-        e2e_v = step_throughput(w.B, Ke, world, e2e_s, len(w.modes))
-        e2e = {"value": e2e_v, "unit": UNIT, "h2d_bytes_per_step": int(h2d),
-               "d2h_bytes_per_step": int(d2h),
-               "inputs": "queries, positions and the appended cache entries; cache resident"}
+
+        def timed(step):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            barrier(world)
+            e0.record(cur)
+            for _ in range(Ke):
+                step()
+            e1.record(cur)
+            torch.cuda.synchronize()
+            return allreduce_max(e0.elapsed_time(e1) / 1e3, world)
+
+        eager_s = timed(e2e_step)
+        eager_v = step_throughput(w.B, Ke, world, eager_s, len(w.modes))
+        e2e = {"value": eager_v, "unit": UNIT, "h2d_bytes_per_step": int(h2d),
+               "d2h_bytes_per_step": int(d2h), "eager_value": eager_v,
+               "inputs": "queries, positions and the appended cache entries; cache resident",
+               "issue": "call by call"}
+        try:
+            g_e2e = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g_e2e, stream=stream):
+                e2e_step()
+            torch.cuda.synchronize()
+            for _ in range(max(1, min(W, 3))):
+                g_e2e.replay()
+            torch.cuda.synchronize()
+            graph_s = timed(g_e2e.replay)
+            e2e["value"] = step_throughput(w.B, Ke, world, graph_s, len(w.modes))
+            e2e["issue"] = ("one CUDA graph per step: copies in, layer group, copies out "
+                            "(eager_value: the same step issued call by call)")
+        except RuntimeError as ex:  # keep the call-by-call number, say why
+            torch.cuda.synchronize()
+            e2e["issue"] = f"call by call (graph capture failed: {str(ex).splitlines()[0]})"
 
     total_s = allreduce_max(sum(step_ms) / 1e3, world)
     ms_per_step = total_s * 1e3 / K
