@@ -145,10 +145,10 @@ csa2_status csa2_workspace_init(void* ws, size_t ws_bytes, cudaStream_t stream) 
 csa2_status csa2_read_status(void* ws, cudaStream_t stream, int32_t* device_bits) {
   if (!ws) return CSA2_ERR_WORKSPACE;
   int32_t bits = 0;
-  if (cudaMemcpyAsync(&bits, ws, 4, cudaMemcpyDeviceToHost, stream) != cudaSuccess)
-    return CSA2_ERR_CUDA;
-  if (cudaMemsetAsync(ws, 0, 4, stream) != cudaSuccess) return CSA2_ERR_CUDA;
-  if (cudaStreamSynchronize(stream) != cudaSuccess) return CSA2_ERR_CUDA;
+  csa2_status s = check_launch(cudaMemcpyAsync(&bits, ws, 4, cudaMemcpyDeviceToHost, stream));
+  if (s == CSA2_OK) s = check_launch(cudaMemsetAsync(ws, 0, 4, stream));
+  if (s == CSA2_OK) s = check_launch(cudaStreamSynchronize(stream));
+  if (s != CSA2_OK) return s;
   if (device_bits) *device_bits = bits;
   if (bits & kStatusBadIndex) return CSA2_ERR_BAD_INDEX;
   if (bits & kStatusTimeout) return CSA2_ERR_TIMEOUT;
@@ -243,7 +243,7 @@ csa2_status csa2_hier_pool_index(const uint8_t* q_fp8, const uint8_t* k_fp8, int
   float* pscores = reinterpret_cast<float*>(wsb + w.pool_scores);
   cudaError_t e = launch_pool_scores(q_fp8, k_fp8, B, H_I, D_I, N, kv_seq_stride, q_per_seq, pool,
                                      P, pscores, status_ptr(ws), stream);
-  if (e != cudaSuccess) return CSA2_ERR_CUDA;
+  if (e != cudaSuccess) return check_launch(e);
   return check_launch(
       launch_topk(pscores, B, P, k, nullptr, 1, nullptr, pool, idx, stream, /*pdl=*/true));
 }

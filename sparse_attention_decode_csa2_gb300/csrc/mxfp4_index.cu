@@ -561,13 +561,10 @@ cudaError_t launch_index_scores_mxfp4(const uint8_t* q_mx, const uint8_t* k_mx, 
                                       int32_t* status, cudaStream_t stream) {
   if (B == 0 || N == 0) return cudaSuccess;
   const size_t smem = sizeof(ScanSmem);
-  static bool attr_set = false;  // per process; the attribute is per kernel
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(mx_scores_kernel,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
+  // set on every call: the attribute belongs to the current device's context
+  cudaError_t e = cudaFuncSetAttribute(mx_scores_kernel,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
   const int S = (B + q_per_seq - 1) / q_per_seq;
   const int64_t total = (int64_t)S * ((N + kTileRows - 1) / kTileRows);
   int dev = 0, smem_sm = 0;
@@ -588,13 +585,10 @@ cudaError_t launch_pool_scores_mxfp4(const uint8_t* q_mx, const uint8_t* k_mx, i
                                      int32_t* status, cudaStream_t stream) {
   if (B == 0 || P == 0) return cudaSuccess;
   const size_t smem = sizeof(PoolSmem);
-  static bool attr_set = false;  // per process; the attribute is per kernel
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(mx_pool_scores_kernel,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
+  // set on every call: the attribute belongs to the current device's context
+  cudaError_t e = cudaFuncSetAttribute(mx_pool_scores_kernel,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
   dim3 grid((unsigned)((P + kPoolSlots - 1) / kPoolSlots), (unsigned)B);
   return launch_kernel(mx_pool_scores_kernel, grid, dim3(kPoolThreads), smem, stream, false, q_mx,
                        k_mx, H_I, N, kv_seq_stride, q_per_seq, pool, P, pool_scores, status);
