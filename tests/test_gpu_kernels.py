@@ -219,7 +219,10 @@ def _attn_case(rng, B, H, N, k, pad=0, dup=False, q_per_seq=1):
     (40, 64, 2200, 2048, 0, False),
     # a query's slots split over 4, 8 and 2 CTAs, then merged
     (32, 64, 3000, 2048, 0, False), (16, 16, 3000, 2048, 7, False),
-    (64, 32, 1500, 1024, 0, False)])
+    (64, 32, 1500, 1024, 0, False),
+    # one CTA per query (B above the SM count) over more slots than the kernel keeps in
+    # shared memory: slots past the first 2048 are read from global memory
+    (153, 16, 3000, 2500, 3, False)])
 def test_attention_matches_oracle(C, B, H, N, k, pad, dup):
     rng = np.random.default_rng(B * 7 + H + k)
     kv, q, idx = _attn_case(rng, B, H, N, k, pad, dup)
