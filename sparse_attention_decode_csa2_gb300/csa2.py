@@ -138,6 +138,17 @@ def _dev(t: torch.Tensor, dtype, name: str) -> torch.Tensor:
     return t
 
 
+def _out(t: torch.Tensor, shape, dtype, name: str) -> torch.Tensor:
+    """A caller-supplied output: the library writes exactly `shape` elements
+    through its pointer, so a tensor of another shape is refused before any
+    launch (it would be written out of bounds or only in part)."""
+    if not isinstance(t, torch.Tensor):
+        raise ValueError(f"{name} must be a tensor")
+    if tuple(t.shape) != tuple(int(x) for x in shape):
+        raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
+    return _dev(t, dtype, name)
+
+
 def _bits16(t: torch.Tensor, name: str) -> torch.Tensor:
     """bf16 tensor (or its int16/uint16 bit view) -> same storage as int16."""
     if t.dtype == torch.bfloat16:
@@ -184,7 +195,7 @@ def quantize_kv_fp4(x: torch.Tensor, out: Optional[torch.Tensor] = None) -> torc
     n, d = x.reshape(-1, x.shape[-1]).shape
     if out is None:
         out = torch.empty((n, d // 2 + d // 16), dtype=torch.uint8, device=x.device)
-    _dev(out, torch.uint8, "out")
+    _out(out, (n, d // 2 + d // 16), torch.uint8, "out")
     _check(lib.csa2_quantize_kv_fp4(_ptr(x), n, d, _ptr(out), _stream()), "csa2_quantize_kv_fp4")
     return out
 
@@ -198,7 +209,7 @@ def index_scores(q_fp8: torch.Tensor, k_fp8: torch.Tensor, N: int, kv_seq_stride
     B, H_I, D_I = q_fp8.shape
     if out is None:
         out = torch.empty((B, N), dtype=torch.float32, device=q_fp8.device)
-    _dev(out, torch.float32, "scores")
+    _out(out, (B, N), torch.float32, "scores")
     qp = _opt_pos(q_pos)
     _check(lib.csa2_index_scores(_ptr(q_fp8), _ptr(k_fp8), B, H_I, D_I, N, kv_seq_stride,
                                  q_per_seq, _ptr(qp), ratio, _ptr(out), _stream()),
@@ -214,7 +225,7 @@ def quantize_mxfp4(x: torch.Tensor, out: Optional[torch.Tensor] = None) -> torch
     if out is None:
         out = torch.empty(x.shape[:-1] + (mxfp4_row_bytes(d),), dtype=torch.uint8,
                           device=x.device)
-    _dev(out, torch.uint8, "out")
+    _out(out, x.shape[:-1] + (mxfp4_row_bytes(d),), torch.uint8, "out")
     _check(lib.csa2_quantize_mxfp4(_ptr(x), n, d, _ptr(out), _stream()), "csa2_quantize_mxfp4")
     return out
 
@@ -228,7 +239,7 @@ def index_scores_mxfp4(q_mx: torch.Tensor, k_mx: torch.Tensor, N: int, kv_seq_st
     B, H_I, rb = q_mx.shape
     if out is None:
         out = torch.empty((B, N), dtype=torch.float32, device=q_mx.device)
-    _dev(out, torch.float32, "scores")
+    _out(out, (B, N), torch.float32, "scores")
     qp = _opt_pos(q_pos)
     _check(lib.csa2_index_scores_mxfp4(_ptr(q_mx), _ptr(k_mx), B, H_I, _mx_dim(rb), N,
                                        kv_seq_stride, q_per_seq, _ptr(qp), ratio, _ptr(out),
@@ -249,7 +260,7 @@ def hier_pool_index_mxfp4(q_mx: torch.Tensor, k_mx: torch.Tensor, N: int, kv_seq
         ws = make_workspace(B, 0, k, 0, P, q_mx.device)
     if out is None:
         out = torch.empty((B, k), dtype=torch.int32, device=q_mx.device)
-    _dev(out, torch.int32, "idx")
+    _out(out, (B, k), torch.int32, "idx")
     _check(lib.csa2_hier_pool_index_mxfp4(_ptr(q_mx), _ptr(k_mx), B, H_I, _mx_dim(rb), N,
                                           kv_seq_stride, q_per_seq, _ptr(pool), P, k, _ptr(out),
                                           _ptr(ws), ws.numel(), _stream()),
@@ -265,7 +276,7 @@ def topk(scores: torch.Tensor, k: int, q_pos: Optional[torch.Tensor] = None, rat
         ws = make_workspace(B, N, k, 0, 0, scores.device)
     if out is None:
         out = torch.empty((B, k), dtype=torch.int32, device=scores.device)
-    _dev(out, torch.int32, "idx")
+    _out(out, (B, k), torch.int32, "idx")
     qp = _opt_pos(q_pos)
     _check(lib.csa2_topk(_ptr(scores), B, N, k, _ptr(qp), ratio, _ptr(out), _ptr(ws),
                          ws.numel(), _stream()), "csa2_topk")
@@ -284,7 +295,7 @@ def hier_pool_index(q_fp8: torch.Tensor, k_fp8: torch.Tensor, N: int, kv_seq_str
         ws = make_workspace(B, 0, k, 0, P, q_fp8.device)
     if out is None:
         out = torch.empty((B, k), dtype=torch.int32, device=q_fp8.device)
-    _dev(out, torch.int32, "idx")
+    _out(out, (B, k), torch.int32, "idx")
     _check(lib.csa2_hier_pool_index(_ptr(q_fp8), _ptr(k_fp8), B, H_I, D_I, N, kv_seq_stride,
                                     q_per_seq, _ptr(pool), P, k, _ptr(out), _ptr(ws), ws.numel(),
                                     _stream()), "csa2_hier_pool_index")
@@ -303,7 +314,7 @@ def block_pool(scores: torch.Tensor, block: int, n_blocks: int,
         ws = torch.empty(n, dtype=torch.uint8, device=scores.device)
     if out is None:
         out = torch.empty((B, n_blocks * block), dtype=torch.int32, device=scores.device)
-    _dev(out, torch.int32, "pool")
+    _out(out, (B, n_blocks * block), torch.int32, "pool")
     _check(lib.csa2_block_pool(_ptr(scores), B, N, _ptr(qp), ratio, block, n_blocks, _ptr(out),
                                _ptr(ws), ws.numel(), _stream()), "csa2_block_pool")
     return out
@@ -327,7 +338,9 @@ def sparse_attn_fp4(q_bf16: torch.Tensor, kv_fp4: torch.Tensor, N: int, kv_seq_s
         out = torch.empty((B, H, D), dtype=torch.float32, device=q.device)
     if lse is None and want_lse:
         lse = torch.empty((B, H), dtype=torch.float32, device=q.device)
-    _dev(out, torch.float32, "out")
+    _out(out, (B, H, D), torch.float32, "out")
+    if lse is not None:
+        _out(lse, (B, H), torch.float32, "lse")
     _check(lib.csa2_sparse_attn_fp4(_ptr(q), _ptr(kv_fp4), B, H, D, N, kv_seq_stride, q_per_seq,
                                     _ptr(idx), k, softmax_scale, _ptr(out), _ptr(lse), _ptr(ws),
                                     ws.numel(), _stream()), "csa2_sparse_attn_fp4")
@@ -357,7 +370,9 @@ def sparse_attn_fp4_swa(q_bf16: torch.Tensor, kv_fp4: torch.Tensor, N: int, kv_s
         out = torch.empty((B, H, D), dtype=torch.float32, device=q.device)
     if lse is None and want_lse:
         lse = torch.empty((B, H), dtype=torch.float32, device=q.device)
-    _dev(out, torch.float32, "out")
+    _out(out, (B, H, D), torch.float32, "out")
+    if lse is not None:
+        _out(lse, (B, H), torch.float32, "lse")
     _check(lib.csa2_sparse_attn_fp4_swa(_ptr(q), _ptr(kv_fp4), B, H, D, N, kv_seq_stride,
                                         q_per_seq, _ptr(idx), k, _ptr(swa_kv), ring, n_win,
                                         _ptr(qp), softmax_scale, _ptr(out), _ptr(lse), _ptr(ws),

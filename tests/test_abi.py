@@ -67,6 +67,19 @@ def test_binding_refuses_cpu_tensors(libpath):
         csa2.quantize_kv_fp4(torch.zeros(4, 512))
 
 
+def test_binding_refuses_outputs_of_the_wrong_shape(libpath):
+    # the library writes exactly the documented layout through an output pointer: a
+    # caller's tensor of another shape is refused before its device is even looked at
+    import torch
+    from sparse_attention_decode_csa2_gb300 import csa2
+    with pytest.raises(ValueError, match="shape"):
+        csa2._out(torch.zeros(4, 287, dtype=torch.uint8), (4, 288), torch.uint8, "out")
+    with pytest.raises(ValueError, match="shape"):
+        csa2._out(torch.zeros(2, 64, 511), (2, 64, 512), torch.float32, "out")
+    with pytest.raises(ValueError, match="CUDA"):   # right shape, but host memory
+        csa2._out(torch.zeros(2, 64), (2, 64), torch.float32, "lse")
+
+
 def test_mxfp4_argument_validation_before_any_device_work(libpath):
     from sparse_attention_decode_csa2_gb300 import csa2
     lib = csa2.lib
