@@ -114,6 +114,10 @@ csa2_status csa2_quantize_kv_fp4(const float* x, int64_t n_rows, int d, uint8_t*
  *   H_I <= 32); the dot product then accumulates in fp32, which is exact
  *   whenever every partial sum is an fp32-representable value (e.g. integer
  *   inputs).  k_fp8 must be 16-byte aligned.
+ *   Returns CSA2_ERR_UNSUPPORTED when the rows the scan reads,
+ *   (S - 1) * kv_seq_stride + N with S = ceil(B / q_per_seq), number 2^31 or
+ *   more (the scan addresses them with 32-bit tensor coordinates); the
+ *   E4M3 layers of csa2_layer_group have the same limit.
  */
 csa2_status csa2_index_scores(const uint8_t* q_fp8, const uint8_t* k_fp8, int B, int H_I, int D_I,
                               int64_t N, int64_t kv_seq_stride, int q_per_seq,

@@ -75,6 +75,16 @@ csa2_status check_indexer(const uint8_t* q, const uint8_t* k, int B, int H_I, in
   return CSA2_OK;
 }
 
+// The full E4M3 scan reads indexer K through 2D tensor-map coordinates, which
+// are 32-bit: every row it may touch, (sequences - 1) * kv_seq_stride + N of
+// them, must have an index below 2^31.
+csa2_status check_scan_rows(int B, int64_t N, int64_t kv_seq_stride, int q_per_seq) {
+  if (B <= 0) return CSA2_OK;
+  const int64_t S = ((int64_t)B + q_per_seq - 1) / q_per_seq;
+  const int64_t rows = (S - 1) * kv_seq_stride + N;
+  return rows > (int64_t)INT32_MAX ? CSA2_ERR_UNSUPPORTED : CSA2_OK;
+}
+
 // MXFP4 indexer rows (68 bytes at D_I = 128): a sequence's rows must start
 // on a 16-byte boundary for the bulk copies of the full scan.
 csa2_status check_indexer_mx(const uint8_t* q, const uint8_t* k, int B, int H_I, int D_I,
@@ -171,6 +181,7 @@ csa2_status csa2_index_scores(const uint8_t* q_fp8, const uint8_t* k_fp8, int B,
   csa2_status s = check_seq(B, N, kv_seq_stride, q_per_seq);
   if (s != CSA2_OK) return s;
   if ((s = check_indexer(q_fp8, k_fp8, B, H_I, D_I, ratio)) != CSA2_OK) return s;
+  if ((s = check_scan_rows(B, N, kv_seq_stride, q_per_seq)) != CSA2_OK) return s;
   if (B > 0 && N > 0 && !scores) return CSA2_ERR_INVALID_ARG;
   return check_launch(launch_index_scores(q_fp8, k_fp8, B, H_I, D_I, N, kv_seq_stride, q_per_seq,
                                           q_pos, ratio, scores, nullptr, stream));
@@ -350,6 +361,9 @@ csa2_status csa2_layer_group(const csa2_layer* layers, int n_layers, const csa2_
     } else {
       if ((s = check_indexer_fmt(g->indexer_fmt, L.qi_fp8, g->ki_fp8, g->B, g->H_I, g->D_I,
                                  g->ratio, g->kv_seq_stride, g->q_per_seq)) != CSA2_OK)
+        return s;
+      if (g->indexer_fmt == CSA2_INDEXER_E4M3 &&
+          (s = check_scan_rows(g->B, g->N, g->kv_seq_stride, g->q_per_seq)) != CSA2_OK)
         return s;
       if (g->B > 0 && !L.idx_out) return CSA2_ERR_INVALID_ARG;
     }

@@ -115,6 +115,20 @@ def _group(csa2, modes, B=32, N=16384, k=2048, pool=0, pool_block=0, fmt=0):
     return layers, g
 
 
+def test_index_scan_rejects_rows_beyond_32_bit_coordinates(libpath):
+    import ctypes
+    # the full E4M3 scan addresses indexer-K rows with 32-bit tensor coordinates: a call
+    # whose sequences span 2^31 rows or more is refused before any device work
+    from sparse_attention_decode_csa2_gb300 import csa2
+    lib = csa2.lib
+    fake = 1 << 20                     # aligned, never dereferenced: validation fails first
+    half = 1 << 30
+    code = lib.csa2_index_scores(fake, fake, 2, 8, 64, half, half, 1, None, 4, fake, None)
+    assert code == 2                   # CSA2_ERR_UNSUPPORTED: rows = 2^30 + 2^30
+    layers, g = _group(csa2, [0], B=2, N=half)
+    assert lib.csa2_layer_group(layers, 1, ctypes.byref(g), fake, 1 << 40, None) == 2
+
+
 def test_layer_group_launch_counts(libpath):
     import ctypes
     from sparse_attention_decode_csa2_gb300 import csa2
