@@ -421,6 +421,7 @@ def run_gpu(args, rank, world, local):
         "steps": K,
         "warmup": W,
         "ms_per_step": ms_per_step,
+        "step_ms_quantiles": step_quantiles(step_ms),
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
@@ -450,6 +451,15 @@ def run_gpu(args, rank, world, local):
         "wall_s": t_wall,
     }
     return res
+
+
+def step_quantiles(step_ms) -> dict:
+    """p10 / median / p90 of this rank's timed steps (ms), nearest-rank."""
+    xs = sorted(float(x) for x in step_ms)
+    if not xs:
+        return {}
+    pick = lambda q: xs[min(len(xs) - 1, max(0, math.ceil(q * len(xs)) - 1))]
+    return {"p10": pick(0.10), "p50": pick(0.50), "p90": pick(0.90)}
 
 
 def kernel_revision() -> str:

@@ -67,3 +67,12 @@ def test_reference_arm_prints_on_rank_zero_only():
     d = json.loads(lines[0][0])
     assert d["impl"] == "reference" and d["n_gpus"] == 2 and d["value"] > 0
     assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["cores"] == 1
+
+
+def test_step_quantiles_are_nearest_rank():
+    sys.path.insert(0, ROOT)
+    import bench
+    q = bench.step_quantiles(list(range(20, 0, -1)))   # 1..20 ms in any order
+    assert q == {"p10": 2.0, "p50": 10.0, "p90": 18.0}
+    assert bench.step_quantiles([0.25]) == {"p10": 0.25, "p50": 0.25, "p90": 0.25}
+    assert bench.step_quantiles([]) == {}
