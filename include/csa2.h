@@ -221,6 +221,16 @@ csa2_status csa2_hier_pool_index(const uint8_t* q_fp8, const uint8_t* k_fp8, int
                                  size_t ws_bytes, cudaStream_t stream);
 
 /*
+ * csa2_hier_pool_index_mxfp4 -- csa2_hier_pool_index with MXFP4 indexer rows
+ * (q_mx, k_mx as in csa2_index_scores_mxfp4); same pool, idx and workspace
+ * rules.
+ */
+csa2_status csa2_hier_pool_index_mxfp4(const uint8_t* q_mx, const uint8_t* k_mx, int B, int H_I,
+                                       int D_I, int64_t N, int64_t kv_seq_stride, int q_per_seq,
+                                       const int32_t* pool, int P, int k, int32_t* idx, void* ws,
+                                       size_t ws_bytes, cudaStream_t stream);
+
+/*
  * csa2_sparse_attn_fp4 -- gathers the selected FP4 entries, dequantises them
  * and runs MQA softmax attention over them (walkthrough 1.(4) "CSA2";
  * 1.(5).4: the cache is dequantised before attention; 2.(2).1: 64 heads x
@@ -234,16 +244,6 @@ csa2_status csa2_hier_pool_index(const uint8_t* q_fp8, const uint8_t* k_fp8, int
  *   A row with no valid slot yields out = 0 and lse = -inf.
  *   ws       at least csa2_workspace_size(B, 0, k, H, 0) bytes.
  */
-/*
- * csa2_hier_pool_index_mxfp4 -- csa2_hier_pool_index with MXFP4 indexer rows
- * (q_mx, k_mx as in csa2_index_scores_mxfp4); same pool, idx and workspace
- * rules.
- */
-csa2_status csa2_hier_pool_index_mxfp4(const uint8_t* q_mx, const uint8_t* k_mx, int B, int H_I,
-                                       int D_I, int64_t N, int64_t kv_seq_stride, int q_per_seq,
-                                       const int32_t* pool, int P, int k, int32_t* idx, void* ws,
-                                       size_t ws_bytes, cudaStream_t stream);
-
 csa2_status csa2_sparse_attn_fp4(const uint16_t* q_bf16, const uint8_t* kv_fp4, int B, int H,
                                  int D, int64_t N, int64_t kv_seq_stride, int q_per_seq,
                                  const int32_t* idx, int k, float softmax_scale, float* out,
@@ -380,7 +380,9 @@ csa2_status csa2_workspace_init(void* ws, size_t ws_bytes, cudaStream_t stream);
 /*
  * Synchronises `stream`, reads and clears the device status word.  Writes
  * the raw bits to *device_bits (if non-NULL): bit 0 bad index, bit 1 bounded
- * wait timed out.  Returns CSA2_OK, CSA2_ERR_BAD_INDEX or CSA2_ERR_TIMEOUT.
+ * wait timed out.  Returns CSA2_OK, CSA2_ERR_BAD_INDEX or CSA2_ERR_TIMEOUT;
+ * CSA2_ERR_WORKSPACE for a NULL ws, CSA2_ERR_CUDA if the copy, the clear or
+ * the synchronisation fails (csa2_last_cuda_error names the cause).
  */
 csa2_status csa2_read_status(void* ws, cudaStream_t stream, int32_t* device_bits);
 
