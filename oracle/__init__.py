@@ -21,21 +21,31 @@ import numpy as np
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "csa2_oracle.c")
-_LIB_PATH = os.path.join(_HERE, "_libcsa2_oracle.so")
+# CSA2_ORACLE_LIB names a prebuilt copy to load instead (the mutation tests
+# compile copies of csa2_oracle.c with one planted mistake each)
+_VARIANT = os.environ.get("CSA2_ORACLE_LIB")
+_LIB_PATH = _VARIANT or os.path.join(_HERE, "_libcsa2_oracle.so")
 _lock = threading.Lock()
 _lib = None
 
 FULL, REINDEX, REUSE = 0, 1, 2
 
 
+def compile_command(src: str, out: str):
+    """gcc command that builds the oracle library `out` from `src`."""
+    return ["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-ffp-contract=off", "-o", out, src,
+            "-lm"]
+
+
 def build(force: bool = False) -> str:
     """Compile the oracle (gcc, no fast-math, no FMA contraction)."""
+    if _VARIANT:
+        return _LIB_PATH
     if (not force and os.path.exists(_LIB_PATH)
             and os.path.getmtime(_LIB_PATH) >= os.path.getmtime(_SRC)):
         return _LIB_PATH
     tmp = _LIB_PATH + f".tmp{os.getpid()}"
-    subprocess.run(["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-ffp-contract=off",
-                    "-o", tmp, _SRC, "-lm"], check=True)
+    subprocess.run(compile_command(_SRC, tmp), check=True)
     os.replace(tmp, _LIB_PATH)
     return _LIB_PATH
 

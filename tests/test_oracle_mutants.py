@@ -1,0 +1,110 @@
+"""The oracle's pins catch plausible mistakes.  Each case plants one mistake in
+a copy of ``oracle/csa2_oracle.c`` (a wrong constant, index, tie rule, sign,
+bound or schedule step), builds that copy on the CPU and runs the oracle pin
+tests against it in a subprocess; at least one pin must fail.  An unchanged
+copy built the same way must pass them all.  CPU only."""
+import os
+import subprocess
+import sys
+
+import pytest
+
+import oracle
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+SRC = os.path.join(ROOT, "oracle", "csa2_oracle.c")
+PINS = ["tests/test_oracle_formats.py", "tests/test_oracle_select.py",
+        "tests/test_oracle_attention.py", "tests/test_oracle_mxfp4.py"]
+
+# (name, text in csa2_oracle.c, replacement): each text occurs exactly once
+MUTANTS = [
+    ("fp4 scale divisor 4 instead of 6",
+     "orc_e4m3_encode(amax / 6.0)", "orc_e4m3_encode(amax / 4.0)"),
+    ("e2m1 ties to the larger code",
+     """    double d = fabs(orc_e2m1_value(c) - q);
+    if (d < best_d || (d == best_d && (c & 1) == 0)) {""",
+     """    double d = fabs(orc_e2m1_value(c) - q);
+    if (d <= best_d) {"""),
+    ("e4m3 ties to the larger code",
+     """    double d = fabs(orc_e4m3_value(c) - a);
+    if (d < best_d || (d == best_d && (c & 1) == 0)) {""",
+     """    double d = fabs(orc_e4m3_value(c) - a);
+    if (d <= best_d) {"""),
+    ("e4m3 exponent bias 8",
+     "else mag = (1.0 + m / 8.0) * ldexp(1.0, e - 7);",
+     "else mag = (1.0 + m / 8.0) * ldexp(1.0, e - 8);"),
+    ("fp4 nibbles swapped",
+     """        int mag = (s == 0.0) ? 0 : orc_e2m1_encode_magnitude(fabs(xv) / s);
+        int code = (signbit(xv) ? 8 : 0) | mag;
+        codes[ch / 2] |= (uint8_t)((ch & 1) ? (code << 4) : code);""",
+     """        int mag = (s == 0.0) ? 0 : orc_e2m1_encode_magnitude(fabs(xv) / s);
+        int code = (signbit(xv) ? 8 : 0) | mag;
+        codes[ch / 2] |= (uint8_t)((ch & 1) ? code : (code << 4));"""),
+    ("fp4 sign of negative zero dropped",
+     """        int mag = (s == 0.0) ? 0 : orc_e2m1_encode_magnitude(fabs(xv) / s);
+        int code = (signbit(xv) ? 8 : 0) | mag;""",
+     """        int mag = (s == 0.0) ? 0 : orc_e2m1_encode_magnitude(fabs(xv) / s);
+        int code = (xv < 0.0 ? 8 : 0) | mag;"""),
+    ("fp4 dequantise with the scale of the wrong block",
+     "out[ch] = orc_e2m1_value(code) * orc_e4m3_value(scales[ch / 16]);",
+     "out[ch] = orc_e2m1_value(code) * orc_e4m3_value(scales[ch / 32]);"),
+    ("mxfp4 shared exponent off by one",
+     "shared = (e - 1) - 2;", "shared = (e - 1) - 1;"),
+    ("visibility from the entry's first token",
+     "(int64_t)ratio * n + ratio - 1 <= pos", "(int64_t)ratio * n <= pos"),
+    ("indexer score drops the last head",
+     """      idx_row_values(kseq + j * rb, D_I, fmt, kj);
+      double s = 0.0;
+      for (int h = 0; h < H_I; ++h) {""",
+     """      idx_row_values(kseq + j * rb, D_I, fmt, kj);
+      double s = 0.0;
+      for (int h = 0; h < H_I - 1; ++h) {"""),
+    ("top-k ties to the higher index",
+     "return (x->j < y->j) ? -1 : (x->j > y->j);",
+     "return (x->j > y->j) ? -1 : (x->j < y->j);"),
+    ("top-k output in rank order",
+     "  qsort(out, (size_t)take, sizeof(int32_t), cmp_i32);\n", ""),
+    ("block score = its first entry's score",
+     "if (scores[(int64_t)q * N + j] > m) m = scores[(int64_t)q * N + j];",
+     "if (j == b * block) m = scores[(int64_t)q * N + j];"),
+    ("attention logits without the softmax scale",
+     "logit[t] = scale * dot;", "logit[t] = dot;"),
+    ("lse without the max shift",
+     "if (lse) lse[h] = m + log(l);", "if (lse) lse[h] = log(l);"),
+    ("swa window one token longer",
+     "int64_t t0 = pos - n_win + 1 > 0 ? pos - n_win + 1 : 0;",
+     "int64_t t0 = pos - n_win > 0 ? pos - n_win : 0;"),
+    ("reuse takes the full layer's indices past a reindex",
+     """      latest = idx;
+    } else if (modes[l] == ORC_REUSE) {""",
+     """    } else if (modes[l] == ORC_REUSE) {"""),
+]
+
+
+def _build(text: str, tmp_path) -> str:
+    src = tmp_path / "csa2_oracle.c"
+    src.write_text(text)
+    lib = str(tmp_path / "libcsa2_oracle_variant.so")
+    subprocess.run(oracle.compile_command(str(src), lib), check=True)
+    return lib
+
+
+def _run_pins(lib: str) -> subprocess.CompletedProcess:
+    env = dict(os.environ, CSA2_ORACLE_LIB=lib)
+    return subprocess.run([sys.executable, "-m", "pytest", *PINS, "-x", "-q",
+                           "-p", "no:cacheprovider"],
+                          cwd=ROOT, env=env, capture_output=True, text=True, timeout=600)
+
+
+def test_an_unchanged_copy_passes_every_pin(tmp_path):
+    r = _run_pins(_build(open(SRC).read(), tmp_path))
+    assert r.returncode == 0, r.stdout[-3000:]
+
+
+@pytest.mark.parametrize("name,old,new", MUTANTS, ids=[m[0] for m in MUTANTS])
+def test_a_planted_mistake_fails_a_pin(name, old, new, tmp_path):
+    text = open(SRC).read()
+    assert text.count(old) == 1, name
+    r = _run_pins(_build(text.replace(old, new), tmp_path))
+    # exit code 1: the run completed and some pin failed (not a crash or a usage error)
+    assert r.returncode == 1, f"{name} survived the pins:\n{r.stdout[-3000:]}"
