@@ -74,6 +74,29 @@ MUTANTS = [
     ("swa window one token longer",
      "int64_t t0 = pos - n_win + 1 > 0 ? pos - n_win + 1 : 0;",
      "int64_t t0 = pos - n_win > 0 ? pos - n_win : 0;"),
+    ("pool re-index returns pool slots instead of entry ids",
+     "      c[n].j = j;", "      c[n].j = p;"),
+    ("mxfp4 scale byte biased by 126",
+     "scales[b] = (uint8_t)(shared + 127);", "scales[b] = (uint8_t)(shared + 126);"),
+    ("e2m1 normal values halved",
+     "(1.0 + 0.5 * m) * ldexp(1.0, e - 1)", "(1.0 + 0.5 * m) * ldexp(1.0, e - 2)"),
+    ("softmax weights not normalised",
+     "double p = logit[t] / l;", "double p = logit[t];"),
+    ("top-k ranks invisible entries too",
+     """    for (int64_t j = 0; j < nv; ++j) {
+      c[j].s = scores[(int64_t)q * N + j];
+      c[j].j = j;
+    }
+    select_topk(c, nv, k, idx + (int64_t)q * k);""",
+     """    for (int64_t j = 0; j < N; ++j) {
+      c[j].s = scores[(int64_t)q * N + j];
+      c[j].j = j;
+    }
+    select_topk(c, N, k, idx + (int64_t)q * k);"""),
+    ("blockwise pool drops the partial last block",
+     "int64_t nb = (nv + block - 1) / block;", "int64_t nb = nv / block;"),
+    ("reindex in the pool scores with the first layer's query",
+     "orc_hier_pool_index_fmt(qi_fp8[l], ki_fp8", "orc_hier_pool_index_fmt(qi_fp8[0], ki_fp8"),
     ("reuse takes the full layer's indices past a reindex",
      """      latest = idx;
     } else if (modes[l] == ORC_REUSE) {""",
