@@ -3,6 +3,7 @@ a copy of ``oracle/csa2_oracle.c`` (a wrong constant, index, tie rule, sign,
 bound or schedule step), builds that copy on the CPU and runs the oracle pin
 tests against it in a subprocess; at least one pin must fail.  An unchanged
 copy built the same way must pass them all.  CPU only."""
+import concurrent.futures as cf
 import os
 import subprocess
 import sys
@@ -104,30 +105,44 @@ MUTANTS = [
 ]
 
 
-def _build(text: str, tmp_path) -> str:
-    src = tmp_path / "csa2_oracle.c"
-    src.write_text(text)
-    lib = str(tmp_path / "libcsa2_oracle_variant.so")
-    subprocess.run(oracle.compile_command(str(src), lib), check=True)
-    return lib
-
-
-def _run_pins(lib: str) -> subprocess.CompletedProcess:
+def _build_and_run(text: str, workdir: str):
+    """Build one copy of the oracle from `text` and run the pins against it."""
+    os.makedirs(workdir, exist_ok=True)
+    src = os.path.join(workdir, "csa2_oracle.c")
+    with open(src, "w") as f:
+        f.write(text)
+    lib = os.path.join(workdir, "libcsa2_oracle_variant.so")
+    subprocess.run(oracle.compile_command(src, lib), check=True)
     env = dict(os.environ, CSA2_ORACLE_LIB=lib)
-    return subprocess.run([sys.executable, "-m", "pytest", *PINS, "-x", "-q",
-                           "-p", "no:cacheprovider"],
-                          cwd=ROOT, env=env, capture_output=True, text=True, timeout=600)
+    r = subprocess.run([sys.executable, "-m", "pytest", *PINS, "-x", "-q",
+                        "-p", "no:cacheprovider"],
+                       cwd=ROOT, env=env, capture_output=True, text=True, timeout=600)
+    return r.returncode, r.stdout[-3000:]
 
 
-def test_an_unchanged_copy_passes_every_pin(tmp_path):
-    r = _run_pins(_build(open(SRC).read(), tmp_path))
-    assert r.returncode == 0, r.stdout[-3000:]
-
-
-@pytest.mark.parametrize("name,old,new", MUTANTS, ids=[m[0] for m in MUTANTS])
-def test_a_planted_mistake_fails_a_pin(name, old, new, tmp_path):
+@pytest.fixture(scope="module")
+def runs(tmp_path_factory):
+    """Every copy (the unchanged one under the key None) built and run, several at a time."""
     text = open(SRC).read()
-    assert text.count(old) == 1, name
-    r = _run_pins(_build(text.replace(old, new), tmp_path))
+    jobs = {None: text}
+    for name, old, new in MUTANTS:
+        assert text.count(old) == 1, name
+        jobs[name] = text.replace(old, new)
+    base = tmp_path_factory.mktemp("oracle_mutants")
+    workers = max(1, min(8, os.cpu_count() or 1))
+    with cf.ThreadPoolExecutor(workers) as ex:
+        futs = {key: ex.submit(_build_and_run, body, str(base / f"m{i}"))
+                for i, (key, body) in enumerate(jobs.items())}
+        return {key: f.result() for key, f in futs.items()}
+
+
+def test_an_unchanged_copy_passes_every_pin(runs):
+    rc, out = runs[None]
+    assert rc == 0, out
+
+
+@pytest.mark.parametrize("name", [m[0] for m in MUTANTS])
+def test_a_planted_mistake_fails_a_pin(runs, name):
+    rc, out = runs[name]
     # exit code 1: the run completed and some pin failed (not a crash or a usage error)
-    assert r.returncode == 1, f"{name} survived the pins:\n{r.stdout[-3000:]}"
+    assert rc == 1, f"{name} survived the pins:\n{out}"
