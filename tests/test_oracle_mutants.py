@@ -98,6 +98,14 @@ MUTANTS = [
      "int64_t nb = (nv + block - 1) / block;", "int64_t nb = nv / block;"),
     ("reindex in the pool scores with the first layer's query",
      "orc_hier_pool_index_fmt(qi_fp8[l], ki_fp8", "orc_hier_pool_index_fmt(qi_fp8[0], ki_fp8"),
+    ("swa ring row off by one",
+     "(s * swa_ring + t % swa_ring) * D", "(s * swa_ring + (t + 1) % swa_ring) * D"),
+    # (swapping the nibbles in the MXFP4 decode is no mistake the oracle can show: q and K
+    # are permuted alike inside one scale block, so every score is unchanged; the byte
+    # order itself is pinned by the quantiser's golden rows)
+    ("e8m0 bias 128",
+     "double orc_e8m0_value(int byte) { return ldexp(1.0, byte - 127); }",
+     "double orc_e8m0_value(int byte) { return ldexp(1.0, byte - 128); }"),
     ("reuse takes the full layer's indices past a reindex",
      """      latest = idx;
     } else if (modes[l] == ORC_REUSE) {""",
