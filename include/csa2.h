@@ -110,10 +110,14 @@ csa2_status csa2_quantize_kv_fp4(const float* x, int64_t n_rows, int d, uint8_t*
  *            indexer heads (sequence s at entry offset s * kv_seq_stride)
  *   scores   fp32 [B][N]: scores[q][j] = sum_h sum_d q[q][h][d] * k[s][j][d]
  *            for visible j, -inf for invisible j
- *   For E4M3 inputs the head sum is formed first (exact in fp32 for
- *   H_I <= 32); the dot product then accumulates in fp32, which is exact
- *   whenever every partial sum is an fp32-representable value (e.g. integer
- *   inputs).  k_fp8 must be 16-byte aligned.
+ *   Arithmetic: the tensor-core scan forms each head's D_I-term dot
+ *   product with exact E4M3 x E4M3 products accumulated in fp32, then adds
+ *   the H_I per-head fp32 sums in fp32.  Every step is exact whenever every
+ *   partial sum is fp32-representable (e.g. integer inputs, where |score| <=
+ *   H_I * D_I * 64 < 2^24); otherwise each sum carries ordinary fp32
+ *   rounding.  (The pool re-index of csa2_hier_pool_index forms the head sum
+ *   of the query first, in two f16 parts: exact for integer inputs.)
+ *   k_fp8 must be 16-byte aligned.
  *   Returns CSA2_ERR_UNSUPPORTED when the rows the scan reads,
  *   (S - 1) * kv_seq_stride + N with S = ceil(B / q_per_seq), number 2^31 or
  *   more (the scan addresses them with 32-bit tensor coordinates); the
@@ -298,7 +302,10 @@ csa2_status csa2_sparse_attn_fp4_swa(const uint16_t* q_bf16, const uint8_t* kv_f
  *   the last call's contents (nothing needs to start cleared): calls that
  *   overlap on the GPU (other streams, other host threads) race on it and must
  *   be serialised by the caller.  There is no status word: indices outside
- *   [-1, N) are skipped as in csa2_sparse_attn_fp4 but not reported.
+ *   [-1, N) are skipped as in csa2_sparse_attn_fp4, and a bounded device wait
+ *   that gives up (about 2 s) ends its CTA early, but neither is reported.
+ *   A failing CUDA call returns CSA2_ERR_CUDA and leaves its message for
+ *   csa2_last_cuda_error().
  */
 csa2_status csa2_sparse_attn_fp4_noalloc(const uint16_t* q_bf16, const uint8_t* kv_fp4, int B,
                                          int H, int D, int64_t N, int64_t kv_seq_stride,

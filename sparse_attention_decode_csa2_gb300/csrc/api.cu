@@ -17,6 +17,14 @@ int device_sm_count() {
   return sms > 0 ? sms : 148;
 }
 
+thread_local const char* g_last_cuda_error = "no error";
+
+csa2_status check_launch(cudaError_t e) {
+  if (e == cudaSuccess) return CSA2_OK;
+  g_last_cuda_error = cudaGetErrorString(e);
+  return CSA2_ERR_CUDA;
+}
+
 namespace {
 
 struct WsLayout {
@@ -50,14 +58,6 @@ WsLayout layout(int B, int64_t N, int k, int H, int P) {
 }
 
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
-
-thread_local const char* g_last_cuda_error = "no error";
-
-csa2_status check_launch(cudaError_t e) {
-  if (e == cudaSuccess) return CSA2_OK;
-  g_last_cuda_error = cudaGetErrorString(e);
-  return CSA2_ERR_CUDA;
-}
 
 csa2_status check_seq(int B, int64_t N, int64_t kv_seq_stride, int q_per_seq) {
   if (B < 0 || N < 0 || N > INT32_MAX - 1) return CSA2_ERR_INVALID_ARG;

@@ -71,11 +71,12 @@ extern "C" csa2_status csa2_sparse_attn_fp4_noalloc(const uint16_t* q_bf16, cons
   if (attn_scratch_bytes(B, H, k) > kNoallocScratchBytes) return CSA2_ERR_WORKSPACE;
   if (B == 0) return CSA2_OK;
   void* scratch = nullptr;
-  if (scratch_address(&scratch) != cudaSuccess) return CSA2_ERR_CUDA;
+  csa2_status s = check_launch(scratch_address(&scratch));
+  if (s != CSA2_OK) return s;
   // The partials are fully written before they are read, so nothing needs
   // clearing between calls.  No status word: indices outside [-1, N) are
-  // skipped exactly as in csa2_sparse_attn_fp4, but not reported.
-  cudaError_t e = launch_sparse_attn(q_bf16, kv_fp4, B, H, N, kv_seq_stride, q_per_seq, idx, k,
-                                     softmax_scale, out, lse, scratch, nullptr, stream);
-  return e == cudaSuccess ? CSA2_OK : CSA2_ERR_CUDA;
+  // skipped exactly as in csa2_sparse_attn_fp4, and a bounded device wait
+  // that gives up ends its CTA early, but neither is reported.
+  return check_launch(launch_sparse_attn(q_bf16, kv_fp4, B, H, N, kv_seq_stride, q_per_seq, idx,
+                                         k, softmax_scale, out, lse, scratch, nullptr, stream));
 }

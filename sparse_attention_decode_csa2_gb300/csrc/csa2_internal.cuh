@@ -203,4 +203,8 @@ cudaError_t launch_sparse_attn_tc(const uint16_t* q_bf16, const uint8_t* kv_fp4,
 
 int device_sm_count();
 
+// CSA2_OK for cudaSuccess; otherwise keeps cudaGetErrorString(e) for
+// csa2_last_cuda_error() (per host thread) and returns CSA2_ERR_CUDA.
+csa2_status check_launch(cudaError_t e);
+
 }  // namespace csa2

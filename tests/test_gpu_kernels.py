@@ -155,6 +155,34 @@ def test_topk_bit_exact(C, B, N, k, kind):
     assert (got == oracle.topk(s.astype(np.float64), k)).all()
 
 
+@pytest.mark.parametrize("B,N,k,kind", [
+    (2, 40000, 2048, "ties"), (2, 40000, 8192, "normal"), (2, 262144, 2048, "normal"),
+    (2, 262144, 8192, "ties"), (3, 50000, 20000, "ties"), (1, 2200000, 2048, "normal"),
+    (2, 40000, 3000, "equal")])
+def test_topk_one_kernel_long_rows_bit_exact(C, B, N, k, kind):
+    # Rows longer than 32768 candidates take the one-kernel selection when the
+    # workspace holds only the 256-byte status word, when k > 16384, or when a
+    # row needs more than 64 chunks of 32768 (N > 2^21); ties still go to the
+    # lower index and the output is ascending, -1 padded.
+    rng = np.random.default_rng(3 * N + k)
+    if kind == "ties":
+        s = rng.integers(-40, 40, (B, N)).astype(np.float32) * 64
+    elif kind == "normal":
+        s = rng.standard_normal((B, N)).astype(np.float32)
+    else:
+        s = np.full((B, N), -2.25, np.float32)
+    pos = rng.integers(4 * 30000, 4 * N + 4, B).astype(np.int32)
+    pos[0] = 4 * N + 100
+    small = torch.zeros(256, dtype=torch.uint8, device="cuda")
+    assert C.workspace_size(B, N, k) > 256 or N > (1 << 21) or k > 16384
+    got = C.topk(cuda(s), k, cuda(pos), 4, small).cpu().numpy()
+    ref = oracle.topk(s.astype(np.float64), k, pos, 4)
+    assert (got == ref).all()
+    got = C.topk(cuda(s), k, None, 1, small).cpu().numpy()
+    assert (got == oracle.topk(s.astype(np.float64), k)).all()
+    assert C.read_status(small) == (0, 0)
+
+
 def test_topk_with_infinities(C):
     rng = np.random.default_rng(9)
     s = rng.integers(-3, 3, (3, 5000)).astype(np.float32)
@@ -178,6 +206,21 @@ def test_hier_pool_bit_exact(C, N, P, k):
     got = C.hier_pool_index(cuda(qi1), cuda(ki), N, N, 1, cuda(pool), k).cpu().numpy()
     ref = oracle.hier_pool_index(qi1, ki, N, N, 1, pool, k)
     assert (got == ref).all()
+
+
+@pytest.mark.parametrize("P,k", [(40000, 2048), (40000, 8192)])
+def test_hier_pool_longer_than_one_cta_bit_exact(C, P, k):
+    # a pool of more than 32768 candidates: selected through the position map
+    # by the one-kernel long-row selection
+    rng = np.random.default_rng(P + k)
+    B, N, H_I, D_I = 2, 50000, 8, 64
+    qi0 = int_e4m3(rng, (B, H_I, D_I))
+    qi1 = int_e4m3(rng, (B, H_I, D_I))
+    ki = int_e4m3(rng, (B * N, D_I))
+    pos = np.array([4 * N - 1, 4 * (N - 3000)], np.int32)
+    pool = oracle.topk(oracle.index_scores(qi0, ki, N, N, 1, pos, 4), P, pos, 4)
+    got = C.hier_pool_index(cuda(qi1), cuda(ki), N, N, 1, cuda(pool), k).cpu().numpy()
+    assert (got == oracle.hier_pool_index(qi1, ki, N, N, 1, pool, k)).all()
 
 
 def test_hier_pool_flags_unsorted_pool(C):
