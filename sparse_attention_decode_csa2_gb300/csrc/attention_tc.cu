@@ -5,28 +5,61 @@
 // dequantised 512-channel latent shared by the heads.
 //
 // One CTA = one query x a chunk of its selected slots, in tiles of 128
-// entries.  The problem is computed transposed so that the 128 entries of a
-// tile fill the M = 128 rows of a tcgen05.mma:
-//   S^T[e][h]  = sum_c V[e][c] Q[h][c]         A = V tile (K-major, SW128)
-//   O^T[c][h] += sum_e V[e][c] P[h][e]         A = the same V bytes read as an
-//                                              MN-major operand, 4 x 128 rows
-// B operands (Q, P) are K-major SW128 tiles in shared memory; both
-// accumulators live in tensor memory (O^T: 4 x H columns, S^T: H columns).
+// entries:
+//   S[h][e]    = sum_c Q[h][c] V[e][c]     M = 64 heads, N = 128 entries
+//                                          (A = Q, B = V tile, both K-major SW128)
+//   O^T[c][h] += sum_e V[e][c] P[h][e]    M = 4 x 128 channels, N = 64 heads,
+//                                          K = 128 entries (A = the same V bytes
+//                                          read MN-major, B = P K-major)
+// Both accumulators live in tensor memory: O^T in 4 x 64 columns, S (one head
+// per TMEM lane of the M = 64 layout: heads 16q .. 16q + 15 in lanes 32q ..
+// 32q + 15) in two buffers of 128 columns.  A tcgen05.mma of this shape costs
+// about the same whether it covers 64 or 128 entries, so the tile is as wide
+// as shared memory allows.
 //
-// Warp roles (512 threads):
-//   warps 0-7   softmax + epilogue: thread = TMEM lane = entry (S) / channel
-//               (O), warps w and w + 4 share lanes and split the 64 heads;
-//               warp 0 allocates TMEM and its lane 0 issues every MMA
-//   warps 8-15  dequantisers: each thread loads half of one FP4 row (144 B)
-//               straight from global memory one tile ahead, converts E2M1 x
-//               E4M3 to fp16 (exact) and stores it into the swizzled V tile
-// Per tile: dequant V (per 64-channel atom, signalled by mbarriers) -> S^T
-// MMAs -> online softmax (fp32, exp2, lazy rescale: the reference max moves
-// only when a tile max exceeds it by more than 2^8 in the exp2 domain, so P
-// <= 256 stays in fp16 range and O is rarely touched) -> P (fp16) to smem ->
-// O^T MMAs -> next tile.  All mbarrier waits are bounded (about 2 s of
-// %globaltimer); a wait that gives up sets the timeout status bit and the CTA
-// drains and exits, freeing its tensor memory.
+// Pipeline.  There is one V buffer, handed over per pair of 64-channel atoms:
+// O^T(t) M-block p reads atoms 2p, 2p + 1 of V(t); once it completes the
+// dequantisers write those atoms of V(t + 1); S(t + 1) consumes atoms in K
+// order as they arrive.  The tensor pipe thus runs O^T(t) and S(t + 1) back
+// to back and idles only while the softmax of t + 1 runs.  Warp roles (512
+// threads):
+//   warps 0-3   softmax: warp q holds heads 16q .. 16q + 15; a paired 16-lane
+//               load gives lane l head 16q + l % 16 and half of the tile's
+//               entries (lanes l and l ^ 16 share a head), so a head's max and
+//               sum need one shuffle.  Online softmax in fp32 with exp2 and a
+//               lazy per-head reference max (it moves only when a logit passes
+//               it by more than 2^8 in the exp2 domain, so P <= 256 stays in
+//               fp16 range and O is rarely rescaled)
+//   warps 4-11  dequantisers: a thread loads one row's half (four atoms of
+//               32 code bytes + 4 scale bytes) into registers a tile ahead;
+//               all eight warps convert one atom pair at a time, E2M1 x E4M3
+//               -> fp16 (exact), into the swizzled V tile
+//   warp 12     TMEM allocation; lane 0 issues every MMA
+//   warp 13     prefetcher: requests the selected rows of tiles 2, 3, ... (and
+//               the SWA window) into L2 up to 16 tiles ahead of the
+//               dequantisers, so that DRAM streams a chunk's rows while earlier
+//               tiles are computed
+//   warps 14-15 join the epilogue
+// (Two measured alternatives were slower: staging rows in shared memory, since
+// the tensor cores read their operands from shared memory and its bandwidth
+// bounds a tile; and one cp.async.bulk copy per 288-byte row, bounded by the
+// copy engine's per-request cost.)
+// The chunk's slot ids are read once at the start: the first kIdxCache into
+// shared memory, the validity of every slot into a bit mask.
+// SWA branch: the CTA of a query's last chunk also attends the query's sliding
+// window (E4M3 rows of the layer's SWA ring) as extra tiles after its selected
+// entries, in the same online softmax.
+// Epilogue: every warp reads one M-block x 32 channels of O^T from tensor
+// memory and writes the output ([head][channel] fp32), or the split partial
+// ([channel][head] fp16, so that a thread's heads are contiguous; the merge
+// kernel transposes).  (Merging the
+// splits of a query inside the kernel, as one thread-block cluster reading
+// its peers' partials through distributed shared memory, was measured no
+// faster than the merge kernel: the remote reads ran at a few bytes per
+// cycle per SM.)
+// Every mbarrier wait is bounded (about 2 s of %globaltimer): a wait that
+// gives up sets the timeout status bit and the CTA drains, frees its tensor
+// memory and exits.
 #include "csa2_internal.cuh"
 #include "tc_common.cuh"
 
@@ -35,62 +68,77 @@ namespace {
 
 using namespace tc;
 
-constexpr int kSoftWarps = 8;                  // warps 0-7 (warp 0 lane 0 also issues the MMAs)
-constexpr int kDeqWarp0 = 8;                   // warps 8-15
 constexpr int kThreadsTc = 16 * 32;
-constexpr int kTileE = 128;
-constexpr int kHN = 64;                        // MMA N: heads, zero-padded to 64
-constexpr int kIdxCache = 2048;                // slots of the CTA's chunk kept in smem
+constexpr int kTileE = 128;         // entries per tile
+constexpr int kHN = 64;             // heads, zero-padded to 64
+constexpr int kSoftWarps = 4;       // warps 0-3
+constexpr int kDeqWarp0 = 4;        // warps 4-11
+constexpr int kDeqWarps = 8;
+constexpr int kIssuerWarp = 12;
+constexpr int kPrefWarp = 13;
+constexpr int kAheadTiles = 16;     // tiles requested into L2 ahead of the dequantisers
+constexpr int kIdxCache = 2048;     // slot ids kept in shared memory
+constexpr int kMaxSlots = 16384;    // validity bits kept for a chunk
 
 struct TcLayout {
-  static constexpr uint32_t q_atom = kHN * 128;           // [8 atoms][64 rows][128 B]
-  static constexpr uint32_t q_off = 0;
-  static constexpr uint32_t v_atom = kTileE * 128;        // [8 atoms][128 rows][128 B]
-  static constexpr uint32_t v_off = q_off + 8 * q_atom;
-  static constexpr uint32_t p_off = v_off + 8 * v_atom;   // [128 rows][128 B] (MN-major B)
-  static constexpr uint32_t idx_off = p_off + kTileE * 128;
-  static constexpr uint32_t ctl_off = idx_off + kIdxCache * 4;
-  static constexpr uint32_t bytes = ctl_off + 4096;
+  static constexpr uint32_t q_atom = 64 * 128;            // [64 heads][128 B]
+  static constexpr uint32_t v_atom = kTileE * 128;        // [128 entries][128 B]
+  static constexpr uint32_t p_atom = 64 * 128;            // [64 heads][64 entries x 2 B]
+  static constexpr uint32_t q_off = 0;                    // 8 atoms
+  static constexpr uint32_t v_off = q_off + 8 * q_atom;   // 8 atoms
+  static constexpr uint32_t p_off = v_off + 8 * v_atom;   // 2 atoms
+  static constexpr uint32_t idx_off = p_off + 2 * p_atom;
+  static constexpr uint32_t mask_off = idx_off + kIdxCache * 4;
+  static constexpr uint32_t ctl_off = mask_off + kMaxSlots / 8;
+  static constexpr uint32_t bytes = ctl_off + 1024;
   static constexpr uint32_t alloc = bytes + 1024;         // slack to align the base to 1 KiB
 };
+static_assert(TcLayout::alloc <= 232448, "shared memory");
 
 struct TcCtl {
-  uint64_t bar_v[8];    // V atom a of the current tile written (4 dequant-warp arrivals)
-  uint64_t bar_s;       // S^T MMAs done (commit)
-  uint64_t bar_p;       // P written and O rescaled (8 softmax-warp arrivals)
-  uint64_t bar_o[4];    // O^T MMAs of M-block mb done (commit)
+  uint64_t v_ready[4];   // atoms 2p, 2p + 1 of the current V tile written (8 warps)
+  uint64_t s_full[2];    // S of a tile in S buffer (commit)
+  uint64_t o_blk[4];     // O^T(t) M-block p done: atoms 2p, 2p + 1 free (commit)
+  uint64_t p_half[2];    // P entries 64 j .. 64 j + 63 written (4 softmax warps)
   uint32_t tmem_base;
-  int32_t exceed[2];    // some logit of the tile passed its head's reference max (+ margin)
-  int32_t rescale;
-  float red[4][kHN];    // per entry-warp partial max / sum per head
-  float mref[kHN];      // reference max per head (raw logit units)
-  float alpha[kHN];     // rescale factor of the current tile per head
-  float linv[kHN];      // 1 / row sum per head (epilogue)
+  int32_t abort;         // a bounded wait gave up somewhere in the CTA
+  int32_t tiles_done;    // tiles the first dequantiser warp has written
+  float alpha[kHN];      // rescale factor of O^T per head (rare)
+  float linv[kHN];       // 1 / row sum per head (epilogue)
 };
-
-// Butterfly transpose-reduce of 32 values over the 32 lanes of a warp: lane l
-// ends up with element l reduced over all lanes.
-template <bool kMax>
-__device__ __forceinline__ float warp_reduce32(float* v) {
-  const int lane = threadIdx.x & 31;
-#pragma unroll
-  for (int o = 16; o >= 1; o >>= 1) {
-    const bool upper = (lane & o) != 0;
-#pragma unroll
-    for (int i = 0; i < 16; ++i) {
-      if (i < o) {
-        const float mine = upper ? v[i + o] : v[i];
-        const float send = upper ? v[i] : v[i + o];
-        const float other = __shfl_xor_sync(0xffffffffu, send, o);
-        v[i] = kMax ? fmaxf(mine, other) : mine + other;
-      }
-    }
-  }
-  return v[0];
-}
+static_assert(sizeof(TcCtl) <= 1024, "control block");
 
 __device__ __forceinline__ void softmax_bar() {
-  asm volatile("bar.sync 1, 256;" ::: "memory");
+  asm volatile("bar.sync 1, 128;" ::: "memory");
+}
+
+// Barrier of the softmax warps that also returns the OR of a predicate over
+// their threads: every warp takes the same decision.
+__device__ __forceinline__ bool softmax_bar_or(bool p) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\t"
+      "bar.red.or.pred q, 1, 128, p;\n\tselp.u32 %0, 1, 0, q;\n\t}"
+      : "=r"(r)
+      : "r"((uint32_t)p)
+      : "memory");
+  return r != 0;
+}
+
+// 16 TMEM columns of 16 lanes, twice: lanes 0-15 of the warp read lanes
+// base + l at columns [col, col + 16), lanes 16-31 read lanes base + l - 16 at
+// columns [col + 32, col + 48).
+__device__ __forceinline__ void tmem_ld16_pair32(uint32_t taddr, float* v) {
+  uint32_t r[16];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.16x32bx2.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,"
+      "%13,%14,%15}, [%16], 32;"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr));
+#pragma unroll
+  for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
 }
 
 __device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
@@ -99,18 +147,72 @@ __device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
   return r;
 }
 
-// SWA branch (swa_kv non-null): the CTA of the last chunk of query b also
-// attends the query's sliding window of the layer's SWA KV (E4M3 rows, per
-// sequence a ring with token t at row t mod swa_ring; window
-// max(0, pos - n_win + 1) .. pos) as extra tiles after its selected entries,
-// in the same online softmax; the split-k merge then combines everything
-// into one softmax over both sets.
+// Brings the lines holding row[0], row[128], ... (offsets below `bytes`)
+// into L2; every address it names lies inside the row.
+__device__ __forceinline__ void prefetch_l2(const uint8_t* row, int bytes) {
+  for (int off = 0; off < bytes; off += 128)
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(reinterpret_cast<const void*>(row + off)));
+}
+
+// The same bounded wait for every lane of a warp, with one answer for all of
+// them (the warp's later .sync.aligned instructions need every lane).
+__device__ __forceinline__ bool warp_wait(TcCtl& ctl, uint64_t* bar, uint32_t parity,
+                                          int32_t* status) {
+  bool ok = mbar_wait(su32(bar), parity, status);
+  ok = __all_sync(0xffffffffu, ok);
+  if (!ok) *reinterpret_cast<volatile int32_t*>(&ctl.abort) = 1;
+  return ok;
+}
+
+__device__ __forceinline__ bool aborted(TcCtl& ctl) {
+  return *reinterpret_cast<volatile int32_t*>(&ctl.abort) != 0;
+}
+
+// 32 bytes of read-only global data into two uint4: one 256-bit load when
+// the address is 32-byte aligned (fewer requests in flight per SM), two
+// 128-bit loads otherwise.
+__device__ __forceinline__ void ld32(const uint8_t* p, bool wide, uint4& lo, uint4& hi) {
+  if (wide) {
+    asm volatile("ld.global.nc.v8.u32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+                 : "=r"(lo.x), "=r"(lo.y), "=r"(lo.z), "=r"(lo.w), "=r"(hi.x), "=r"(hi.y),
+                   "=r"(hi.z), "=r"(hi.w)
+                 : "l"(p));
+  } else {
+    lo = __ldg(reinterpret_cast<const uint4*>(p));
+    hi = __ldg(reinterpret_cast<const uint4*>(p) + 1);
+  }
+}
+
+// 8 fp16 channels from 8 E2M1 codes (one 32-bit word) times a scale (f16x2).
+__device__ __forceinline__ uint4 dequant8(uint32_t w, __half2 sc) {
+  uint32_t o[4];
+#pragma unroll
+  for (int q4 = 0; q4 < 4; ++q4) {
+    uint32_t v2 = e2m1x2_to_f16x2((w >> (8 * q4)) & 0xFFu);
+    __half2 hv = __hmul2(*reinterpret_cast<__half2*>(&v2), sc);
+    o[q4] = *reinterpret_cast<uint32_t*>(&hv);
+  }
+  return make_uint4(o[0], o[1], o[2], o[3]);
+}
+
+// Byte offset of the 16-byte chunk ci (channels 8 ci .. 8 ci + 7 of atom a)
+// of row e in the V tile (K-major SW128 atoms of 128 rows).
+__device__ __forceinline__ uint32_t v_chunk_off(int a, int e, int ci) {
+  return (uint32_t)a * TcLayout::v_atom + (uint32_t)(e >> 3) * 1024u + (uint32_t)(e & 7) * 128u +
+         (uint32_t)((ci ^ (e & 7)) << 4);
+}
+
+// One atom of a row held by a dequantiser: 32 code bytes.
+struct Eighth {
+  uint4 cw[2];
+};
+
 template <int H>
 __global__ void __launch_bounds__(kThreadsTc, 1)
 sparse_attn_tc_kernel(const uint16_t* __restrict__ q_bf16, const uint8_t* __restrict__ kv_fp4,
                       int64_t N, int64_t kv_seq_stride, int q_per_seq,
                       const int32_t* __restrict__ idx, int k, int chunk, float scale_log2,
-                      float* __restrict__ out, float* __restrict__ lse, float* __restrict__ part_o,
+                      float* __restrict__ out, float* __restrict__ lse, __half* __restrict__ part_o,
                       float* __restrict__ part_lse, int32_t* status,
                       const uint8_t* __restrict__ swa_kv, int64_t swa_ring, int n_win,
                       const int32_t* __restrict__ q_pos, int32_t* __restrict__ idx_copy) {
@@ -122,6 +224,7 @@ sparse_attn_tc_kernel(const uint16_t* __restrict__ q_bf16, const uint8_t* __rest
   const uint32_t sbase = raw_s + pad;
   TcCtl& ctl = *reinterpret_cast<TcCtl*>(smem + L::ctl_off);
   int32_t* idx_s = reinterpret_cast<int32_t*>(smem + L::idx_off);
+  uint32_t* mask_s = reinterpret_cast<uint32_t*>(smem + L::mask_off);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int b = blockIdx.y, split = blockIdx.x, nsplit = gridDim.x;
@@ -142,13 +245,11 @@ sparse_attn_tc_kernel(const uint16_t* __restrict__ q_bf16, const uint8_t* __rest
   const int32_t* slots = idx + (int64_t)b * k + s0;
   const uint8_t* kvseq = kv_fp4 + (int64_t)(b / q_per_seq) * kv_seq_stride * kRowBytes;
   const uint32_t q_s = sbase + L::q_off, v_s = sbase + L::v_off, p_s = sbase + L::p_off;
-  // slot s of this chunk (s < cnt): entry id, -1 if empty
-  auto slot_at = [&](int s) -> int32_t { return s < kIdxCache ? idx_s[s] : slots[s]; };
 
   pdl_trigger();
   // ---- prologue: Q (bf16 -> fp16, swizzled, zero-padded to 64 rows), TMEM,
-  //      barriers; then (once the kernel that selected them has finished) the
-  //      slot indices ----
+  //      barriers; the slot ids are read only after the kernel that selected
+  //      them has finished ----
   {
     constexpr int kQChunks = kHN * (kD / 8);
     constexpr int kPer = (kQChunks + kThreadsTc - 1) / kThreadsTc;
@@ -175,26 +276,47 @@ sparse_attn_tc_kernel(const uint16_t* __restrict__ q_bf16, const uint8_t* __rest
       }
     }
   }
-  if (warp == 0) {
+  if (warp == kIssuerWarp) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], 512;" ::"r"(
         su32(&ctl.tmem_base)));
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
   }
   if (tid == 0) {
-    for (int a = 0; a < 8; ++a) mbar_init(su32(&ctl.bar_v[a]), 4);
-    mbar_init(su32(&ctl.bar_s), 1);
-    mbar_init(su32(&ctl.bar_p), kSoftWarps);
-    for (int mb = 0; mb < 4; ++mb) mbar_init(su32(&ctl.bar_o[mb]), 1);
+    for (int i = 0; i < 4; ++i) {
+      mbar_init(su32(&ctl.v_ready[i]), kDeqWarps);
+      mbar_init(su32(&ctl.o_blk[i]), 1);
+    }
+    for (int i = 0; i < 2; ++i) mbar_init(su32(&ctl.s_full[i]), 1);
+    for (int i = 0; i < 2; ++i) mbar_init(su32(&ctl.p_half[i]), kSoftWarps);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-    ctl.exceed[0] = ctl.exceed[1] = 0;
-    ctl.rescale = 0;
+    ctl.abort = 0;
+    ctl.tiles_done = 0;
   }
-  if (tid < kHN) ctl.mref[tid] = -INFINITY;
   pdl_wait();
-  for (int i = tid; i < min(cnt, kIdxCache); i += kThreadsTc) idx_s[i] = slots[i];
-  if (idx_copy) {  // the caller's copy of the slots this CTA reads
-    int32_t* dst = idx_copy + (int64_t)b * k + s0;
-    for (int i = tid; i < cnt; i += kThreadsTc) dst[i] = slots[i];
+  // ---- the chunk's slot ids (all threads): bad ids raise the status bit, the
+  //      Reuse layers' copy of the slots is written, the first kIdxCache ids
+  //      are kept in shared memory and every slot's validity in a bit mask ----
+  {
+    constexpr int kUnroll = kIdxCache / kThreadsTc;
+    for (int base = 0; base < cnt; base += kUnroll * kThreadsTc) {
+      int32_t j[kUnroll];
+#pragma unroll
+      for (int i = 0; i < kUnroll; ++i) {
+        const int s = base + i * kThreadsTc + tid;
+        j[i] = s < cnt ? slots[s] : -1;
+      }
+#pragma unroll
+      for (int i = 0; i < kUnroll; ++i) {
+        const int s = base + i * kThreadsTc + tid;
+        if (s < cnt) {
+          if (j[i] >= N || j[i] < -1) set_status(status, kStatusBadIndex);
+          if (idx_copy) idx_copy[(int64_t)b * k + s0 + s] = j[i];
+          if (s < kIdxCache) idx_s[s] = j[i];
+        }
+        const uint32_t m = __ballot_sync(0xffffffffu, s < cnt && j[i] >= 0 && j[i] < N);
+        if (lane == 0 && s < cnt) mask_s[s >> 5] = m;
+      }
+    }
   }
   proxy_fence();
   tc_fence_before();
@@ -202,322 +324,400 @@ sparse_attn_tc_kernel(const uint16_t* __restrict__ q_bf16, const uint8_t* __rest
   tc_fence_after();
   const uint32_t tmem = ctl.tmem_base;
   const uint32_t tm_o = tmem;          // columns [0, 256): 4 M-blocks x 64 heads
-  const uint32_t tm_s = tmem + 256;    // columns [256, 320)
+  const uint32_t tm_s = tmem + 256;    // columns [256, 512): 2 S buffers x 128 entries
+  auto slot_id = [&](int s) -> int32_t { return s < kIdxCache ? idx_s[s] : slots[s]; };
+  auto slot_ok = [&](int s) -> bool { return (mask_s[s >> 5] >> (s & 31)) & 1u; };
+  bool alive = true;
 
-  if (warp >= kDeqWarp0) {
-    // ================= dequantisers =================
-    const int dt = tid - kDeqWarp0 * 32;
-    const int e = dt & 127, half = dt >> 7;
-    uint4 raw[9];
-    auto load_row = [&](int t, uint4* r) {
-      const int s = t * kTileE + e;
-      const int32_t j = (s < cnt) ? slot_at(s) : -1;
-      const bool ok = (j >= 0) && (j < N);
-      if (half == 0 && (j >= N || j < -1)) set_status(status, kStatusBadIndex);
-      if (ok) {
-        const uint4* src = reinterpret_cast<const uint4*>(kvseq + (int64_t)j * kRowBytes);
-#pragma unroll
-        for (int i = 0; i < 8; ++i) r[i] = __ldg(src + half * 8 + i);
-        r[8] = __ldg(src + 16 + half);
-      } else {
-#pragma unroll
-        for (int i = 0; i < 9; ++i) r[i] = make_uint4(0, 0, 0, 0);
-      }
-    };
-    // this thread's 256 bytes of window row sw*128 + e (tile sw of the window)
-    auto swa_row = [&](int sw) -> const uint4* {
-      const int sl = sw * kTileE + e;
-      return sl < wcnt ? reinterpret_cast<const uint4*>(swaseq + ((w0 + sl) % swa_ring) * kD) +
-                             16 * half
-                       : nullptr;
-    };
-    if (nmain > 0) load_row(0, raw);
-    bool alive = true;
-    for (int t = 0; t < ntiles && alive; ++t) {
-      if (t >= nmain) {
-        // ---- a tile of the SWA window: E4M3 -> fp16 (exact), two atoms per load ----
-        const uint4* src = swa_row(t - nmain);
-        if (t + 1 < ntiles)
-          if (const uint4* nx = swa_row(t + 1 - nmain))
-            for (int i = 0; i < 2; ++i) asm volatile("prefetch.global.L2 [%0];" ::"l"(nx + 8 * i));
-#pragma unroll 1
-        for (int ap = 0; ap < 2 && alive; ++ap) {
-          uint4 wv[8];
-#pragma unroll
-          for (int i = 0; i < 8; ++i) wv[i] = src ? __ldg(src + 8 * ap + i) : make_uint4(0, 0, 0, 0);
-#pragma unroll
-          for (int aj = 0; aj < 2; ++aj) {
-            const int ai = 2 * ap + aj;
-            const int a = half * 4 + ai;
-            if (t > 0 && aj == 0 && !mbar_wait(su32(&ctl.bar_o[a >> 1]), (t - 1) & 1, status)) {
-              alive = false;
-              break;
-            }
-#pragma unroll
-            for (int ci = 0; ci < 8; ++ci) {
-              // channels 8 ci .. 8 ci + 7 of atom a: bytes 8 (ci & 1) .. of wv[4 aj + ci / 2]
-              const uint4 u = wv[4 * aj + (ci >> 1)];
-              const uint32_t lo = (ci & 1) ? u.z : u.x, hi = (ci & 1) ? u.w : u.y;
-              const uint32_t off = L::v_off + (uint32_t)a * L::v_atom +
-                                   (uint32_t)(e >> 3) * 1024u + (uint32_t)(e & 7) * 128u +
-                                   (uint32_t)((ci ^ (e & 7)) << 4);
-              *reinterpret_cast<uint4*>(smem + off) =
-                  make_uint4(e4m3x2_to_f16x2((uint16_t)(lo & 0xFFFFu)),
-                             e4m3x2_to_f16x2((uint16_t)(lo >> 16)),
-                             e4m3x2_to_f16x2((uint16_t)(hi & 0xFFFFu)),
-                             e4m3x2_to_f16x2((uint16_t)(hi >> 16)));
-            }
-            proxy_fence();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(su32(&ctl.bar_v[a]));
-          }
-        }
+  if (warp == kPrefWarp) {
+    // ================= prefetcher =================
+    // the window rows first (small), then tile t's 128 rows (four per lane)
+    // once the dequantisers have written fewer than kAheadTiles tiles before it
+    for (int r = lane; r < wcnt; r += 32)
+      prefetch_l2(swaseq + ((w0 + r) % swa_ring) * kD, kD);
+    uint64_t t_idle = 0;
+    for (int t = 2; t < nmain && !aborted(ctl);) {  // the dequantisers load tiles 0, 1 themselves
+      const int done = *reinterpret_cast<volatile int32_t*>(&ctl.tiles_done);
+      if (t >= done + kAheadTiles) {
+        if (t_idle == 0) t_idle = globaltimer();
+        if (globaltimer() - t_idle > kWaitLimitNs) break;  // the consumer has stopped
+        __nanosleep(256);
         continue;
       }
-      uint4 nxt[9];
-      if (t + 1 < nmain) {
-        load_row(t + 1, nxt);
-      } else {
-        if (t + 1 < ntiles)  // the window follows: bring its rows into L2 meanwhile
-          if (const uint4* nx = swa_row(0))
-            for (int i = 0; i < 2; ++i) asm volatile("prefetch.global.L2 [%0];" ::"l"(nx + 8 * i));
+      t_idle = 0;
 #pragma unroll
-        for (int i = 0; i < 9; ++i) nxt[i] = make_uint4(0, 0, 0, 0);
+      for (int i = 0; i < kTileE / 32; ++i) {
+        const int s = t * kTileE + lane + 32 * i;
+        if (s < cnt && slot_ok(s)) prefetch_l2(kvseq + (int64_t)slot_id(s) * kRowBytes, kRowBytes);
       }
-      const uint32_t sc_words[4] = {raw[8].x, raw[8].y, raw[8].z, raw[8].w};
+      ++t;
+    }
+  } else if (warp >= kDeqWarp0 && warp < kDeqWarp0 + kDeqWarps) {
+    // ================= dequantisers =================
+    // Atom pairs in order; for pair p a thread converts row e, atom 2 p + ah
+    // (32 code bytes + 4 scale bytes), so all eight warps finish a pair
+    // together and S can start on it while the next pair is converted.
+    const int dt = tid - kDeqWarp0 * 32;  // 0..255
+    const int e = dt & 127, ah = dt >> 7;
+    // 256-bit loads need a 32-byte aligned cache (rows are 288 = 9 x 32 bytes)
+    const bool wide = (reinterpret_cast<uintptr_t>(kv_fp4) & 31u) == 0;
+    // this thread's row of tile t: its source, or null past the chunk / for an empty slot
+    auto row_src = [&](int t) -> const uint8_t* {
+      const int s = t * kTileE + e;
+      return (t < nmain && s < cnt && slot_ok(s)) ? kvseq + (int64_t)slot_id(s) * kRowBytes
+                                                  : nullptr;
+    };
+    // atom 2 p + ah (channels 64 a .. +64: code bytes 32 a ..) of a row
+    auto load_atom = [&](const uint8_t* src, int p, Eighth& q) {
+      if (src) {
+        ld32(src + 32 * (2 * p + ah), wide, q.cw[0], q.cw[1]);
+      } else {
+        q.cw[0] = q.cw[1] = make_uint4(0, 0, 0, 0);
+      }
+    };
+    // the row's 32 scale bytes (block b = channels 16 b .. +16)
+    auto load_scales = [&](const uint8_t* src, uint4& s_lo, uint4& s_hi) {
+      if (src) {
+        ld32(src + kCodeBytes, wide, s_lo, s_hi);
+      } else {
+        s_lo = s_hi = make_uint4(0, 0, 0, 0);
+      }
+    };
+    uint8_t* vt = smem + L::v_off;
+    Eighth cur[4];  // this thread's row of the current tile, one atom per pair
+    uint4 sc_lo, sc_hi;
+    {
+      const uint8_t* src = row_src(0);
+      load_scales(src, sc_lo, sc_hi);
 #pragma unroll
-      for (int ai = 0; ai < 4; ++ai) {
-        const int a = half * 4 + ai;
-        // atom a feeds the O^T M-block a / 2 of the previous tile
-        if (t > 0 && (ai & 1) == 0 && !mbar_wait(su32(&ctl.bar_o[a >> 1]), (t - 1) & 1, status)) {
+      for (int p = 0; p < 4; ++p) load_atom(src, p, cur[p]);
+    }
+    for (int t = 0; t < ntiles && alive; ++t) {
+      // the next tile's row: its scales now, pair p once pair p of this tile is stored
+      const uint8_t* nsrc = row_src(t + 1);
+      uint4 nsc_lo, nsc_hi;
+      load_scales(nsrc, nsc_lo, nsc_hi);
+      Eighth nxt[4];
+#pragma unroll
+      for (int p = 0; p < 4; ++p) {
+        if (!alive) break;
+        const int a = 2 * p + ah;
+        // atoms 2p, 2p + 1 are free once O^T(t - 1) M-block p has read them
+        if (t >= 1 && !warp_wait(ctl, &ctl.o_blk[p], (uint32_t)(t - 1) & 1u, status)) {
           alive = false;
           break;
         }
-        const uint32_t cw[8] = {raw[2 * ai].x,     raw[2 * ai].y,     raw[2 * ai].z,
-                                raw[2 * ai].w,     raw[2 * ai + 1].x, raw[2 * ai + 1].y,
-                                raw[2 * ai + 1].z, raw[2 * ai + 1].w};
+        if (t < nmain) {
+          // word w of code vector u: channels 64 a + 32 u + 8 w .. +8, scale
+          // byte 4 a + 2 u + w / 2, 16-byte chunk 4 u + w of atom a
+          const uint32_t scw[8] = {sc_lo.x, sc_lo.y, sc_lo.z, sc_lo.w,
+                                   sc_hi.x, sc_hi.y, sc_hi.z, sc_hi.w};
 #pragma unroll
-        for (int ci = 0; ci < 8; ++ci) {
-          // 8 channels (8 ci .. 8 ci + 7 of atom a) = 4 code bytes; scale of block 2 ai + ci / 2
-          const uint32_t sb = (sc_words[ai] >> (8 * (ci >> 1))) & 0xFFu;
-          const uint32_t s2 = e4m3x2_to_f16x2((uint16_t)(sb | (sb << 8)));
-          const __half2 sc = *reinterpret_cast<const __half2*>(&s2);
-          uint32_t o[4];
-#pragma unroll
-          for (int q4 = 0; q4 < 4; ++q4) {
-            uint32_t v2 = e2m1x2_to_f16x2((cw[ci] >> (8 * q4)) & 0xFFu);
-            __half2 hv = __hmul2(*reinterpret_cast<__half2*>(&v2), sc);
-            o[q4] = *reinterpret_cast<uint32_t*>(&hv);
+          for (int u = 0; u < 2; ++u) {
+            const uint32_t sword = ah ? scw[2 * p + 1] : scw[2 * p];  // scale bytes 4 a .. 4 a + 3
+            const uint32_t sbytes = (sword >> (16 * u)) & 0xFFFFu;
+            const uint32_t s_lo = e4m3x2_to_f16x2((uint16_t)((sbytes & 0xFFu) * 0x101u));
+            const uint32_t s_hi = e4m3x2_to_f16x2((uint16_t)((sbytes >> 8) * 0x101u));
+            const __half2 h_lo = *reinterpret_cast<const __half2*>(&s_lo);
+            const __half2 h_hi = *reinterpret_cast<const __half2*>(&s_hi);
+            const uint4 w = cur[p].cw[u];
+            *reinterpret_cast<uint4*>(vt + v_chunk_off(a, e, 4 * u + 0)) = dequant8(w.x, h_lo);
+            *reinterpret_cast<uint4*>(vt + v_chunk_off(a, e, 4 * u + 1)) = dequant8(w.y, h_lo);
+            *reinterpret_cast<uint4*>(vt + v_chunk_off(a, e, 4 * u + 2)) = dequant8(w.z, h_hi);
+            *reinterpret_cast<uint4*>(vt + v_chunk_off(a, e, 4 * u + 3)) = dequant8(w.w, h_hi);
           }
-          const uint32_t off = L::v_off + (uint32_t)a * L::v_atom + (uint32_t)(e >> 3) * 1024u +
-                               (uint32_t)(e & 7) * 128u + (uint32_t)((ci ^ (e & 7)) << 4);
-          *reinterpret_cast<uint4*>(smem + off) = make_uint4(o[0], o[1], o[2], o[3]);
+        } else {
+          // a tile of the SWA window: E4M3 row from global (in L2), -> fp16 (exact)
+          const int sl = (t - nmain) * kTileE + e;
+          uint4 wv[4];
+          if (sl < wcnt) {
+            const uint4* src =
+                reinterpret_cast<const uint4*>(swaseq + ((w0 + sl) % swa_ring) * kD) + 4 * a;
+#pragma unroll
+            for (int i = 0; i < 4; ++i) wv[i] = __ldg(src + i);
+          } else {
+#pragma unroll
+            for (int i = 0; i < 4; ++i) wv[i] = make_uint4(0, 0, 0, 0);
+          }
+#pragma unroll
+          for (int ci = 0; ci < 8; ++ci) {
+            // channels 8 ci .. 8 ci + 7 of atom a: bytes 8 (ci & 1) .. of wv[ci / 2]
+            const uint4 u = wv[ci >> 1];
+            const uint32_t lo = (ci & 1) ? u.z : u.x, hi = (ci & 1) ? u.w : u.y;
+            *reinterpret_cast<uint4*>(vt + v_chunk_off(a, e, ci)) =
+                make_uint4(e4m3x2_to_f16x2((uint16_t)(lo & 0xFFFFu)),
+                           e4m3x2_to_f16x2((uint16_t)(lo >> 16)),
+                           e4m3x2_to_f16x2((uint16_t)(hi & 0xFFFFu)),
+                           e4m3x2_to_f16x2((uint16_t)(hi >> 16)));
+          }
         }
-        proxy_fence();
+        proxy_fence();  // the tensor cores read V through the async proxy
         __syncwarp();
-        if (lane == 0) mbar_arrive(su32(&ctl.bar_v[a]));
+        if (lane == 0) mbar_arrive(su32(&ctl.v_ready[p]));
+        load_atom(nsrc, p, nxt[p]);
       }
+      if (warp == kDeqWarp0 && lane == 0)
+        *reinterpret_cast<volatile int32_t*>(&ctl.tiles_done) = t + 1;
 #pragma unroll
-      for (int i = 0; i < 9; ++i) raw[i] = nxt[i];
+      for (int p = 0; p < 4; ++p) cur[p] = nxt[p];
+      sc_lo = nsc_lo;
+      sc_hi = nsc_hi;
     }
-  } else {
-    // ================= softmax (warps 0-7) =================
-    // thread = TMEM lane = entry e of the tile; warp w covers heads 32 (w / 4) .. +32
-    const int e = (warp & 3) * 32 + lane;
-    const int hh = warp >> 2;
-    const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
-    const float c = scale_log2;
-    const float tau_raw = 8.0f / c;  // lazy-rescale margin in raw logit units
-    float m_own = -INFINITY;         // reference max of head tid (tid < 64)
-    float l_part[32];                // this thread's share of the row sums of its 32 heads
+  } else if (warp == kIssuerWarp) {
+    // ================= MMA issuer =================
+    if (lane == 0 && ntiles > 0) {
+      // S: A = Q (K-major, 64 rows), B = V (K-major, 128 rows).  O^T: A = V
+      // (MN-major: channels), B = P (K-major, 64 head rows).  Each MMA adds a
+      // compile-time offset (16-byte units) to a base descriptor.
+      const uint32_t id_s = (1u << 4) | ((uint32_t)(kTileE >> 3) << 17) | ((64u >> 4) << 24);
+      const uint32_t id_o =
+          (1u << 4) | ((uint32_t)(kHN >> 3) << 17) | ((128u >> 4) << 24) | (1u << 15);
+      const uint64_t dS_a = sw128_desc(q_s, 16, 1024);
+      const uint64_t dS_b = sw128_desc(v_s, 16, 1024);
+      const uint64_t dO_a = sw128_desc(v_s, L::v_atom, 1024);
+      const uint64_t dO_b = sw128_desc(p_s, 16, 1024);
+      uint64_t* last = nullptr;  // barrier of the last commit, and its phase parity
+      uint32_t last_par = 0;
+      bool ok = true;
+      for (int t = 0; t < ntiles && ok; ++t) {
+        const uint32_t d_s = tm_s + (uint32_t)(t & 1) * kTileE;
+        // S(t), atom pair by atom pair as the dequantisers finish them
 #pragma unroll
-    for (int i = 0; i < 32; ++i) l_part[i] = 0.0f;
-    // S^T: A = V (K-major), B = Q (K-major).  O^T: A = V (MN-major), B = P (MN-major).
-    const uint32_t id_s = (1u << 4) | ((uint32_t)(kHN >> 3) << 17) | ((128u >> 4) << 24);
-    const uint32_t id_o = id_s | (1u << 15) | (1u << 16);
-    // Base descriptors; each MMA only adds a compile-time offset (in 16-byte
-    // units) to the start-address field, so issuing costs a few instructions.
-    const uint64_t dS_a = sw128_desc(v_s, 16, 1024);
-    const uint64_t dS_b = sw128_desc(q_s, 16, 1024);
-    const uint64_t dO_a = sw128_desc(v_s, L::v_atom, 1024);
-    const uint64_t dO_b = sw128_desc(p_s, L::v_atom, 1024);
-    const bool issuer = (tid == 0);
-    bool alive = true;
-    for (int t = 0; t < ntiles && alive; ++t) {
-      if (issuer) {
-        // S^T(t) over the 8 channel atoms as the dequantisers finish them
-#pragma unroll
-        for (int a = 0; a < 8; ++a) {
-          if (!alive) break;
-          if (!mbar_wait(su32(&ctl.bar_v[a]), t & 1, status)) {
-            alive = false;
+        for (int p = 0; p < 4; ++p) {
+          if (!mbar_wait(su32(&ctl.v_ready[p]), (uint32_t)t & 1u, status)) {
+            ok = false;
             break;
           }
           tc_fence_after();
 #pragma unroll
-          for (int jj = 0; jj < 4; ++jj)
-            mma_f16(tm_s, dS_a + ((a * L::v_atom + jj * 32) >> 4),
-                    dS_b + ((a * L::q_atom + jj * 32) >> 4), id_s, (a | jj) != 0 ? 1u : 0u);
-        }
-        if (alive) mma_commit(su32(&ctl.bar_s));
-      }
-      __syncwarp();
-      if (!mbar_wait(su32(&ctl.bar_s), t & 1, status)) {
-        alive = false;
-        break;
-      }
-      tc_fence_after();
-      float s[32];
-      tmem_ld16(tm_s + lane_base + hh * 32, s);
-      tmem_ld16(tm_s + lane_base + hh * 32 + 16, s + 16);
-      tmem_wait_ld();
-      {
-        const int sl = t * kTileE + e;
-        bool valid;
-        if (t < nmain) {
-          const int32_t j = sl < cnt ? slot_at(sl) : -1;
-          valid = j >= 0 && j < N;
-        } else {
-          valid = (t - nmain) * kTileE + e < wcnt;  // a window row
-        }
-        if (!valid) {
+          for (int a = 2 * p; a < 2 * p + 2; ++a)
 #pragma unroll
-          for (int i = 0; i < 32; ++i) s[i] = -INFINITY;
+            for (int jj = 0; jj < 4; ++jj)
+              mma_f16(d_s, dS_a + ((a * L::q_atom + jj * 32) >> 4),
+                      dS_b + ((a * L::v_atom + jj * 32) >> 4), id_s, (a | jj) != 0 ? 1u : 0u);
         }
-      }
-      // does any logit pass its head's reference max by more than the margin?
-      bool ex = false;
+        if (!ok) break;
+        mma_commit(su32(&ctl.s_full[t & 1]));
+        last = &ctl.s_full[t & 1];
+        last_par = ((uint32_t)t >> 1) & 1u;
+        // O^T(t): entries 0-63 once their P is written (the softmax is
+        // still on entries 64-127), then entries 64-127 M-block by M-block, so
+        // that M-block p's atoms are freed as early as possible
 #pragma unroll
-      for (int i = 0; i < 32; ++i) ex |= s[i] > ctl.mref[hh * 32 + i] + tau_raw;
-      if (__any_sync(0xffffffffu, ex) && lane == 0) ctl.exceed[t & 1] = 1;
-      softmax_bar();
-      if (tid == 0) ctl.exceed[(t + 1) & 1] = 0;  // every thread has read the previous tile's flag
-      if (ctl.exceed[t & 1]) {
-        // exact tile max per head, new reference where it moved past the margin
-        float v[32];
-#pragma unroll
-        for (int i = 0; i < 32; ++i) v[i] = s[i];
-        ctl.red[warp & 3][hh * 32 + lane] = warp_reduce32<true>(v);
-        softmax_bar();
-        if (tid < kHN) {
-          const float mt = fmaxf(fmaxf(ctl.red[0][tid], ctl.red[1][tid]),
-                                 fmaxf(ctl.red[2][tid], ctl.red[3][tid]));
-          float a = 1.0f;
-          if (mt > m_own + tau_raw) {
-            a = exp2f((m_own - mt) * c);  // 0 while m_own = -inf
-            m_own = mt;
-            if (t > 0) ctl.rescale = 1;
+        for (int hf = 0; hf < 2; ++hf) {
+          if (!mbar_wait(su32(&ctl.p_half[hf]), (uint32_t)t & 1u, status)) {
+            ok = false;
+            break;
           }
-          ctl.mref[tid] = m_own;
-          ctl.alpha[tid] = a;
-        }
-        softmax_bar();
-        if (ctl.rescale) {
+          tc_fence_after();
 #pragma unroll
-          for (int i = 0; i < 32; ++i) l_part[i] *= ctl.alpha[hh * 32 + i];
-          // every earlier O^T MMA is complete: this tile's S^T was issued after them
-#pragma unroll 1
           for (int mb = 0; mb < 4; ++mb) {
-#pragma unroll 1
-            for (int c16 = 0; c16 < 2; ++c16) {
-              float o16[16];
-              const uint32_t ta = tm_o + lane_base + mb * kHN + hh * 32 + c16 * 16;
-              tmem_ld16(ta, o16);
-              tmem_wait_ld();
 #pragma unroll
-              for (int i = 0; i < 16; ++i) o16[i] *= ctl.alpha[hh * 32 + c16 * 16 + i];
-              tmem_st16(ta, o16);
-            }
+            for (int kk = 4 * hf; kk < 4 * hf + 4; ++kk)
+              // A = V^T channels 128 mb .. +128 x entries 16 kk .. +16;
+              // B = P heads x entries 16 kk .. +16 (atom kk / 4)
+              mma_f16(tm_o + mb * kHN, dO_a + ((2 * mb * L::v_atom + kk * 2048) >> 4),
+                      dO_b + (((kk >> 2) * L::p_atom + (kk & 3) * 32) >> 4), id_o,
+                      (t > 0 || kk > 0) ? 1u : 0u);
+            if (hf == 1) mma_commit(su32(&ctl.o_blk[mb]));
+          }
+        }
+        if (!ok) break;
+        last = &ctl.o_blk[3];
+        last_par = (uint32_t)t & 1u;
+      }
+      if (!ok) *reinterpret_cast<volatile int32_t*>(&ctl.abort) = 1;
+      // the MMAs complete in order: once the last commit has arrived none is
+      // in flight, whatever the other roles did (tensor memory is freed below)
+      if (last) mbar_wait(su32(last), last_par, status);
+    }
+    __syncwarp();
+  } else if (warp < kSoftWarps) {
+    // ================= softmax (warps 0-3) =================
+    // lane l of warp q: head 16 q + l % 16; entries col0 + 32 (l / 16) + 0..15
+    // for col0 in {0, 16, 64, 80}
+    const int qd = warp, h = qd * 16 + (lane & 15), hs = lane >> 4;
+    const uint32_t lane_base = (uint32_t)(qd * 32) << 16;
+    const float c = scale_log2;
+    const float tau_raw = 8.0f / c;  // lazy-rescale margin in raw logit units
+    float m_ref = -INFINITY;         // reference max of head h (raw logit units)
+    float l_acc = 0.0f;              // this thread's share of head h's row sum
+    for (int t = 0; t < ntiles; ++t) {
+      const int sb = t & 1;
+      // validity of this thread's 64 entries of the tile (bit i: entry i of the thread)
+      uint64_t vmask = 0;
+#pragma unroll
+      for (int bi = 0; bi < 4; ++bi) {
+        const int col0 = (bi < 2 ? 16 * bi : 64 + 16 * (bi - 2)) + 32 * hs;
+        uint32_t m16;
+        if (t < nmain) {
+          const int sbase_i = t * kTileE + col0;  // a multiple of 16
+          m16 = sbase_i < cnt ? (mask_s[sbase_i >> 5] >> (sbase_i & 31)) & 0xFFFFu : 0u;
+        } else {
+          const int wr = (t - nmain) * kTileE + col0;  // window rows wr .. wr + 15
+          const int nv = min(16, max(0, wcnt - wr));
+          m16 = nv >= 16 ? 0xFFFFu : ((1u << nv) - 1u);
+        }
+        vmask |= (uint64_t)m16 << (16 * bi);
+      }
+      if (!warp_wait(ctl, &ctl.s_full[sb], ((uint32_t)t >> 1) & 1u, status)) alive = false;
+      float s[64];
+      if (alive) {
+        tc_fence_after();
+        const uint32_t ta = tm_s + sb * kTileE + lane_base;
+        tmem_ld16_pair32(ta + 0, s);
+        tmem_ld16_pair32(ta + 16, s + 16);
+        tmem_ld16_pair32(ta + 64, s + 32);
+        tmem_ld16_pair32(ta + 80, s + 48);
+        tmem_wait_ld();
+      }
+      if (!alive || vmask != ~0ull) {
+#pragma unroll
+        for (int i = 0; i < 64; ++i)
+          if (!alive || !((vmask >> i) & 1u)) s[i] = -INFINITY;
+      }
+      float mx4[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) mx4[j] = s[j];
+#pragma unroll
+      for (int i = 4; i < 64; ++i) mx4[i & 3] = fmaxf(mx4[i & 3], s[i]);
+      float mx = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3]));
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+      // a new reference max for this head when the tile's max passes it by
+      // more than the margin; O^T's column needs rescaling only if the head
+      // already has a contribution
+      float alpha = 1.0f;
+      bool resc = false;
+      if (mx > m_ref + tau_raw) {
+        resc = m_ref != -INFINITY;
+        alpha = resc ? exp2f((m_ref - mx) * c) : 0.0f;
+        m_ref = mx;
+      }
+      l_acc *= alpha;
+      if (softmax_bar_or(resc || aborted(ctl))) {
+        if (softmax_bar_or(aborted(ctl))) {  // every softmax warp leaves together
+          alive = false;
+          break;
+        }
+        if (lane < 16) ctl.alpha[h] = resc ? alpha : 1.0f;
+        softmax_bar();
+        // O^T(t - 1), the last product into O, must be complete; O^T rows are
+        // channels: this warp rescales all 256 columns of its quadrant's lanes
+        if (warp_wait(ctl, &ctl.o_blk[3], (uint32_t)(t - 1) & 1u, status)) {
+          tc_fence_after();
+#pragma unroll 1
+          for (int c4 = 0; c4 < 64; ++c4) {
+            uint32_t o4[4];
+            const uint32_t ta = tm_o + lane_base + c4 * 4;
+            asm volatile("tcgen05.ld.sync.aligned.32x32b.x4.b32 {%0,%1,%2,%3}, [%4];"
+                         : "=r"(o4[0]), "=r"(o4[1]), "=r"(o4[2]), "=r"(o4[3])
+                         : "r"(ta));
+            tmem_wait_ld();
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+              o4[i] = __float_as_uint(__uint_as_float(o4[i]) * ctl.alpha[(c4 & 15) * 4 + i]);
+            asm volatile("tcgen05.st.sync.aligned.32x32b.x4.b32 [%0], {%1,%2,%3,%4};" ::"r"(ta),
+                         "r"(o4[0]), "r"(o4[1]), "r"(o4[2]), "r"(o4[3])
+                         : "memory");
           }
           tmem_wait_st();
         }
-        softmax_bar();
-        if (tid == 0) ctl.rescale = 0;
       }
-      // P = exp2(c s - c m_ref), fp16, into row e of the MN-major P tile
-      uint32_t pk[16];
+      // P is free once O^T(t - 1) has read it
+      if (t > 0 && !warp_wait(ctl, &ctl.o_blk[3], (uint32_t)(t - 1) & 1u, status)) alive = false;
+      // P = exp2(c s - c m_ref), fp16, into row h of the K-major P tile
+      const float mneg = m_ref == -INFINITY ? 0.0f : -m_ref * c;
+      float lsum[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+      // blocks 0, 1 hold entries 0-63 (P atom 0), blocks 2, 3 entries 64-127
 #pragma unroll
-      for (int i = 0; i < 32; i += 2) {
-        const float m0 = ctl.mref[hh * 32 + i], m1 = ctl.mref[hh * 32 + i + 1];
-        const float p0 = exp2f(fmaf(s[i], c, m0 == -INFINITY ? 0.0f : -m0 * c));
-        const float p1 = exp2f(fmaf(s[i + 1], c, m1 == -INFINITY ? 0.0f : -m1 * c));
-        l_part[i] += p0;
-        l_part[i + 1] += p1;
-        pk[i >> 1] = pack_f16x2(p0, p1);
-      }
+      for (int bi = 0; bi < 4; ++bi) {
+        const int col0 = (bi < 2 ? 16 * bi : 64 + 16 * (bi - 2)) + 32 * hs;  // first entry
+        uint32_t pk[8];
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const int chunk = hh * 4 + j;  // heads 8 chunk .. +8
-        const uint32_t off = L::p_off + (uint32_t)(e >> 3) * 1024u + (uint32_t)(e & 7) * 128u +
-                             (uint32_t)((chunk ^ (e & 7)) << 4);
-        *reinterpret_cast<uint4*>(smem + off) =
-            make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
-      }
-      proxy_fence();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(su32(&ctl.bar_p));
-      if (issuer) {
-        // O^T(t) once every softmax warp has written its part of P
-        if (!mbar_wait(su32(&ctl.bar_p), t & 1, status)) {
-          alive = false;
-        } else {
-          tc_fence_after();
-          const uint32_t acc0 = t > 0 ? 1u : 0u;
+        for (int i = 0; i < 16; i += 2) {
+          const float p0 = exp2f(fmaf(s[16 * bi + i], c, mneg));
+          const float p1 = exp2f(fmaf(s[16 * bi + i + 1], c, mneg));
+          lsum[(i >> 1) & 3] += p0 + p1;
+          pk[i >> 1] = pack_f16x2(p0, p1);
+        }
+        if (alive) {
 #pragma unroll
-          for (int mb = 0; mb < 4; ++mb) {
-#pragma unroll
-            for (int kk = 0; kk < kTileE / 16; ++kk) {
-              // A = V^T rows 128 mb .. +128 (channels) x entries 16 kk .. +16;
-              // B = P entries 16 kk .. +16 x 64 heads
-              mma_f16(tm_o + mb * kHN, dO_a + ((2 * mb * L::v_atom + kk * 2048) >> 4),
-                      dO_b + ((kk * 2048) >> 4), id_o, kk > 0 ? 1u : acc0);
-            }
-            mma_commit(su32(&ctl.bar_o[mb]));
+          for (int half = 0; half < 2; ++half) {
+            const int e0 = col0 + 8 * half;  // entries e0 .. e0 + 7: atom e0 / 64, chunk (e0 % 64) / 8
+            const uint32_t off = L::p_off + (uint32_t)(e0 >> 6) * L::p_atom +
+                                 (uint32_t)(h >> 3) * 1024u + (uint32_t)(h & 7) * 128u +
+                                 (uint32_t)((((e0 & 63) >> 3) ^ (h & 7)) << 4);
+            *reinterpret_cast<uint4*>(smem + off) =
+                make_uint4(pk[4 * half], pk[4 * half + 1], pk[4 * half + 2], pk[4 * half + 3]);
           }
         }
+        if (bi & 1) {  // entries 64 (bi / 2) .. +64 written by this warp
+          proxy_fence();
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(su32(&ctl.p_half[bi >> 1]));
+        }
       }
-      __syncwarp();
+      l_acc += (lsum[0] + lsum[1]) + (lsum[2] + lsum[3]);
     }
-    // ---- epilogue ----
-    if (alive && ntiles > 0) alive = mbar_wait(su32(&ctl.bar_o[3]), (ntiles - 1) & 1, status);
-    tc_fence_after();
-    ctl.red[warp & 3][hh * 32 + lane] = warp_reduce32<false>(l_part);
-    softmax_bar();
-    const float ln2 = 0.69314718055994530942f;
-    if (tid < kHN) {
-      const float l = (ctl.red[0][tid] + ctl.red[1][tid]) + (ctl.red[2][tid] + ctl.red[3][tid]);
+    // ---- row sums, lse ----
+    const float l = l_acc + __shfl_xor_sync(0xffffffffu, l_acc, 16);
+    if (lane < 16) {
+      const float ln2 = 0.69314718055994530942f;
       const bool empty = !(l > 0.0f);
-      ctl.linv[tid] = empty ? 0.0f : 1.0f / l;
-      if (tid < H) {
-        const float lse_v = empty ? -INFINITY : (m_own * c + log2f(l)) * ln2;
+      ctl.linv[h] = empty ? 0.0f : 1.0f / l;
+      if (h < H) {
+        const float lse_v = empty ? -INFINITY : (m_ref * c + log2f(l)) * ln2;
         if (nsplit == 1) {
-          if (lse) lse[(int64_t)b * H + tid] = lse_v;
+          if (lse) lse[(int64_t)b * H + h] = lse_v;
         } else {
-          part_lse[((int64_t)b * nsplit + split) * H + tid] = lse_v;
+          part_lse[((int64_t)b * nsplit + split) * H + h] = lse_v;
         }
       }
     }
-    softmax_bar();
-    float* obase = (nsplit == 1) ? out + (int64_t)b * H * kD
-                                 : part_o + ((int64_t)b * nsplit + split) * H * kD;
+  }
+
+  // ---- epilogue: every warp reads one M-block x 32 channels of O^T from
+  //      tensor memory; a thread holds one channel of every head ----
+  __syncthreads();
+  bool have_o = ntiles > 0 && !aborted(ctl);
+  if (have_o)
+    have_o = __all_sync(0xffffffffu, mbar_wait(su32(&ctl.o_blk[3]),
+                                               (uint32_t)(ntiles - 1) & 1u, status));
+  tc_fence_after();
+  {
+    const int qd = warp & 3, mb = warp >> 2;
+    const uint32_t lane_base = (uint32_t)(qd * 32) << 16;
+    const int ch = mb * 128 + qd * 32 + lane;  // this thread's channel
+    // output [head][channel] fp32: per head, a warp stores 32 consecutive
+    // channels; split partial [channel][head] fp16: a thread stores its
+    // channel's heads contiguously, 16 heads per 32-byte store (the partial
+    // buffer is 256-byte aligned and a channel's row is 2 H bytes)
+    float* orow = out + (int64_t)b * H * kD + ch;
+    uint4* prow = reinterpret_cast<uint4*>(part_o + (((int64_t)b * nsplit + split) * kD + ch) * H);
 #pragma unroll 1
-    for (int mb = 0; mb < 4; ++mb) {
-      const int ch = mb * 128 + e;  // this thread's channel
-#pragma unroll 1
-      for (int c16 = 0; c16 < 2; ++c16) {
-        const int h0 = hh * 32 + c16 * 16;
-        if (h0 >= H) continue;
-        float o16[16];
-        if (alive && ntiles > 0) {
-          tmem_ld16(tm_o + lane_base + mb * kHN + h0, o16);
-          tmem_wait_ld();
-        } else {
+    for (int h0 = 0; h0 < H; h0 += 16) {
+      float o16[16];
+      if (have_o) {
+        tmem_ld16(tm_o + lane_base + mb * kHN + h0, o16);
+        tmem_wait_ld();
+      } else {
 #pragma unroll
-          for (int i = 0; i < 16; ++i) o16[i] = 0.0f;
-        }
+        for (int i = 0; i < 16; ++i) o16[i] = 0.0f;
+      }
 #pragma unroll
-        for (int i = 0; i < 16; ++i) obase[(int64_t)(h0 + i) * kD + ch] = o16[i] * ctl.linv[h0 + i];
+      for (int i = 0; i < 16; ++i) o16[i] *= ctl.linv[h0 + i];
+      if (nsplit == 1) {
+#pragma unroll
+        for (int i = 0; i < 16; ++i) orow[(int64_t)(h0 + i) * kD] = o16[i];
+      } else {
+        // one 32-byte store: a whole sector
+        asm volatile("st.global.v8.u32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(prow + h0 / 8),
+                     "r"(pack_f16x2(o16[0], o16[1])), "r"(pack_f16x2(o16[2], o16[3])),
+                     "r"(pack_f16x2(o16[4], o16[5])), "r"(pack_f16x2(o16[6], o16[7])),
+                     "r"(pack_f16x2(o16[8], o16[9])), "r"(pack_f16x2(o16[10], o16[11])),
+                     "r"(pack_f16x2(o16[12], o16[13])), "r"(pack_f16x2(o16[14], o16[15]))
+                     : "memory");
       }
     }
   }
@@ -525,7 +725,7 @@ sparse_attn_tc_kernel(const uint16_t* __restrict__ q_bf16, const uint8_t* __rest
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  if (warp == 0)
+  if (warp == kIssuerWarp)
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, 512;" ::"r"(tmem));
 }
 
@@ -535,7 +735,7 @@ template <int H>
 static cudaError_t launch_tc_t(const uint16_t* q_bf16, const uint8_t* kv_fp4, int B, int64_t N,
                                int64_t kv_seq_stride, int q_per_seq, const int32_t* idx, int k,
                                int nsplit, int chunk, float scale_log2, float* out, float* lse,
-                               float* part_o, float* part_lse, int32_t* status,
+                               __half* part_o, float* part_lse, int32_t* status,
                                const SwaArgs* swa, int32_t* idx_copy, cudaStream_t stream,
                                bool pdl) {
   using L = TcLayout;
@@ -552,7 +752,7 @@ static cudaError_t launch_tc_t(const uint16_t* q_bf16, const uint8_t* kv_fp4, in
 cudaError_t launch_sparse_attn_tc(const uint16_t* q_bf16, const uint8_t* kv_fp4, int B, int H,
                                   int64_t N, int64_t kv_seq_stride, int q_per_seq,
                                   const int32_t* idx, int k, int nsplit, int chunk,
-                                  float scale_log2, float* out, float* lse, float* part_o,
+                                  float scale_log2, float* out, float* lse, __half* part_o,
                                   float* part_lse, int32_t* status, const SwaArgs* swa,
                                   int32_t* idx_copy, cudaStream_t stream, bool pdl) {
   switch (H) {

@@ -193,11 +193,12 @@ cudaError_t launch_sparse_attn(const uint16_t* q_bf16, const uint8_t* kv_fp4, in
                                int32_t* status, cudaStream_t stream, bool pdl = false,
                                const SwaArgs* swa = nullptr, int32_t* idx_copy = nullptr);
 
-// tcgen05 kernel of one sparse-attention call (partials when nsplit > 1).
+// tcgen05 kernel of one sparse-attention call (fp16 partials [B][nsplit][512][H]
+// and fp32 partial lse [B][nsplit][H] when nsplit > 1).
 cudaError_t launch_sparse_attn_tc(const uint16_t* q_bf16, const uint8_t* kv_fp4, int B, int H,
                                   int64_t N, int64_t kv_seq_stride, int q_per_seq,
                                   const int32_t* idx, int k, int nsplit, int chunk,
-                                  float scale_log2, float* out, float* lse, float* part_o,
+                                  float scale_log2, float* out, float* lse, __half* part_o,
                                   float* part_lse, int32_t* status, const SwaArgs* swa,
                                   int32_t* idx_copy, cudaStream_t stream, bool pdl);
 

@@ -144,6 +144,9 @@ def test_layer_group_launch_counts(libpath):
     assert count(layers, g) == (1 + 1 + 1 + 2) + (2 + 2)  # Full also selects the pool
     layers, g = _group(csa2, [0, 1], pool=16384, pool_block=8)
     assert count(layers, g) == (1 + 3 + 1 + 2) + (2 + 2)  # blockwise pool: three kernels
+    # 160 queries: one CTA per query, no merge kernel
+    layers, g = _group(csa2, [0, 2], B=160, k=2048)
+    assert count(layers, g) == (1 + 1 + 1) + 1
     layers, g = _group(csa2, [2, 0])                      # no Full layer first
     assert count(layers, g) == -1
     layers, g = _group(csa2, [0], B=0)
