@@ -378,6 +378,18 @@ csa2_status csa2_layer_group(const csa2_layer* layers, int n_layers, const csa2_
   const int32_t* latest = nullptr;
   const bool mx = g->indexer_fmt == CSA2_INDEXER_MXFP4;
   cudaError_t e = cudaSuccess;
+  // A layer's top-k requests the FP4 rows it selects into L2 while it writes
+  // them, so that the attention's first tiles find their rows there; only
+  // when the selected rows of the batch take at most half of L2 (not for
+  // many queries over one shared context, whose rows repeat).
+  RowPrefetch pf;
+  if ((reinterpret_cast<uintptr_t>(g->kv_fp4) & 15u) == 0 &&
+      (int64_t)g->B * g->k * kRowBytes <= (int64_t)64 << 20) {
+    pf.kv = g->kv_fp4;
+    pf.seq_bytes = g->kv_seq_stride * kRowBytes;
+    pf.n = g->N;
+    pf.q_per_seq = g->q_per_seq;
+  }
   for (int l = 0; l < n_layers && e == cudaSuccess; ++l) {
     const csa2_layer& L = layers[l];
     const int32_t* use = nullptr;
@@ -399,7 +411,7 @@ csa2_status csa2_layer_group(const csa2_layer* layers, int n_layers, const csa2_
       }
       if (e == cudaSuccess)
         e = launch_topk(scores, g->B, g->N, g->k, g->q_pos, g->ratio, nullptr, nullptr, L.idx_out,
-                        stream, /*pdl=*/true, wsb + w.topk, w.topk_bytes);
+                        stream, /*pdl=*/true, wsb + w.topk, w.topk_bytes, pf);
       use = L.idx_out;
     } else if (L.mode == CSA2_REINDEX) {
       e = mx ? launch_pool_scores_mxfp4(L.qi_fp8, g->ki_fp8, g->B, g->H_I, g->N,
@@ -410,7 +422,7 @@ csa2_status csa2_layer_group(const csa2_layer* layers, int n_layers, const csa2_
                                   pscores, status, stream);
       if (e == cudaSuccess)
         e = launch_topk(pscores, g->B, g->pool_size, g->k, nullptr, 1, nullptr, g->pool_out,
-                        L.idx_out, stream, /*pdl=*/true);
+                        L.idx_out, stream, /*pdl=*/true, nullptr, 0, pf);
       use = L.idx_out;
     } else {  // REUSE: the attention kernel writes the copy of the reused indices
       use = latest;

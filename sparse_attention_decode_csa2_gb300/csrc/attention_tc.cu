@@ -35,7 +35,7 @@
 //               all eight warps convert one atom pair at a time, E2M1 x E4M3
 //               -> fp16 (exact), into the swizzled V tile
 //   warp 12     TMEM allocation; lane 0 issues every MMA
-//   warp 13     prefetcher: requests the selected rows of tiles 2, 3, ... (and
+//   warp 13     prefetcher: requests the selected rows of tiles 1, 2, ... (and
 //               the SWA window) into L2 up to 16 tiles ahead of the
 //               dequantisers, so that DRAM streams a chunk's rows while earlier
 //               tiles are computed
@@ -79,6 +79,7 @@ constexpr int kPrefWarp = 13;
 constexpr int kAheadTiles = 16;     // tiles requested into L2 ahead of the dequantisers
 constexpr int kIdxCache = 2048;     // slot ids kept in shared memory
 constexpr int kMaxSlots = 16384;    // validity bits kept for a chunk
+constexpr int kMaxSplitTc = 8;      // splits of a query (one cluster), a power of two
 
 struct TcLayout {
   static constexpr uint32_t q_atom = 64 * 128;            // [64 heads][128 B]
@@ -96,15 +97,16 @@ struct TcLayout {
 static_assert(TcLayout::alloc <= 232448, "shared memory");
 
 struct TcCtl {
-  uint64_t v_ready[4];   // atoms 2p, 2p + 1 of the current V tile written (8 warps)
+  float alpha[kHN];      // rescale factor of O^T per head (rare)
+  float linv[kHN];       // 1 / row sum per head (epilogue)
+  uint64_t v_ready[2];   // atoms 4h .. 4h + 3 of the current V tile written (8 warps)
   uint64_t s_full[2];    // S of a tile in S buffer (commit)
-  uint64_t o_blk[4];     // O^T(t) M-block p done: atoms 2p, 2p + 1 free (commit)
+  uint64_t o_half[2];    // O^T(t) M-blocks 2h, 2h + 1 done: atoms 4h .. 4h + 3 free (commit)
   uint64_t p_half[2];    // P entries 64 j .. 64 j + 63 written (4 softmax warps)
+  uint64_t recv;         // the split merge's partial blocks have arrived (bulk copies)
   uint32_t tmem_base;
   int32_t abort;         // a bounded wait gave up somewhere in the CTA
   int32_t tiles_done;    // tiles the first dequantiser warp has written
-  float alpha[kHN];      // rescale factor of O^T per head (rare)
-  float linv[kHN];       // 1 / row sum per head (epilogue)
 };
 static_assert(sizeof(TcCtl) <= 1024, "control block");
 
@@ -147,11 +149,29 @@ __device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
   return r;
 }
 
-// Brings the lines holding row[0], row[128], ... (offsets below `bytes`)
-// into L2; every address it names lies inside the row.
+// Requests `bytes` bytes at `row` (16-byte aligned, a multiple of 16) into
+// L2 through the bulk-copy unit: no load/store-unit traffic, which the
+// softmax and dequantiser warps of the SM share.
 __device__ __forceinline__ void prefetch_l2(const uint8_t* row, int bytes) {
-  for (int off = 0; off < bytes; off += 128)
-    asm volatile("prefetch.global.L2 [%0];" ::"l"(reinterpret_cast<const void*>(row + off)));
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(row), "r"((uint32_t)bytes)
+               : "memory");
+}
+
+// Bulk copies (the SM's copy engine): shared -> global in a bulk group, and
+// global -> shared completing on an mbarrier.  Addresses 16-byte aligned,
+// sizes multiples of 16.
+__device__ __forceinline__ void bulk_store(void* dst, uint32_t src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(dst), "r"(src),
+               "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes,
+                                          uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          dst),
+      "l"(src), "r"(bytes), "r"(bar)
+      : "memory");
 }
 
 // The same bounded wait for every lane of a warp, with one answer for all of
@@ -212,8 +232,8 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
 sparse_attn_tc_kernel(const uint16_t* __restrict__ q_bf16, const uint8_t* __restrict__ kv_fp4,
                       int64_t N, int64_t kv_seq_stride, int q_per_seq,
                       const int32_t* __restrict__ idx, int k, int chunk, float scale_log2,
-                      float* __restrict__ out, float* __restrict__ lse, __half* __restrict__ part_o,
-                      float* __restrict__ part_lse, int32_t* status,
+                      float* __restrict__ out, float* __restrict__ lse,
+                      __half* __restrict__ part_o, float* __restrict__ part_lse, int32_t* status,
                       const uint8_t* __restrict__ swa_kv, int64_t swa_ring, int n_win,
                       const int32_t* __restrict__ q_pos, int32_t* __restrict__ idx_copy) {
   using L = TcLayout;
@@ -282,12 +302,13 @@ sparse_attn_tc_kernel(const uint16_t* __restrict__ q_bf16, const uint8_t* __rest
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
   }
   if (tid == 0) {
-    for (int i = 0; i < 4; ++i) {
+    for (int i = 0; i < 2; ++i) {
       mbar_init(su32(&ctl.v_ready[i]), kDeqWarps);
-      mbar_init(su32(&ctl.o_blk[i]), 1);
+      mbar_init(su32(&ctl.o_half[i]), 1);
     }
     for (int i = 0; i < 2; ++i) mbar_init(su32(&ctl.s_full[i]), 1);
     for (int i = 0; i < 2; ++i) mbar_init(su32(&ctl.p_half[i]), kSoftWarps);
+    mbar_init(su32(&ctl.recv), 1);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     ctl.abort = 0;
     ctl.tiles_done = 0;
@@ -336,7 +357,7 @@ sparse_attn_tc_kernel(const uint16_t* __restrict__ q_bf16, const uint8_t* __rest
     for (int r = lane; r < wcnt; r += 32)
       prefetch_l2(swaseq + ((w0 + r) % swa_ring) * kD, kD);
     uint64_t t_idle = 0;
-    for (int t = 2; t < nmain && !aborted(ctl);) {  // the dequantisers load tiles 0, 1 themselves
+    for (int t = 1; t < nmain && !aborted(ctl);) {  // the dequantisers load tile 0 themselves
       const int done = *reinterpret_cast<volatile int32_t*>(&ctl.tiles_done);
       if (t >= done + kAheadTiles) {
         if (t_idle == 0) t_idle = globaltimer();
@@ -354,114 +375,105 @@ sparse_attn_tc_kernel(const uint16_t* __restrict__ q_bf16, const uint8_t* __rest
     }
   } else if (warp >= kDeqWarp0 && warp < kDeqWarp0 + kDeqWarps) {
     // ================= dequantisers =================
-    // Atom pairs in order; for pair p a thread converts row e, atom 2 p + ah
-    // (32 code bytes + 4 scale bytes), so all eight warps finish a pair
-    // together and S can start on it while the next pair is converted.
+    // V is handed over in two halves of four 64-channel atoms.  For half h a
+    // lane converts atom 4 h + lane / 8 of rows 16 w + 8 i + lane % 8 (i = 0,
+    // 1; w = the dequantiser warp): each load instruction of a warp reads 128
+    // contiguous bytes of eight rows (a few cache lines per row instead of one
+    // per lane), and the eight lanes of each phase of a 16-byte shared-memory
+    // store write eight consecutive rows of one atom, i.e. eight different
+    // 16-byte slots of the swizzle.
     const int dt = tid - kDeqWarp0 * 32;  // 0..255
-    const int e = dt & 127, ah = dt >> 7;
+    const int dw = dt >> 5, sub = lane >> 3, rsub = lane & 7;
     // 256-bit loads need a 32-byte aligned cache (rows are 288 = 9 x 32 bytes)
     const bool wide = (reinterpret_cast<uintptr_t>(kv_fp4) & 31u) == 0;
-    // this thread's row of tile t: its source, or null past the chunk / for an empty slot
-    auto row_src = [&](int t) -> const uint8_t* {
-      const int s = t * kTileE + e;
-      return (t < nmain && s < cnt && slot_ok(s)) ? kvseq + (int64_t)slot_id(s) * kRowBytes
-                                                  : nullptr;
-    };
-    // atom 2 p + ah (channels 64 a .. +64: code bytes 32 a ..) of a row
-    auto load_atom = [&](const uint8_t* src, int p, Eighth& q) {
-      if (src) {
-        ld32(src + 32 * (2 * p + ah), wide, q.cw[0], q.cw[1]);
-      } else {
-        q.cw[0] = q.cw[1] = make_uint4(0, 0, 0, 0);
-      }
-    };
-    // the row's 32 scale bytes (block b = channels 16 b .. +16)
-    auto load_scales = [&](const uint8_t* src, uint4& s_lo, uint4& s_hi) {
-      if (src) {
-        ld32(src + kCodeBytes, wide, s_lo, s_hi);
-      } else {
-        s_lo = s_hi = make_uint4(0, 0, 0, 0);
-      }
-    };
     uint8_t* vt = smem + L::v_off;
-    Eighth cur[4];  // this thread's row of the current tile, one atom per pair
-    uint4 sc_lo, sc_hi;
-    {
-      const uint8_t* src = row_src(0);
-      load_scales(src, sc_lo, sc_hi);
+    Eighth cur[2][2];   // [half][i]: 32 code bytes of the lane's atom of a row
+    uint32_t scw[2][2];  // [half][i]: the atom's 4 scale bytes
+    auto load_tile = [&](int t) {
 #pragma unroll
-      for (int p = 0; p < 4; ++p) load_atom(src, p, cur[p]);
-    }
+      for (int i = 0; i < 2; ++i) {
+        const int sl = t * kTileE + 16 * dw + 8 * i + rsub;
+        const uint8_t* src = (t < nmain && sl < cnt && slot_ok(sl))
+                                 ? kvseq + (int64_t)slot_id(sl) * kRowBytes
+                                 : nullptr;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const int a = 4 * h + sub;
+          if (src) {
+            ld32(src + 32 * a, wide, cur[h][i].cw[0], cur[h][i].cw[1]);
+            scw[h][i] = __ldg(reinterpret_cast<const uint32_t*>(src + kCodeBytes + 4 * a));
+          } else {
+            cur[h][i].cw[0] = cur[h][i].cw[1] = make_uint4(0, 0, 0, 0);
+            scw[h][i] = 0u;
+          }
+        }
+      }
+    };
+    load_tile(0);
     for (int t = 0; t < ntiles && alive; ++t) {
-      // the next tile's row: its scales now, pair p once pair p of this tile is stored
-      const uint8_t* nsrc = row_src(t + 1);
-      uint4 nsc_lo, nsc_hi;
-      load_scales(nsrc, nsc_lo, nsc_hi);
-      Eighth nxt[4];
 #pragma unroll
-      for (int p = 0; p < 4; ++p) {
-        if (!alive) break;
-        const int a = 2 * p + ah;
-        // atoms 2p, 2p + 1 are free once O^T(t - 1) M-block p has read them
-        if (t >= 1 && !warp_wait(ctl, &ctl.o_blk[p], (uint32_t)(t - 1) & 1u, status)) {
+      for (int h = 0; h < 2; ++h) {
+        // atoms 4h .. 4h + 3 are free once O^T(t - 1) M-blocks 2h, 2h + 1 have read them
+        if (t >= 1 && !warp_wait(ctl, &ctl.o_half[h], (uint32_t)(t - 1) & 1u, status)) {
           alive = false;
           break;
         }
-        if (t < nmain) {
-          // word w of code vector u: channels 64 a + 32 u + 8 w .. +8, scale
-          // byte 4 a + 2 u + w / 2, 16-byte chunk 4 u + w of atom a
-          const uint32_t scw[8] = {sc_lo.x, sc_lo.y, sc_lo.z, sc_lo.w,
-                                   sc_hi.x, sc_hi.y, sc_hi.z, sc_hi.w};
+        const int a = 4 * h + sub;
 #pragma unroll
-          for (int u = 0; u < 2; ++u) {
-            const uint32_t sword = ah ? scw[2 * p + 1] : scw[2 * p];  // scale bytes 4 a .. 4 a + 3
-            const uint32_t sbytes = (sword >> (16 * u)) & 0xFFFFu;
-            const uint32_t s_lo = e4m3x2_to_f16x2((uint16_t)((sbytes & 0xFFu) * 0x101u));
-            const uint32_t s_hi = e4m3x2_to_f16x2((uint16_t)((sbytes >> 8) * 0x101u));
-            const __half2 h_lo = *reinterpret_cast<const __half2*>(&s_lo);
-            const __half2 h_hi = *reinterpret_cast<const __half2*>(&s_hi);
-            const uint4 w = cur[p].cw[u];
-            *reinterpret_cast<uint4*>(vt + v_chunk_off(a, e, 4 * u + 0)) = dequant8(w.x, h_lo);
-            *reinterpret_cast<uint4*>(vt + v_chunk_off(a, e, 4 * u + 1)) = dequant8(w.y, h_lo);
-            *reinterpret_cast<uint4*>(vt + v_chunk_off(a, e, 4 * u + 2)) = dequant8(w.z, h_hi);
-            *reinterpret_cast<uint4*>(vt + v_chunk_off(a, e, 4 * u + 3)) = dequant8(w.w, h_hi);
-          }
-        } else {
-          // a tile of the SWA window: E4M3 row from global (in L2), -> fp16 (exact)
-          const int sl = (t - nmain) * kTileE + e;
-          uint4 wv[4];
-          if (sl < wcnt) {
-            const uint4* src =
-                reinterpret_cast<const uint4*>(swaseq + ((w0 + sl) % swa_ring) * kD) + 4 * a;
+        for (int i = 0; i < 2; ++i) {
+          const int e = 16 * dw + 8 * i + rsub;
+          if (t < nmain) {
+            // word w of code vector u: channels 64 a + 32 u + 8 w .. +8,
+            // scale byte 2 u + w / 2 of the atom, 16-byte chunk 4 u + w
 #pragma unroll
-            for (int i = 0; i < 4; ++i) wv[i] = __ldg(src + i);
+            for (int u = 0; u < 2; ++u) {
+              const uint32_t sbytes = (scw[h][i] >> (16 * u)) & 0xFFFFu;
+              const uint32_t s_lo = e4m3x2_to_f16x2((uint16_t)((sbytes & 0xFFu) * 0x101u));
+              const uint32_t s_hi = e4m3x2_to_f16x2((uint16_t)((sbytes >> 8) * 0x101u));
+              const __half2 h_lo = *reinterpret_cast<const __half2*>(&s_lo);
+              const __half2 h_hi = *reinterpret_cast<const __half2*>(&s_hi);
+              const uint4 w = cur[h][i].cw[u];
+              *reinterpret_cast<uint4*>(vt + v_chunk_off(a, e, 4 * u + 0)) = dequant8(w.x, h_lo);
+              *reinterpret_cast<uint4*>(vt + v_chunk_off(a, e, 4 * u + 1)) = dequant8(w.y, h_lo);
+              *reinterpret_cast<uint4*>(vt + v_chunk_off(a, e, 4 * u + 2)) = dequant8(w.z, h_hi);
+              *reinterpret_cast<uint4*>(vt + v_chunk_off(a, e, 4 * u + 3)) = dequant8(w.w, h_hi);
+            }
           } else {
+            // a tile of the SWA window: E4M3 row from global (in L2), -> fp16 (exact)
+            const int sl = (t - nmain) * kTileE + e;
+            uint4 wv[4];
+            if (sl < wcnt) {
+              const uint4* src =
+                  reinterpret_cast<const uint4*>(swaseq + ((w0 + sl) % swa_ring) * kD) + 4 * a;
 #pragma unroll
-            for (int i = 0; i < 4; ++i) wv[i] = make_uint4(0, 0, 0, 0);
-          }
+              for (int j = 0; j < 4; ++j) wv[j] = __ldg(src + j);
+            } else {
 #pragma unroll
-          for (int ci = 0; ci < 8; ++ci) {
-            // channels 8 ci .. 8 ci + 7 of atom a: bytes 8 (ci & 1) .. of wv[ci / 2]
-            const uint4 u = wv[ci >> 1];
-            const uint32_t lo = (ci & 1) ? u.z : u.x, hi = (ci & 1) ? u.w : u.y;
-            *reinterpret_cast<uint4*>(vt + v_chunk_off(a, e, ci)) =
-                make_uint4(e4m3x2_to_f16x2((uint16_t)(lo & 0xFFFFu)),
-                           e4m3x2_to_f16x2((uint16_t)(lo >> 16)),
-                           e4m3x2_to_f16x2((uint16_t)(hi & 0xFFFFu)),
-                           e4m3x2_to_f16x2((uint16_t)(hi >> 16)));
+              for (int j = 0; j < 4; ++j) wv[j] = make_uint4(0, 0, 0, 0);
+            }
+#pragma unroll
+            for (int ci = 0; ci < 8; ++ci) {
+              // channels 8 ci .. 8 ci + 7 of atom a: bytes 8 (ci & 1) .. of wv[ci / 2]
+              const uint4 u = wv[ci >> 1];
+              const uint32_t lo = (ci & 1) ? u.z : u.x, hi = (ci & 1) ? u.w : u.y;
+              *reinterpret_cast<uint4*>(vt + v_chunk_off(a, e, ci)) =
+                  make_uint4(e4m3x2_to_f16x2((uint16_t)(lo & 0xFFFFu)),
+                             e4m3x2_to_f16x2((uint16_t)(lo >> 16)),
+                             e4m3x2_to_f16x2((uint16_t)(hi & 0xFFFFu)),
+                             e4m3x2_to_f16x2((uint16_t)(hi >> 16)));
+            }
           }
         }
         proxy_fence();  // the tensor cores read V through the async proxy
         __syncwarp();
-        if (lane == 0) mbar_arrive(su32(&ctl.v_ready[p]));
-        load_atom(nsrc, p, nxt[p]);
+        if (lane == 0) mbar_arrive(su32(&ctl.v_ready[h]));
       }
       if (warp == kDeqWarp0 && lane == 0)
         *reinterpret_cast<volatile int32_t*>(&ctl.tiles_done) = t + 1;
-#pragma unroll
-      for (int p = 0; p < 4; ++p) cur[p] = nxt[p];
-      sc_lo = nsc_lo;
-      sc_hi = nsc_hi;
+      // the next tile's rows, requested only now: an arrive (release) waits
+      // for the loads its thread has in flight, so loads issued before the
+      // arrives above would hold this tile's handovers for a memory round trip
+      if (alive && t + 1 < nmain) load_tile(t + 1);
     }
   } else if (warp == kIssuerWarp) {
     // ================= MMA issuer =================
@@ -481,16 +493,16 @@ sparse_attn_tc_kernel(const uint16_t* __restrict__ q_bf16, const uint8_t* __rest
       bool ok = true;
       for (int t = 0; t < ntiles && ok; ++t) {
         const uint32_t d_s = tm_s + (uint32_t)(t & 1) * kTileE;
-        // S(t), atom pair by atom pair as the dequantisers finish them
+        // S(t), half by half as the dequantisers finish them
 #pragma unroll
-        for (int p = 0; p < 4; ++p) {
-          if (!mbar_wait(su32(&ctl.v_ready[p]), (uint32_t)t & 1u, status)) {
+        for (int h = 0; h < 2; ++h) {
+          if (!mbar_wait(su32(&ctl.v_ready[h]), (uint32_t)t & 1u, status)) {
             ok = false;
             break;
           }
           tc_fence_after();
 #pragma unroll
-          for (int a = 2 * p; a < 2 * p + 2; ++a)
+          for (int a = 4 * h; a < 4 * h + 4; ++a)
 #pragma unroll
             for (int jj = 0; jj < 4; ++jj)
               mma_f16(d_s, dS_a + ((a * L::q_atom + jj * 32) >> 4),
@@ -519,11 +531,11 @@ sparse_attn_tc_kernel(const uint16_t* __restrict__ q_bf16, const uint8_t* __rest
               mma_f16(tm_o + mb * kHN, dO_a + ((2 * mb * L::v_atom + kk * 2048) >> 4),
                       dO_b + (((kk >> 2) * L::p_atom + (kk & 3) * 32) >> 4), id_o,
                       (t > 0 || kk > 0) ? 1u : 0u);
-            if (hf == 1) mma_commit(su32(&ctl.o_blk[mb]));
+            if (hf == 1 && (mb & 1)) mma_commit(su32(&ctl.o_half[mb >> 1]));
           }
         }
         if (!ok) break;
-        last = &ctl.o_blk[3];
+        last = &ctl.o_half[1];
         last_par = (uint32_t)t & 1u;
       }
       if (!ok) *reinterpret_cast<volatile int32_t*>(&ctl.abort) = 1;
@@ -603,7 +615,7 @@ sparse_attn_tc_kernel(const uint16_t* __restrict__ q_bf16, const uint8_t* __rest
         softmax_bar();
         // O^T(t - 1), the last product into O, must be complete; O^T rows are
         // channels: this warp rescales all 256 columns of its quadrant's lanes
-        if (warp_wait(ctl, &ctl.o_blk[3], (uint32_t)(t - 1) & 1u, status)) {
+        if (warp_wait(ctl, &ctl.o_half[1], (uint32_t)(t - 1) & 1u, status)) {
           tc_fence_after();
 #pragma unroll 1
           for (int c4 = 0; c4 < 64; ++c4) {
@@ -624,7 +636,7 @@ sparse_attn_tc_kernel(const uint16_t* __restrict__ q_bf16, const uint8_t* __rest
         }
       }
       // P is free once O^T(t - 1) has read it
-      if (t > 0 && !warp_wait(ctl, &ctl.o_blk[3], (uint32_t)(t - 1) & 1u, status)) alive = false;
+      if (t > 0 && !warp_wait(ctl, &ctl.o_half[1], (uint32_t)(t - 1) & 1u, status)) alive = false;
       // P = exp2(c s - c m_ref), fp16, into row h of the K-major P tile
       const float mneg = m_ref == -INFINITY ? 0.0f : -m_ref * c;
       float lsum[4] = {0.0f, 0.0f, 0.0f, 0.0f};
@@ -678,55 +690,156 @@ sparse_attn_tc_kernel(const uint16_t* __restrict__ q_bf16, const uint8_t* __rest
   }
 
   // ---- epilogue: every warp reads one M-block x 32 channels of O^T from
-  //      tensor memory; a thread holds one channel of every head ----
+  //      tensor memory (a thread holds one channel of every head) and scales
+  //      it by 1 / row sum.  One split: the output [head][channel] fp32 (for
+  //      each head a warp stores one 128-byte line).  Several: this split's
+  //      partial, staged in shared memory (V is no longer read) as eight
+  //      64-channel blocks [block][channel][head] fp16, 16-byte chunks of a
+  //      row swizzled by the channel (a thread's heads are one row: wide
+  //      conflict-free stores) ----
   __syncthreads();
   bool have_o = ntiles > 0 && !aborted(ctl);
   if (have_o)
-    have_o = __all_sync(0xffffffffu, mbar_wait(su32(&ctl.o_blk[3]),
+    have_o = __all_sync(0xffffffffu, mbar_wait(su32(&ctl.o_half[1]),
                                                (uint32_t)(ntiles - 1) & 1u, status));
   tc_fence_after();
+  constexpr int kCr = H / 8;                        // 16-byte chunks per staged row
+  const uint32_t blk_bytes = (uint32_t)H * 64u * 2u;  // one fp16 partial block
+  auto chunk_off = [&](int j, int ch, int c) -> uint32_t {  // staged block j, row ch, chunk c
+    return (uint32_t)j * blk_bytes + (uint32_t)ch * (H * 2) + (uint32_t)((c ^ (ch & (kCr - 1))) << 4);
+  };
   {
     const int qd = warp & 3, mb = warp >> 2;
     const uint32_t lane_base = (uint32_t)(qd * 32) << 16;
     const int ch = mb * 128 + qd * 32 + lane;  // this thread's channel
-    // output [head][channel] fp32: per head, a warp stores 32 consecutive
-    // channels; split partial [channel][head] fp16: a thread stores its
-    // channel's heads contiguously, 16 heads per 32-byte store (the partial
-    // buffer is 256-byte aligned and a channel's row is 2 H bytes)
-    float* orow = out + (int64_t)b * H * kD + ch;
-    uint4* prow = reinterpret_cast<uint4*>(part_o + (((int64_t)b * nsplit + split) * kD + ch) * H);
-#pragma unroll 1
-    for (int h0 = 0; h0 < H; h0 += 16) {
-      float o16[16];
-      if (have_o) {
-        tmem_ld16(tm_o + lane_base + mb * kHN + h0, o16);
-        tmem_wait_ld();
-      } else {
+    float o[kHN];
+    if (have_o) {  // all of the thread's columns: one tensor-memory round trip
 #pragma unroll
-        for (int i = 0; i < 16; ++i) o16[i] = 0.0f;
-      }
+      for (int h0 = 0; h0 < H; h0 += 16) tmem_ld16(tm_o + lane_base + mb * kHN + h0, o + h0);
+      tmem_wait_ld();
+    } else {
 #pragma unroll
-      for (int i = 0; i < 16; ++i) o16[i] *= ctl.linv[h0 + i];
-      if (nsplit == 1) {
+      for (int i = 0; i < kHN; ++i) o[i] = 0.0f;
+    }
 #pragma unroll
-        for (int i = 0; i < 16; ++i) orow[(int64_t)(h0 + i) * kD] = o16[i];
-      } else {
-        // one 32-byte store: a whole sector
-        asm volatile("st.global.v8.u32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(prow + h0 / 8),
-                     "r"(pack_f16x2(o16[0], o16[1])), "r"(pack_f16x2(o16[2], o16[3])),
-                     "r"(pack_f16x2(o16[4], o16[5])), "r"(pack_f16x2(o16[6], o16[7])),
-                     "r"(pack_f16x2(o16[8], o16[9])), "r"(pack_f16x2(o16[10], o16[11])),
-                     "r"(pack_f16x2(o16[12], o16[13])), "r"(pack_f16x2(o16[14], o16[15]))
-                     : "memory");
-      }
+    for (int i = 0; i < H; i += 4) {
+      const float4 li = *reinterpret_cast<const float4*>(&ctl.linv[i]);
+      o[i] *= li.x;
+      o[i + 1] *= li.y;
+      o[i + 2] *= li.z;
+      o[i + 3] *= li.w;
+    }
+    if (nsplit == 1) {
+      float* orow = out + (int64_t)b * H * kD + ch;
+#pragma unroll
+      for (int i = 0; i < H; ++i) orow[(int64_t)i * kD] = o[i];
+    } else {
+#pragma unroll
+      for (int c = 0; c < kCr; ++c)
+        *reinterpret_cast<uint4*>(smem + L::v_off + chunk_off(ch >> 6, ch & 63, c)) =
+            make_uint4(pack_f16x2(o[8 * c], o[8 * c + 1]), pack_f16x2(o[8 * c + 2], o[8 * c + 3]),
+                       pack_f16x2(o[8 * c + 4], o[8 * c + 5]), pack_f16x2(o[8 * c + 6], o[8 * c + 7]));
     }
   }
-
+  proxy_fence();  // the bulk copies read the staged blocks through the async proxy
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   if (warp == kIssuerWarp)
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, 512;" ::"r"(tmem));
+
+  if (nsplit > 1) {
+    // ---- merge of the query's splits (the cluster is the query's nsplit
+    //      CTAs, nsplit a power of two): CTA `split` owns the 64-channel
+    //      blocks j = split, split + nsplit, ...  Each CTA stores the blocks
+    //      it does not own (bulk copies through L2, which the measured
+    //      distributed-shared-memory reads were slower than), and after the
+    //      cluster barrier fetches the other splits' copies of its own blocks
+    //      and forms o = sum_s exp(lse_s - lse) o_s, lse the log-sum-exp of
+    //      the lse_s ----
+    const int n_own = 8 / nsplit;
+    if (tid == 0) {
+      uint8_t* dst = reinterpret_cast<uint8_t*>(part_o) + ((int64_t)b * nsplit + split) * 8 * blk_bytes;
+      for (int j = 0; j < 8; ++j)
+        if (j % nsplit != split) bulk_store(dst + j * blk_bytes, sbase + L::v_off + j * blk_bytes, blk_bytes);
+      asm volatile("cp.async.bulk.commit_group;\n\tcp.async.bulk.wait_group 0;" ::: "memory");
+      asm volatile("fence.proxy.async.global;" ::: "memory");
+    }
+    asm volatile(
+        "barrier.cluster.arrive.release.aligned;\n\t"
+        "barrier.cluster.wait.acquire.aligned;" ::: "memory");
+    const uint32_t recv_s = sbase + L::v_off + 8 * blk_bytes;  // [peer][own block]
+    if (tid == 0) {
+      asm volatile("fence.proxy.async.global;" ::: "memory");
+      mbar_expect_tx(su32(&ctl.recv), (uint32_t)(nsplit - 1) * n_own * blk_bytes);
+      const uint8_t* src = reinterpret_cast<const uint8_t*>(part_o) + (int64_t)b * nsplit * 8 * blk_bytes;
+      for (int s2 = 0, slot = 0; s2 < nsplit; ++s2) {
+        if (s2 == split) continue;
+        for (int kk = 0; kk < n_own; ++kk, ++slot)
+          bulk_load(recv_s + slot * blk_bytes, src + ((int64_t)s2 * 8 + split + kk * nsplit) * blk_bytes,
+                    blk_bytes, su32(&ctl.recv));
+      }
+    }
+    // weights exp(lse_s - M) / sum (per split and head), in the free Q region
+    float* wts = reinterpret_cast<float*>(smem + L::q_off);
+    if (tid >= 32 && tid < 32 + H) {
+      const int hh = tid - 32;
+      const float* pl = part_lse + (int64_t)b * nsplit * H + hh;
+      float lv[kMaxSplitTc];
+#pragma unroll
+      for (int s2 = 0; s2 < kMaxSplitTc; ++s2)
+        lv[s2] = s2 < nsplit ? __ldcg(pl + (int64_t)s2 * H) : -INFINITY;
+      float m = -INFINITY;
+#pragma unroll
+      for (int s2 = 0; s2 < kMaxSplitTc; ++s2) m = fmaxf(m, lv[s2]);
+      float sum = 0.0f;
+#pragma unroll
+      for (int s2 = 0; s2 < kMaxSplitTc; ++s2) {
+        lv[s2] = m == -INFINITY ? 0.0f : expf(lv[s2] - m);
+        sum += lv[s2];
+      }
+      const float inv = sum > 0.0f ? 1.0f / sum : 0.0f;
+#pragma unroll
+      for (int s2 = 0; s2 < kMaxSplitTc; ++s2)
+        if (s2 < nsplit) wts[s2 * 64 + hh] = lv[s2] * inv;
+      if (split == 0 && lse) lse[(int64_t)b * H + hh] = sum > 0.0f ? m + logf(sum) : -INFINITY;
+    }
+    __syncthreads();
+    const bool got = __all_sync(0xffffffffu, mbar_wait(su32(&ctl.recv), 0u, status));
+    // warp w: channels 32 (w & 1) .. +32 of a block (lane = channel), heads
+    // 8 (w >> 1) .. +8; for each head the warp stores one 128-byte line
+    const int cc = 32 * (warp & 1) + lane, c8 = warp >> 1;
+    if (c8 < kCr) {
+      for (int kk = 0; kk < n_own; ++kk) {
+        const int j = split + kk * nsplit;
+        float acc[8] = {0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f};
+        for (int s2 = 0, slot = 0; s2 < nsplit; ++s2) {
+          uint32_t off;
+          if (s2 == split) {
+            off = L::v_off + chunk_off(j, cc, c8);
+          } else {
+            off = L::v_off + 8 * blk_bytes + (uint32_t)(slot * n_own + kk) * blk_bytes +
+                  chunk_off(0, cc, c8);
+            ++slot;
+          }
+          const uint4 v = *reinterpret_cast<const uint4*>(smem + off);
+          const float4 w0 = *reinterpret_cast<const float4*>(wts + s2 * 64 + 8 * c8);
+          const float4 w1 = *reinterpret_cast<const float4*>(wts + s2 * 64 + 8 * c8 + 4);
+          const float wv[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
+          const uint32_t u[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const float2 f = half2_bits_to_float2(u[q]);
+            acc[2 * q] = fmaf(got ? wv[2 * q] : 0.0f, f.x, acc[2 * q]);
+            acc[2 * q + 1] = fmaf(got ? wv[2 * q + 1] : 0.0f, f.y, acc[2 * q + 1]);
+          }
+        }
+        float* orow = out + ((int64_t)b * H + 8 * c8) * kD + 64 * j + cc;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) orow[(int64_t)i * kD] = acc[i];
+      }
+    }
+  }
 }
 
 }  // namespace
@@ -742,11 +855,32 @@ static cudaError_t launch_tc_t(const uint16_t* q_bf16, const uint8_t* kv_fp4, in
   cudaError_t e = cudaFuncSetAttribute(sparse_attn_tc_kernel<H>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)L::alloc);
   if (e != cudaSuccess) return e;
-  return launch_kernel(sparse_attn_tc_kernel<H>, dim3((unsigned)nsplit, (unsigned)B),
-                       dim3(kThreadsTc), L::alloc, stream, pdl, q_bf16, kv_fp4, N, kv_seq_stride,
-                       q_per_seq, idx, k, chunk, scale_log2, out, lse, part_o, part_lse, status,
-                       swa ? swa->kv : nullptr, swa ? swa->ring : (int64_t)0, swa ? swa->n_win : 0,
-                       swa ? swa->q_pos : nullptr, idx_copy);
+  // a query's splits run as one thread-block cluster, which merges them
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)nsplit, (unsigned)B);
+  cfg.blockDim = dim3(kThreadsTc);
+  cfg.dynamicSmemBytes = L::alloc;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[2];
+  unsigned na = 0;
+  if (nsplit > 1) {
+    attr[na].id = cudaLaunchAttributeClusterDimension;
+    attr[na].val.clusterDim.x = (unsigned)nsplit;
+    attr[na].val.clusterDim.y = 1;
+    attr[na].val.clusterDim.z = 1;
+    ++na;
+  }
+  if (pdl) {
+    attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[na].val.programmaticStreamSerializationAllowed = 1;
+    ++na;
+  }
+  cfg.attrs = attr;
+  cfg.numAttrs = na;
+  return cudaLaunchKernelEx(&cfg, sparse_attn_tc_kernel<H>, q_bf16, kv_fp4, N, kv_seq_stride,
+                            q_per_seq, idx, k, chunk, scale_log2, out, lse, part_o, part_lse,
+                            status, swa ? swa->kv : nullptr, swa ? swa->ring : (int64_t)0,
+                            swa ? swa->n_win : 0, swa ? swa->q_pos : nullptr, idx_copy);
 }
 
 cudaError_t launch_sparse_attn_tc(const uint16_t* q_bf16, const uint8_t* kv_fp4, int B, int H,

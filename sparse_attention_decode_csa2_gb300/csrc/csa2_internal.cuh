@@ -143,17 +143,28 @@ cudaError_t launch_pool_scores_mxfp4(const uint8_t* q_mx, const uint8_t* k_mx, i
                                      const int32_t* pool, int P, float* pool_scores,
                                      int32_t* status, cudaStream_t stream);
 
+// Where a top-k's selected entries are read next: their FP4 rows (row j of
+// query b at kv + (b / q_per_seq) * seq_bytes + j * kRowBytes, j < n; kv
+// 16-byte aligned), which the top-k requests into L2 as it writes the
+// indices.  kv == nullptr: no requests.
+struct RowPrefetch {
+  const uint8_t* kv = nullptr;
+  int64_t seq_bytes = 0;
+  int64_t n = 0;
+  int q_per_seq = 1;
+};
+
 // Top-k over rows of `scores` [B][N].  The number of candidates of row b is
 // n_visible(q_pos, b, ratio, N) when n_valid is null, else n_valid[b].  When
 // `map` is non-null the selected position p is written as map[b*N + p].
 // pdl: launched as a programmatic dependent of the kernel before it.
 // Rows longer than 32768 entries are selected in three launches when
 // `scratch` holds topk_scratch_bytes(B, N, k) bytes, else by one slower
-// kernel.
+// kernel.  `pf`: the rows to request into L2 (none by default).
 cudaError_t launch_topk(const float* scores, int B, int64_t N, int k, const int32_t* q_pos,
                         int ratio, const int32_t* n_valid, const int32_t* map, int32_t* idx,
                         cudaStream_t stream, bool pdl = false, void* scratch = nullptr,
-                        size_t scratch_bytes = 0);
+                        size_t scratch_bytes = 0, const RowPrefetch& pf = RowPrefetch{});
 size_t topk_scratch_bytes(int B, int64_t N, int k);
 int topk_launches(int B, int64_t N, int k, size_t scratch_bytes);
 
@@ -193,8 +204,11 @@ cudaError_t launch_sparse_attn(const uint16_t* q_bf16, const uint8_t* kv_fp4, in
                                int32_t* status, cudaStream_t stream, bool pdl = false,
                                const SwaArgs* swa = nullptr, int32_t* idx_copy = nullptr);
 
-// tcgen05 kernel of one sparse-attention call (fp16 partials [B][nsplit][512][H]
-// and fp32 partial lse [B][nsplit][H] when nsplit > 1).
+// tcgen05 kernel of one sparse-attention call.  With nsplit > 1 (a power of
+// two, at most 8) a query's nsplit CTAs form one thread-block cluster that
+// writes fp16 partials part_o [B][nsplit][8 blocks][64 channels][H] (16-byte
+// chunks of a row swizzled) and partial lse part_lse [B][nsplit][H], then
+// merges them into `out` / `lse`.
 cudaError_t launch_sparse_attn_tc(const uint16_t* q_bf16, const uint8_t* kv_fp4, int B, int H,
                                   int64_t N, int64_t kv_seq_stride, int q_per_seq,
                                   const int32_t* idx, int k, int nsplit, int chunk,

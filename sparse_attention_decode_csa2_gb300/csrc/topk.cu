@@ -34,6 +34,19 @@ namespace {
 constexpr int kThreads = 1024;
 constexpr int kWarps = kThreads / 32;
 
+// The FP4 row of selected entry j of row b, requested into L2 for the
+// attention launched next (every 128-byte line the row touches; no effect on
+// the result).
+__device__ __forceinline__ void prefetch_row(const RowPrefetch& pf, int b, int32_t j) {
+  if (pf.kv != nullptr && j >= 0 && j < pf.n) {
+    const uint8_t* r = pf.kv + (int64_t)(b / pf.q_per_seq) * pf.seq_bytes + (int64_t)j * kRowBytes;
+#pragma unroll
+    for (int off = 0; off < kRowBytes; off += 128)
+      asm volatile("prefetch.global.L2 [%0];" ::"l"(r + off));
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(r + kRowBytes - 1));
+  }
+}
+
 struct TopkShared {
   int32_t hist[2048];
   int32_t warp_a[kWarps];
@@ -164,7 +177,8 @@ template <int KPT>
 __global__ void __launch_bounds__(kRegThreads, 1)
 topk_reg_kernel(const float* __restrict__ scores, int64_t N, int k,
                 const int32_t* __restrict__ q_pos, int ratio, const int32_t* __restrict__ n_valid,
-                const int32_t* __restrict__ map, int32_t* __restrict__ idx, int chunk) {
+                const int32_t* __restrict__ map, int32_t* __restrict__ idx, int chunk,
+                RowPrefetch pf) {
   // two sets of per-warp 8-bit digit histograms: one is counted into while
   // the other is cleared for the next pass; reused to stage the output
   __shared__ __align__(16) int32_t whist[2][kRegWarps * 256];
@@ -195,8 +209,11 @@ topk_reg_kernel(const float* __restrict__ scores, int64_t N, int k,
   }
   if (chunk) n = (int)max((int64_t)0, min((int64_t)chunk, (int64_t)n - pos0));
   if (n <= k) {
-    for (int j = tid; j < k; j += kRegThreads)
-      out[j] = (j < n) ? (mrow ? mrow[j] : (int32_t)(pos0 + j)) : -1;
+    for (int j = tid; j < k; j += kRegThreads) {
+      const int32_t v = (j < n) ? (mrow ? mrow[j] : (int32_t)(pos0 + j)) : -1;
+      out[j] = v;
+      prefetch_row(pf, b, v);
+    }
     return;
   }
 
@@ -345,10 +362,13 @@ topk_reg_kernel(const float* __restrict__ scores, int64_t N, int k,
     while (sel != 0u && off < k) {
       const int p = base + 32 * w + __ffs(sel) - 1;
       sel &= sel - 1u;
-      if (staged)
+      if (staged) {
         stage[off] = p;
-      else
-        out[off] = mrow ? mrow[p] : (int32_t)(pos0 + p);
+      } else {
+        const int32_t v = mrow ? mrow[p] : (int32_t)(pos0 + p);
+        out[off] = v;
+        prefetch_row(pf, b, v);
+      }
       ++off;
     }
   }
@@ -356,7 +376,9 @@ topk_reg_kernel(const float* __restrict__ scores, int64_t N, int k,
     __syncthreads();
     for (int j = tid; j < k; j += kRegThreads) {
       const int32_t p = stage[j];
-      out[j] = mrow ? mrow[p] : (int32_t)(pos0 + p);
+      const int32_t v = mrow ? mrow[p] : (int32_t)(pos0 + p);
+      out[j] = v;
+      prefetch_row(pf, b, v);
     }
   }
 }
@@ -426,7 +448,7 @@ __global__ void __launch_bounds__(kRegThreads, 1)
 topk_cluster_kernel(const float* __restrict__ scores, int64_t N, int k,
                     const int32_t* __restrict__ q_pos, int ratio,
                     const int32_t* __restrict__ n_valid, const int32_t* __restrict__ map,
-                    int32_t* __restrict__ idx) {
+                    int32_t* __restrict__ idx, RowPrefetch pf) {
   __shared__ __align__(16) int32_t whist[2][kRegWarps * 256];
   __shared__ __align__(16) int32_t csum[256];
   __shared__ __align__(16) int32_t pub[2][256];  // this CTA's digit counts (descending digits)
@@ -459,7 +481,11 @@ topk_cluster_kernel(const float* __restrict__ scores, int64_t N, int k,
   }
   if (n <= k) {  // the whole cluster leaves here together
     if (rank == 0)
-      for (int j = tid; j < k; j += kRegThreads) out[j] = (j < n) ? (mrow ? mrow[j] : j) : -1;
+      for (int j = tid; j < k; j += kRegThreads) {
+        const int32_t v = (j < n) ? (mrow ? mrow[j] : j) : -1;
+        out[j] = v;
+        prefetch_row(pf, b, v);
+      }
     return;
   }
 
@@ -631,7 +657,9 @@ topk_cluster_kernel(const float* __restrict__ scores, int64_t N, int k,
     while (sel != 0u && off < k) {
       const int p = base + 32 * w + __ffs(sel) - 1;
       sel &= sel - 1u;
-      out[off] = mrow ? mrow[p] : p;
+      const int32_t v = mrow ? mrow[p] : p;
+      out[off] = v;
+      prefetch_row(pf, b, v);
       ++off;
     }
   }
@@ -642,7 +670,7 @@ template <bool kSmem>
 __global__ void __launch_bounds__(kThreads, 1)
 topk_long_kernel(const float* __restrict__ scores, int64_t N, int k, const int32_t* __restrict__ q_pos,
             int ratio, const int32_t* __restrict__ n_valid, const int32_t* __restrict__ map,
-            int32_t* __restrict__ idx) {
+            int32_t* __restrict__ idx, RowPrefetch pf) {
   extern __shared__ __align__(16) uint8_t smem_raw[];
   TopkShared& sh = *reinterpret_cast<TopkShared*>(smem_raw);
   uint32_t* keys = reinterpret_cast<uint32_t*>(smem_raw + align_up(sizeof(TopkShared), 16));
@@ -678,6 +706,7 @@ topk_long_kernel(const float* __restrict__ scores, int64_t N, int k, const int32
       int32_t v = -1;
       if (j < n) v = mrow ? mrow[j] : j;
       out[j] = v;
+      prefetch_row(pf, b, v);
     }
     return;
   }
@@ -765,7 +794,11 @@ topk_long_kernel(const float* __restrict__ scores, int64_t N, int k, const int32
     int pos = sh.out_pos;
     for (int w = 0; w < warp; ++w) pos += sh.warp_b[w];
     pos += __popc(tm & lt_mask);
-    if (take && pos < k) out[pos] = mrow ? mrow[j] : j;
+    if (take && pos < k) {
+      const int32_t v = mrow ? mrow[j] : j;
+      out[pos] = v;
+      prefetch_row(pf, b, v);
+    }
     __syncthreads();
     if (tid == 0) {
       int te = 0, tt = 0;
@@ -843,15 +876,15 @@ bool chunked_ok(int64_t N, int k) {
 template <int KPT>
 cudaError_t launch_reg(dim3 grid, const float* scores, int64_t N, int k, const int32_t* q_pos,
                        int ratio, const int32_t* n_valid, const int32_t* map, int32_t* idx,
-                       int chunk, cudaStream_t stream, bool pdl) {
+                       int chunk, cudaStream_t stream, bool pdl, const RowPrefetch& pf) {
   return launch_kernel(topk_reg_kernel<KPT>, grid, dim3(kRegThreads), 0, stream, pdl, scores, N, k,
-                       q_pos, ratio, n_valid, map, idx, chunk);
+                       q_pos, ratio, n_valid, map, idx, chunk, pf);
 }
 
 template <int KPT, int CL>
 cudaError_t launch_cluster(int B, const float* scores, int64_t N, int k, const int32_t* q_pos,
                            int ratio, const int32_t* n_valid, const int32_t* map, int32_t* idx,
-                           cudaStream_t stream, bool pdl) {
+                           cudaStream_t stream, bool pdl, const RowPrefetch& pf) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(CL, (unsigned)B);
   cfg.blockDim = dim3(kRegThreads);
@@ -867,18 +900,19 @@ cudaError_t launch_cluster(int B, const float* scores, int64_t N, int k, const i
   cfg.attrs = attr;
   cfg.numAttrs = pdl ? 2 : 1;
   return cudaLaunchKernelEx(&cfg, topk_cluster_kernel<KPT, CL>, scores, N, k, q_pos, ratio,
-                            n_valid, map, idx);
+                            n_valid, map, idx, pf);
 }
 
 template <int CL>
 cudaError_t launch_cluster_kpt(int kpt, int B, const float* scores, int64_t N, int k,
                                const int32_t* q_pos, int ratio, const int32_t* n_valid,
-                               const int32_t* map, int32_t* idx, cudaStream_t stream, bool pdl) {
+                               const int32_t* map, int32_t* idx, cudaStream_t stream, bool pdl,
+                               const RowPrefetch& pf) {
   switch (kpt) {
-    case 4: return launch_cluster<4, CL>(B, scores, N, k, q_pos, ratio, n_valid, map, idx, stream, pdl);
-    case 8: return launch_cluster<8, CL>(B, scores, N, k, q_pos, ratio, n_valid, map, idx, stream, pdl);
-    case 16: return launch_cluster<16, CL>(B, scores, N, k, q_pos, ratio, n_valid, map, idx, stream, pdl);
-    default: return launch_cluster<32, CL>(B, scores, N, k, q_pos, ratio, n_valid, map, idx, stream, pdl);
+    case 4: return launch_cluster<4, CL>(B, scores, N, k, q_pos, ratio, n_valid, map, idx, stream, pdl, pf);
+    case 8: return launch_cluster<8, CL>(B, scores, N, k, q_pos, ratio, n_valid, map, idx, stream, pdl, pf);
+    case 16: return launch_cluster<16, CL>(B, scores, N, k, q_pos, ratio, n_valid, map, idx, stream, pdl, pf);
+    default: return launch_cluster<32, CL>(B, scores, N, k, q_pos, ratio, n_valid, map, idx, stream, pdl, pf);
   }
 }
 
@@ -889,7 +923,7 @@ cudaError_t launch_cluster_kpt(int kpt, int B, const float* scores, int64_t N, i
 // when the shape does not qualify.
 bool cluster_launch(int B, const float* scores, int64_t N, int k, const int32_t* q_pos,
                     int ratio, const int32_t* n_valid, const int32_t* map, int32_t* idx,
-                    cudaStream_t stream, bool pdl, cudaError_t* err) {
+                    cudaStream_t stream, bool pdl, cudaError_t* err, const RowPrefetch& pf) {
   const int sms = device_sm_count();
   int CL = 0;
   for (int c = 8; c >= 2 && CL == 0; c >>= 1)
@@ -900,25 +934,25 @@ bool cluster_launch(int B, const float* scores, int64_t N, int k, const int32_t*
   while ((int64_t)kpt * kRegThreads < per) kpt *= 2;
   if (kpt > 32) return false;
   *err = CL == 8 ? launch_cluster_kpt<8>(kpt, B, scores, N, k, q_pos, ratio, n_valid, map, idx,
-                                          stream, pdl)
+                                          stream, pdl, pf)
        : CL == 4 ? launch_cluster_kpt<4>(kpt, B, scores, N, k, q_pos, ratio, n_valid, map, idx,
-                                          stream, pdl)
+                                          stream, pdl, pf)
                  : launch_cluster_kpt<2>(kpt, B, scores, N, k, q_pos, ratio, n_valid, map, idx,
-                                          stream, pdl);
+                                          stream, pdl, pf);
   return true;
 }
 
 cudaError_t launch_reg_any(dim3 grid, const float* scores, int64_t N, int64_t keys, int k,
                            const int32_t* q_pos, int ratio, const int32_t* n_valid,
                            const int32_t* map, int32_t* idx, int chunk, cudaStream_t stream,
-                           bool pdl) {
+                           bool pdl, const RowPrefetch& pf) {
   if (keys <= kRegThreads * 8)
-    return launch_reg<8>(grid, scores, N, k, q_pos, ratio, n_valid, map, idx, chunk, stream, pdl);
+    return launch_reg<8>(grid, scores, N, k, q_pos, ratio, n_valid, map, idx, chunk, stream, pdl, pf);
   if (keys <= kRegThreads * 16)
-    return launch_reg<16>(grid, scores, N, k, q_pos, ratio, n_valid, map, idx, chunk, stream, pdl);
+    return launch_reg<16>(grid, scores, N, k, q_pos, ratio, n_valid, map, idx, chunk, stream, pdl, pf);
   if (keys <= kRegThreads * 32)
-    return launch_reg<32>(grid, scores, N, k, q_pos, ratio, n_valid, map, idx, chunk, stream, pdl);
-  return launch_reg<64>(grid, scores, N, k, q_pos, ratio, n_valid, map, idx, chunk, stream, pdl);
+    return launch_reg<32>(grid, scores, N, k, q_pos, ratio, n_valid, map, idx, chunk, stream, pdl, pf);
+  return launch_reg<64>(grid, scores, N, k, q_pos, ratio, n_valid, map, idx, chunk, stream, pdl, pf);
 }
 
 struct LongScratch {
@@ -961,13 +995,15 @@ int topk_launches(int B, int64_t N, int k, size_t scratch_bytes) {
 
 cudaError_t launch_topk(const float* scores, int B, int64_t N, int k, const int32_t* q_pos,
                         int ratio, const int32_t* n_valid, const int32_t* map, int32_t* idx,
-                        cudaStream_t stream, bool pdl, void* scratch, size_t scratch_bytes) {
+                        cudaStream_t stream, bool pdl, void* scratch, size_t scratch_bytes,
+                        const RowPrefetch& pf) {
   if (B == 0) return cudaSuccess;
   if (N <= kRegMaxKeys) {
     cudaError_t e;
-    if (cluster_launch(B, scores, N, k, q_pos, ratio, n_valid, map, idx, stream, pdl, &e)) return e;
+    if (cluster_launch(B, scores, N, k, q_pos, ratio, n_valid, map, idx, stream, pdl, &e, pf))
+      return e;
     return launch_reg_any(dim3((unsigned)B), scores, N, N, k, q_pos, ratio, n_valid, map, idx, 0,
-                          stream, pdl);
+                          stream, pdl, pf);
   }
   const size_t need = topk_scratch_bytes(B, N, k);
   if (!map && need > 0 && scratch && scratch_bytes >= need) {
@@ -984,7 +1020,7 @@ cudaError_t launch_topk(const float* scores, int B, int64_t N, int k, const int3
       const int C = long_chunks(M);
       e = launch_reg_any(dim3((unsigned)C, (unsigned)B), cur_score, M, kRegMaxKeys, k, cur_pos,
                          cur_ratio, cur_count, nullptr, ls.sel, kRegMaxKeys, stream,
-                         lvl == 0 ? pdl : true);
+                         lvl == 0 ? pdl : true, RowPrefetch{});
       if (e != cudaSuccess) return e;
       const int o = lvl & 1;
       e = launch_kernel(topk_pack_kernel, dim3((unsigned)B), dim3(256), 0, stream, true, cur_score,
@@ -998,14 +1034,14 @@ cudaError_t launch_topk(const float* scores, int B, int64_t N, int k, const int3
       M = (int64_t)C * k;
     }
     // the packed ids serve as the map: the selected candidates' entry ids
-    if (cluster_launch(B, cur_score, M, k, nullptr, 1, nullptr, cur_id, idx, stream, true, &e))
+    if (cluster_launch(B, cur_score, M, k, nullptr, 1, nullptr, cur_id, idx, stream, true, &e, pf))
       return e;
     return launch_reg_any(dim3((unsigned)B), cur_score, M, M, k, nullptr, 1, nullptr, cur_id, idx,
-                          0, stream, true);
+                          0, stream, true, pf);
   }
   const size_t base = align_up(sizeof(TopkShared), 16);
   return launch_kernel(topk_long_kernel<false>, dim3((unsigned)B), dim3(kThreads), base, stream,
-                       pdl, scores, N, k, q_pos, ratio, n_valid, map, idx);
+                       pdl, scores, N, k, q_pos, ratio, n_valid, map, idx, pf);
 }
 
 }  // namespace csa2

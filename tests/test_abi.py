@@ -135,16 +135,16 @@ def test_layer_group_launch_counts(libpath):
     count = lambda layers, g: csa2.lib.csa2_layer_group_launches(layers, len(layers),
                                                                   ctypes.byref(g))
     # without a device the SM count defaults to 148: 4 splits of 512 slots for 32 queries,
-    # so every attention is a kernel plus its merge
+    # merged inside the attention kernel (one cluster per query)
     layers, g = _group(csa2, [0])
-    assert count(layers, g) == 1 + 1 + 2                  # indexer, top-k, attention + merge
+    assert count(layers, g) == 1 + 1 + 1                  # indexer, top-k, attention
     layers, g = _group(csa2, [0, 2, 1, 2])
-    assert count(layers, g) == 4 + 2 + (2 + 2) + 2        # Reindex: scores + top-k
+    assert count(layers, g) == 3 + 1 + (2 + 1) + 1        # Reindex: scores + top-k
     layers, g = _group(csa2, [0, 1], pool=8192)
-    assert count(layers, g) == (1 + 1 + 1 + 2) + (2 + 2)  # Full also selects the pool
+    assert count(layers, g) == (1 + 1 + 1 + 1) + (2 + 1)  # Full also selects the pool
     layers, g = _group(csa2, [0, 1], pool=16384, pool_block=8)
-    assert count(layers, g) == (1 + 3 + 1 + 2) + (2 + 2)  # blockwise pool: three kernels
-    # 160 queries: one CTA per query, no merge kernel
+    assert count(layers, g) == (1 + 3 + 1 + 1) + (2 + 1)  # blockwise pool: three kernels
+    # 160 queries: one CTA per query
     layers, g = _group(csa2, [0, 2], B=160, k=2048)
     assert count(layers, g) == (1 + 1 + 1) + 1
     layers, g = _group(csa2, [2, 0])                      # no Full layer first

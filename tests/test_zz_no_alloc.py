@@ -41,7 +41,7 @@ def test_noalloc_matches_workspace_entry_point_on_two_calls():
     build.build()
     from sparse_attention_decode_csa2_gb300 import csa2
     lib = csa2.lib
-    B, H, N, k = 4, 64, 5000, 4096       # 32 split chunks per query, merged through scratch
+    B, H, N, k = 4, 64, 5000, 4096       # 8 split chunks per query, merged through scratch
     assert csa2.workspace_size(B, 0, k, H, 0) > 256
     for seed in (1, 2):                  # two calls in a row, different inputs
         q, kv, idx = _case(seed, B, H, N, k)
