@@ -467,6 +467,26 @@ topk_cluster_kernel(const float* __restrict__ scores, int64_t N, int k,
   const int32_t* mrow = map ? map + (int64_t)b * N : nullptr;
   int32_t* out = idx + (int64_t)b * k;
 
+  const int base = (int)rank * (KPT * kRegThreads) + tid * KPT;  // row position of key[0]
+  uint32_t key[KPT];
+  const bool vec = ((N & 3) == 0) && ((reinterpret_cast<uintptr_t>(scores) & 15u) == 0);
+  // the whole row range (entries n .. N - 1 are read, never counted): the
+  // loads need not wait for the candidate count
+#pragma unroll
+  for (int i = 0; i < KPT; i += 4) {
+    const int j = base + i;
+    float v[4];
+    if (vec && j + 3 < N) {
+      const float4 f = *reinterpret_cast<const float4*>(row + j);
+      v[0] = f.x; v[1] = f.y; v[2] = f.z; v[3] = f.w;
+    } else {
+#pragma unroll
+      for (int e = 0; e < 4; ++e) v[e] = (j + e < N) ? row[j + e] : 0.0f;
+    }
+#pragma unroll
+    for (int e = 0; e < 4; ++e) key[i + e] = float_to_ordered(v[e]);
+  }
+
   int n;  // candidates of the row, the same in every CTA of the cluster
   if (map) {
     int c = 0;
@@ -489,25 +509,10 @@ topk_cluster_kernel(const float* __restrict__ scores, int64_t N, int k,
     return;
   }
 
-  const int base = (int)rank * (KPT * kRegThreads) + tid * KPT;  // row position of key[0]
-  uint32_t key[KPT];
-  const bool vec = ((N & 3) == 0) && ((reinterpret_cast<uintptr_t>(scores) & 15u) == 0);
-#pragma unroll
-  for (int i = 0; i < KPT; i += 4) {
-    const int j = base + i;
-    float v[4];
-    if (vec && j + 3 < n) {
-      const float4 f = *reinterpret_cast<const float4*>(row + j);
-      v[0] = f.x; v[1] = f.y; v[2] = f.z; v[3] = f.w;
-    } else {
-#pragma unroll
-      for (int e = 0; e < 4; ++e) v[e] = (j + e < n) ? row[j + e] : 0.0f;
-    }
-#pragma unroll
-    for (int e = 0; e < 4; ++e) key[i + e] = float_to_ordered(v[e]);
-  }
-
-  // OR / AND of the keys per sign (see topk_reg_kernel), over the cluster
+  // OR / AND of the keys per sign (see topk_reg_kernel), over the cluster.
+  // They travel with the first pass, which takes the fixed top digit (bits
+  // 31..24) of every candidate: one cluster exchange fewer than finding the
+  // differing bit range first.
   uint32_t por = 0u, pand = 0xFFFFFFFFu, nor = 0u, nand = 0xFFFFFFFFu;
 #pragma unroll
   for (int i = 0; i < KPT; ++i) {
@@ -531,50 +536,38 @@ topk_cluster_kernel(const float* __restrict__ scores, int64_t N, int k,
   }
   for (int i = tid; i < kRegWarps * 256; i += kRegThreads) whist[0][i] = 0;
   __syncthreads();
+  {
+    int32_t* my_hist = whist[0] + warp * 256;
+#pragma unroll
+    for (int i = 0; i < KPT; ++i)
+      if (base + i < n) atomicAdd(&my_hist[key[i] >> 24], 1);
+  }
   if (tid < 4) {
     uint32_t v = (tid & 1) ? 0xFFFFFFFFu : 0u;
 #pragma unroll
     for (int w = 0; w < kRegWarps; ++w) v = (tid & 1) ? (v & red[tid][w]) : (v | red[tid][w]);
     pub_bits[tid] = v;
   }
-  cluster_barrier();
-  if (tid < 4 * CL) all_bits[tid] = ld_peer(&pub_bits[tid & 3], (uint32_t)(tid >> 2));
-  __syncthreads();
-  por = 0u; pand = 0xFFFFFFFFu; nor = 0u; nand = 0xFFFFFFFFu;
-#pragma unroll
-  for (int r = 0; r < CL; ++r) {
-    por |= all_bits[4 * r];
-    pand &= all_bits[4 * r + 1];
-    nor |= all_bits[4 * r + 2];
-    nand &= all_bits[4 * r + 3];
-  }
-  const int lo_pos = (por ^ pand) ? __ffs(por ^ pand) - 1 : 32;
-  const int lo_neg = (nor ^ nand) ? __ffs(nor ^ nand) - 1 : 32;
-  const uint32_t kor = por | nor, kand = pand & nand;
 
-  uint32_t prefix = kand, mask = 0xFFFFFFFFu;
-  int cur_hi = -1, lo = 0;
-  if (kor != kand) {
-    cur_hi = 31 - __clz(kor ^ kand);
-    mask = ~((2u << cur_hi) - 1u);
-    prefix = kand & mask;
-    lo = min(cur_hi, cur_hi == 31 ? min(lo_pos, lo_neg) : ((kor >> 31) ? lo_pos : lo_neg));
-  }
   int need = k;
   // this thread's share (digit 255 - tid) of the keys above the class / inside
   // it held by the lower-ranked CTAs, summed over the block after the passes
   int gt_part = 0, eq_part = 0;
   bool any_pass = false;
+  uint32_t prefix = 0u, mask = 0u;
+  int cur_hi = 31, lo = 0;
   for (int pass = 0; cur_hi >= lo; ++pass) {
-    const int nbits = min(8, cur_hi + 1 - lo);
+    const int nbits = pass == 0 ? 8 : min(8, cur_hi + 1 - lo);
     const int shift = cur_hi + 1 - nbits;
     const uint32_t dmask = (1u << nbits) - 1u;
     int32_t* hist = whist[pass & 1];
-    int32_t* my_hist = hist + warp * 256;
+    if (pass > 0) {
+      int32_t* my_hist = hist + warp * 256;
 #pragma unroll
-    for (int i = 0; i < KPT; ++i) {
-      if (base + i < n && (key[i] & mask) == prefix)
-        atomicAdd(&my_hist[(key[i] >> shift) & dmask], 1);
+      for (int i = 0; i < KPT; ++i) {
+        if (base + i < n && (key[i] & mask) == prefix)
+          atomicAdd(&my_hist[(key[i] >> shift) & dmask], 1);
+      }
     }
     __syncthreads();
     if (tid < 256) {
@@ -588,6 +581,8 @@ topk_cluster_kernel(const float* __restrict__ scores, int64_t N, int k,
       for (int i = tid - 256; i < kRegWarps * 256; i += kRegThreads - 256) next[i] = 0;
     }
     cluster_barrier();
+    if (pass == 0 && tid >= 256 && tid < 256 + 4 * CL)
+      all_bits[tid - 256] = ld_peer(&pub_bits[(tid - 256) & 3], (uint32_t)((tid - 256) >> 2));
     int lower = 0;  // this digit's count in the lower-ranked CTAs
     if (tid < 256) {
       int c = 0;
@@ -610,6 +605,18 @@ topk_cluster_kernel(const float* __restrict__ scores, int64_t N, int k,
     prefix |= (uint32_t)digit << shift;
     mask |= dmask << shift;
     cur_hi = shift - 1;
+    if (pass == 0) {  // the lowest bit that differs between two keys, per sign
+      por = 0u; pand = 0xFFFFFFFFu; nor = 0u; nand = 0xFFFFFFFFu;
+#pragma unroll
+      for (int r = 0; r < CL; ++r) {
+        por |= all_bits[4 * r];
+        pand &= all_bits[4 * r + 1];
+        nor |= all_bits[4 * r + 2];
+        nand &= all_bits[4 * r + 3];
+      }
+    }
+    const int lo_pos = (por ^ pand) ? __ffs(por ^ pand) - 1 : 32;
+    const int lo_neg = (nor ^ nand) ? __ffs(nor ^ nand) - 1 : 32;
     lo = (prefix >> 31) ? lo_pos : lo_neg;
     if (cnt == need) break;
   }
