@@ -189,12 +189,19 @@ def algorithmic_bytes(w):
     return total, per_layer
 
 
+QUANT_D_MX = 128   # indexer-key width the MXFP4 packer is timed on
+
+
 def kernel_bytes(w):
-    """Algorithmic bytes of each timed component op (one launch over the batch)."""
+    """Algorithmic bytes of each timed component op (one launch over the batch;
+    the packers over the whole cache of the workload: fp32 read + packed write)."""
     B, N, k = w.B, w.N, w.k
     n_scored = sum(min(N, (int(p) + 1) // w.ratio) for p in w.q_pos())
     n_win = sum(min(w.n_win, int(p) + 1) for p in w.q_pos() if p >= 0) if w.n_win else 0
+    rows = w.n_seq * N
     return {
+        "quantize_kv_fp4": rows * (w.D * 4 + w.row_bytes),
+        "quantize_mxfp4": rows * (QUANT_D_MX * 4 + QUANT_D_MX // 2 + QUANT_D_MX // 32),
         "index_scores": n_scored * w.idx_row_bytes + B * w.H_I * w.idx_row_bytes + B * N * 4,
         "topk": n_scored * 4 + B * k * 4,
         "sparse_attn_fp4": B * k * (w.row_bytes + 4) + n_win * w.D + B * w.H * w.D * (2 + 4) +
@@ -286,6 +293,14 @@ def run_gpu(args, rank, world, local):
         (lambda: csa2.sparse_attn_fp4(inp.q[0], inp.kv_fp4, w.N, w.kv_seq_stride, w.q_per_seq,
                                       idx, inp.scale, out=out, lse=lse, ws=ws)),
     }
+    # the packers, over the workload's whole cache (timed alone, not in the step)
+    qrows = w.n_seq * w.N
+    qx = torch.randn((qrows, w.D), dtype=torch.float32, device=dev)
+    qo = torch.empty((qrows, w.row_bytes), dtype=torch.uint8, device=dev)
+    mx = torch.randn((qrows, QUANT_D_MX), dtype=torch.float32, device=dev)
+    mo = torch.empty((qrows, QUANT_D_MX // 2 + QUANT_D_MX // 32), dtype=torch.uint8, device=dev)
+    ops["quantize_kv_fp4"] = lambda: csa2.quantize_kv_fp4(qx, out=qo)
+    ops["quantize_mxfp4"] = lambda: csa2.quantize_mxfp4(mx, out=mo)
     for name, fn in ops.items():
         fn()
         torch.cuda.synchronize()
@@ -299,58 +314,69 @@ def run_gpu(args, rank, world, local):
         torch.cuda.synchronize()
         comp[name] = statistics.mean(a.elapsed_time(b) for a, b in e)
     clocks = sampler.stop()
+    del qx, qo, mx, mo
 
     # end to end through the public API with host buffers.  The FP4 cache, the
     # indexer K and the SWA rings are state that stays resident across decode
     # steps; what a step brings in from the host is its queries (main and
     # indexer, every layer), their positions and the cache entries its tokens
-    # append (the entries holding the queries' positions, and each layer's SWA
-    # ring row of the newest token).  Those are copied from pinned host memory
-    # into the resident buffers every step, then the layer group runs and every
-    # layer's output is copied back.  The step is timed twice: issued call by
-    # call, and as a serving loop runs it, one CUDA graph per step that holds
-    # the copies in, the layer group and the copies out (the graph's copy nodes
-    # read and write the pinned host buffers on every replay).
+    # append: the new main-KV entries as fp32 latent rows (packed into FP4 on
+    # the device), their indexer keys and each layer's SWA ring row of the
+    # newest token.  All of it sits in one pinned buffer that csa2_upload moves
+    # with one copy and places with one kernel; then the layer group runs and
+    # every layer's output is copied back.  The step is timed twice: issued
+    # call by call, and as one CUDA graph per step (the graph's copy nodes read
+    # and write the pinned host buffers on every replay).
     e2e = None
     if not args.no_e2e:
+        from sparse_attention_decode_csa2_gb300 import csa2 as _c
         S, N = w.n_seq, w.N
         pos = w.q_pos()
         ents = np.clip(pos.astype(np.int64) // w.ratio, 0, N - 1)
         e_lo, e_hi = int(ents.min()), int(ents.max())
-        kv3 = inp.kv_fp4.view(S, N, w.row_bytes)[:, e_lo:e_hi + 1]
-        ki3 = inp.ki_fp8.view(S, N, w.idx_row_bytes)[:, e_lo:e_hi + 1]
-        host_in = {
-            "kv_new": kv3.cpu().pin_memory(), "ki_new": ki3.cpu().pin_memory(),
-            "q": [t.cpu().pin_memory() for t in inp.q],
-            "qi": [None if t is None else t.cpu().pin_memory() for t in inp.qi],
-            "q_pos": inp.q_pos.cpu().pin_memory(),
-        }
-        swa_rows = []
+        kv3 = inp.kv_fp4.view(S, N, w.row_bytes)
+        ki3 = inp.ki_fp8.view(S, N, w.idx_row_bytes)
+        segs, fills = [], []
+        rows = np.arange(e_lo, e_hi + 1)
+        if e_lo == e_hi:   # one appended entry per sequence, at the same index
+            segs.append((_c.UPLOAD_KV_FP4, kv3[:, e_lo]))
+            fills.append(np.concatenate([w.kv_latent_rows(s_, rows) for s_ in range(S)]))
+            segs.append((_c.UPLOAD_RAW, ki3[:, e_lo]))
+            fills.append(ki3[:, e_lo].cpu().numpy())
+        else:
+            for s_ in range(S):
+                segs.append((_c.UPLOAD_KV_FP4, kv3[s_, e_lo:e_hi + 1]))
+                fills.append(w.kv_latent_rows(s_, rows))
+                segs.append((_c.UPLOAD_RAW, ki3[s_, e_lo:e_hi + 1]))
+                fills.append(ki3[s_, e_lo:e_hi + 1].cpu().numpy())
         if w.n_win:
-            # ring rows of the step's tokens (one run of rows for every sequence here)
             r_lo, r_hi = int(pos.min()) % w.swa_ring, int(pos.max()) % w.swa_ring
             if r_hi - r_lo == int(pos.max() - pos.min()):
-                swa_rows = [(t[:, r_lo:r_hi + 1], t[:, r_lo:r_hi + 1].cpu().pin_memory())
-                            for t in inp.swa]
+                for t in inp.swa:   # the ring rows of the step's tokens
+                    for s_ in range(S):
+                        segs.append((_c.UPLOAD_RAW, t[s_, r_lo:r_hi + 1]))
+                        fills.append(t[s_, r_lo:r_hi + 1].cpu().numpy())
+        for t in inp.q:
+            v = t.view(-1, 512)
+            segs.append((_c.UPLOAD_RAW, v))
+            fills.append(v.cpu().numpy())
+        for t in inp.qi:
+            if t is not None:
+                v = t.view(t.shape[0], -1)
+                segs.append((_c.UPLOAD_RAW, v))
+                fills.append(v.cpu().numpy())
+        segs.append((_c.UPLOAD_RAW, inp.q_pos.view(1, -1)))
+        fills.append(inp.q_pos.view(1, -1).cpu().numpy())
+        up = _c.StepUpload(segs, device=dev)
+        for pay, f in zip(up.payloads, fills):
+            pay.copy_(torch.from_numpy(np.ascontiguousarray(f)).view(pay.dtype).view(pay.shape))
         host_out = [torch.empty_like(o, device="cpu").pin_memory() for o in lg.out]
-        h2d = (host_in["kv_new"].numel() + host_in["ki_new"].numel()
-               + host_in["q_pos"].numel() * 4
-               + sum(t.numel() * 2 for t in host_in["q"])
-               + sum(t.numel() for t in host_in["qi"] if t is not None)
-               + sum(h.numel() for _, h in swa_rows))
+        ref_out = [o.clone() for o in lg.out]
+        h2d = up.bytes
         d2h = sum(o.numel() * 4 for o in host_out)
 
         def e2e_step():
-            kv3.copy_(host_in["kv_new"], non_blocking=True)
-            ki3.copy_(host_in["ki_new"], non_blocking=True)
-            for d, h in swa_rows:
-                d.copy_(h, non_blocking=True)
-            inp.q_pos.copy_(host_in["q_pos"], non_blocking=True)
-            for d, h in zip(inp.q, host_in["q"]):
-                d.copy_(h, non_blocking=True)
-            for d, h in zip(inp.qi, host_in["qi"]):
-                if d is not None:
-                    d.copy_(h, non_blocking=True)
+            up()
             outs, _, _, _ = lg()
             for h, o in zip(host_out, outs):
                 h.copy_(o, non_blocking=True)
@@ -358,6 +384,9 @@ def run_gpu(args, rank, world, local):
         for _ in range(max(1, min(W, 3))):
             e2e_step()
         torch.cuda.synchronize()
+        # the uploaded step reproduces the resident one (appended rows packed
+        # on the device are the cache's own bytes)
+        same = all(torch.equal(h, r.cpu()) for h, r in zip(host_out, ref_out))
         Ke = max(3, min(K, 10))
 
         def timed(step):
@@ -370,11 +399,23 @@ def run_gpu(args, rank, world, local):
             torch.cuda.synchronize()
             return allreduce_max(e0.elapsed_time(e1) / 1e3, world)
 
+        # the transfers alone (same buffers, same stream): where the e2e time goes
+        def d2h_only():
+            for h, o in zip(host_out, lg.out):
+                h.copy_(o, non_blocking=True)
+
+        parts = {"upload_ms": timed(up) / Ke * 1e3, "d2h_ms": timed(d2h_only) / Ke * 1e3}
         eager_s = timed(e2e_step)
         eager_v = step_throughput(w.B, Ke, world, eager_s, len(w.modes))
         e2e = {"value": eager_v, "unit": UNIT, "h2d_bytes_per_step": int(h2d),
                "d2h_bytes_per_step": int(d2h), "eager_value": eager_v,
-               "inputs": "queries, positions and the appended cache entries; cache resident",
+               "inputs": ("queries, positions and the appended entries (main KV as fp32 latent, "
+                          "packed to FP4 on the device; indexer keys; SWA rows) in one pinned "
+                          "buffer, one copy + one placing kernel; cache resident"),
+               "outputs_match_resident_run": bool(same),
+               "parts_ms": parts,
+               "h2d_gbs": h2d / (parts["upload_ms"] / 1e3) / 1e9,
+               "d2h_gbs": d2h / (parts["d2h_ms"] / 1e3) / 1e9,
                "issue": "call by call"}
         try:
             g_e2e = torch.cuda.CUDAGraph()
@@ -386,7 +427,7 @@ def run_gpu(args, rank, world, local):
             torch.cuda.synchronize()
             graph_s = timed(g_e2e.replay)
             e2e["value"] = step_throughput(w.B, Ke, world, graph_s, len(w.modes))
-            e2e["issue"] = ("one CUDA graph per step: copies in, layer group, copies out "
+            e2e["issue"] = ("one CUDA graph per step: packed upload, layer group, copies out "
                             "(eager_value: the same step issued call by call)")
         except RuntimeError as ex:  # keep the call-by-call number, say why
             torch.cuda.synchronize()
@@ -399,8 +440,10 @@ def run_gpu(args, rank, world, local):
     hbm_peak, bf16_peak, peak_src = measured_peaks()
     step_bytes, _ = algorithmic_bytes(w)
     kb = kernel_bytes(w)
-    dom = max(comp, key=comp.get)
+    step_ops = ("index_scores", "topk", "sparse_attn_fp4")
+    dom = max(step_ops, key=comp.get)   # the step's dominant kernel
     achieved = kb[dom] / (comp[dom] / 1e3) / 1e9
+    kernels_frac = {n: kb[n] / (comp[n] / 1e3) / 1e9 / hbm_peak for n in comp}
     traffic = None
     tpath = os.path.join(ROOT, "profiles", "traffic.json")
     if os.path.exists(tpath):
@@ -444,6 +487,8 @@ def run_gpu(args, rank, world, local):
                      "unit": "GB/s", "frac": achieved / hbm_peak, "traffic": traffic,
                      "peak_source": peak_src},
         "kernels_ms": comp,
+        "kernels_hbm_frac": kernels_frac,
+        "kernels_bytes": {n: int(kb[n]) for n in comp},
         "attn_tflops": attn_flops(w) / (comp["sparse_attn_fp4"] / 1e3) / 1e12,
         "gpu_launches": n_launch * K,
         "clocks": clocks,

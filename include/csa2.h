@@ -103,6 +103,44 @@ csa2_status csa2_quantize_kv_fp4(const float* x, int64_t n_rows, int d, uint8_t*
                                  cudaStream_t stream);
 
 /*
+ * csa2_upload -- a decode step's host inputs in one host-to-device copy.
+ * The pages have no counterpart: this is the serving-side transfer of a
+ * step's inputs into the resident buffers the other calls read.
+ *   host_packed  host buffer of `bytes` bytes (pinned for an asynchronous
+ *                copy): n_segs csa2_upload_seg entries at offset 0, then the
+ *                segments' payloads at the offsets the entries give
+ *   dev_stage    device staging area, >= bytes, 16-byte aligned; the whole
+ *                buffer is copied there (one cudaMemcpyAsync), then one kernel
+ *                writes each segment's rows to its destination:
+ *     CSA2_UPLOAD_RAW     rows x row_bytes payload bytes, row r to
+ *                         dst + r * dst_stride
+ *     CSA2_UPLOAD_KV_FP4  rows x 512 fp32 latent channels (row_bytes = 2048),
+ *                         each packed exactly as csa2_quantize_kv_fp4 packs it
+ *                         into the 288-byte FP4 row at dst + r * dst_stride
+ *                         (dst and dst_stride multiples of 16, dst_stride >= 288)
+ *   Segments are applied in table order (a later segment overwriting the same
+ *   bytes wins).  Payload offsets must be 16-byte aligned and lie inside
+ *   `bytes`; the table is validated on the host before anything is enqueued
+ *   (CSA2_ERR_INVALID_ARG).  Destinations are device addresses owned by the
+ *   caller; the staging area must not be reused until the stream has passed
+ *   the kernel.
+ */
+typedef enum csa2_upload_kind { CSA2_UPLOAD_RAW = 0, CSA2_UPLOAD_KV_FP4 = 1 } csa2_upload_kind;
+
+typedef struct csa2_upload_seg {
+  uint64_t dst;         /* device address of destination row 0 */
+  uint64_t src_off;     /* byte offset of the payload in the packed buffer */
+  uint64_t rows;        /* rows of the segment */
+  uint64_t row_bytes;   /* payload bytes per row (2048 for CSA2_UPLOAD_KV_FP4) */
+  uint64_t dst_stride;  /* bytes between destination rows */
+  uint32_t kind;        /* csa2_upload_kind */
+  uint32_t reserved;    /* 0 */
+} csa2_upload_seg;      /* 48 bytes */
+
+csa2_status csa2_upload(const void* host_packed, size_t bytes, int n_segs, void* dev_stage,
+                        size_t stage_bytes, cudaStream_t stream);
+
+/*
  * csa2_index_scores -- the lightweight indexer (walkthrough 1.(4) "CSA2":
  * indexer Q and indexer K score main-KV entries).
  *   q_fp8    E4M3 [B][H_I][D_I] indexer queries

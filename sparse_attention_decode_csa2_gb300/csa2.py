@@ -62,6 +62,13 @@ class Csa2GroupArgs(ctypes.Structure):
 
 
 INDEXER_E4M3, INDEXER_MXFP4 = 0, 1
+UPLOAD_RAW, UPLOAD_KV_FP4 = 0, 1
+
+
+class Csa2UploadSeg(ctypes.Structure):
+    _fields_ = [("dst", ctypes.c_uint64), ("src_off", ctypes.c_uint64), ("rows", ctypes.c_uint64),
+                ("row_bytes", ctypes.c_uint64), ("dst_stride", ctypes.c_uint64),
+                ("kind", ctypes.c_uint32), ("reserved", ctypes.c_uint32)]
 
 
 def mxfp4_row_bytes(d: int) -> int:
@@ -80,6 +87,7 @@ _SIGS = {
     "csa2_version": (_i32, []),
     "csa2_last_cuda_error": (ctypes.c_char_p, []),
     "csa2_quantize_kv_fp4": (_i32, [_vp, _i64, _i32, _vp, _vp]),
+    "csa2_upload": (_i32, [_vp, _sz, _i32, _vp, _sz, _vp]),
     "csa2_index_scores": (_i32, [_vp, _vp, _i32, _i32, _i32, _i64, _i64, _i32, _vp, _i32, _vp,
                                  _vp]),
     "csa2_quantize_mxfp4": (_i32, [_vp, _i64, _i32, _vp, _vp]),
@@ -198,6 +206,57 @@ def quantize_kv_fp4(x: torch.Tensor, out: Optional[torch.Tensor] = None) -> torc
     _out(out, (n, d // 2 + d // 16), torch.uint8, "out")
     _check(lib.csa2_quantize_kv_fp4(_ptr(x), n, d, _ptr(out), _stream()), "csa2_quantize_kv_fp4")
     return out
+
+
+class StepUpload:
+    """One packed host-to-device transfer per decode step (csa2_upload).
+
+    ``segments`` lists the step's inputs as ``(kind, dst)`` pairs: ``dst`` is a
+    2-D device tensor view whose rows receive the segment (rows may be strided,
+    each row contiguous).  UPLOAD_RAW copies the row bytes as they are;
+    UPLOAD_KV_FP4 takes fp32 latent rows of 512 channels and writes them into
+    ``dst``'s 288-byte FP4 rows (as csa2_quantize_kv_fp4 packs them).  The
+    pinned host buffer (table + payloads) and the device staging area are
+    allocated once; ``payloads[i]`` is the host view the caller fills with
+    segment i's rows before each call."""
+
+    def __init__(self, segments, device=None):
+        specs = []
+        for kind, dst in segments:
+            if dst.dim() != 2 or dst.stride(1) != 1 or not dst.is_cuda:
+                raise ValueError("a segment destination is a 2-D CUDA view with contiguous rows")
+            esz = dst.element_size()
+            if kind == UPLOAD_KV_FP4:
+                if dst.dtype != torch.uint8 or dst.shape[1] != ROW_BYTES:
+                    raise ValueError("an FP4 segment writes uint8 rows of 288 bytes")
+                row_bytes, pshape, pdtype = D_LATENT * 4, (dst.shape[0], D_LATENT), torch.float32
+            elif kind == UPLOAD_RAW:
+                row_bytes, pshape, pdtype = dst.shape[1] * esz, tuple(dst.shape), dst.dtype
+            else:
+                raise ValueError(f"unknown segment kind {kind}")
+            specs.append((kind, dst, row_bytes, pshape, pdtype, dst.stride(0) * esz))
+        self.n = len(specs)
+        off = (self.n * ctypes.sizeof(Csa2UploadSeg) + 15) // 16 * 16
+        table = (Csa2UploadSeg * max(1, self.n))()
+        offs = []
+        for i, (kind, dst, row_bytes, pshape, pdtype, stride) in enumerate(specs):
+            table[i] = Csa2UploadSeg(dst.data_ptr(), off, dst.shape[0], row_bytes, stride, kind, 0)
+            offs.append(off)
+            off += (dst.shape[0] * row_bytes + 15) // 16 * 16
+        self.bytes = max(off, 16)
+        self.host = torch.zeros(self.bytes, dtype=torch.uint8).pin_memory()
+        nt = self.n * ctypes.sizeof(Csa2UploadSeg)
+        if nt:
+            ctypes.memmove(self.host.data_ptr(), ctypes.addressof(table), nt)
+        self.stage = torch.empty(self.bytes, dtype=torch.uint8,
+                                 device=device if device is not None else specs[0][1].device)
+        self.payloads = [self.host[o:o + pshape[0] * rb].view(pdtype).view(pshape)
+                         for o, (_, _, rb, pshape, pdtype, _) in zip(offs, specs)]
+        self._keep = [sp[1] for sp in specs]   # the destinations outlive the table
+
+    def __call__(self) -> None:
+        _check(lib.csa2_upload(self.host.data_ptr(), self.bytes, self.n, self.stage.data_ptr(),
+                               self.bytes, _stream()), "csa2_upload")
 
 
 def index_scores(q_fp8: torch.Tensor, k_fp8: torch.Tensor, N: int, kv_seq_stride: int,

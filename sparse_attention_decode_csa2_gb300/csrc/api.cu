@@ -174,6 +174,37 @@ csa2_status csa2_quantize_kv_fp4(const float* x, int64_t n_rows, int d, uint8_t*
   return check_launch(launch_quantize_kv_fp4(x, n_rows, out, stream));
 }
 
+csa2_status csa2_upload(const void* host_packed, size_t bytes, int n_segs, void* dev_stage,
+                        size_t stage_bytes, cudaStream_t stream) {
+  static_assert(sizeof(csa2_upload_seg) == 48, "upload table entry");
+  if (n_segs < 0 || !host_packed || !dev_stage || !aligned16(dev_stage)) return CSA2_ERR_INVALID_ARG;
+  const size_t table = (size_t)n_segs * sizeof(csa2_upload_seg);
+  if (bytes < table || stage_bytes < bytes) return CSA2_ERR_INVALID_ARG;
+  const csa2_upload_seg* segs = reinterpret_cast<const csa2_upload_seg*>(host_packed);
+  int64_t work = 0;
+  for (int i = 0; i < n_segs; ++i) {
+    const csa2_upload_seg& g = segs[i];
+    if (g.reserved != 0 || (g.src_off & 15u) != 0 || g.src_off < table) return CSA2_ERR_INVALID_ARG;
+    if (g.rows == 0) continue;
+    if (g.dst == 0 || g.row_bytes == 0 || g.row_bytes > bytes || g.rows > bytes / g.row_bytes)
+      return CSA2_ERR_INVALID_ARG;
+    const uint64_t payload = g.rows * g.row_bytes;
+    if (g.src_off > bytes || payload > bytes - g.src_off) return CSA2_ERR_INVALID_ARG;
+    if (g.kind == CSA2_UPLOAD_KV_FP4) {
+      if (g.row_bytes != (uint64_t)kD * 4 || ((g.dst | g.dst_stride) & 15u) != 0 ||
+          (g.rows > 1 && g.dst_stride < (uint64_t)kRowBytes))
+        return CSA2_ERR_INVALID_ARG;
+      work += (int64_t)g.rows * 32;
+    } else if (g.kind == CSA2_UPLOAD_RAW) {
+      if (g.rows > 1 && g.dst_stride < g.row_bytes) return CSA2_ERR_INVALID_ARG;
+      work += (int64_t)((payload + 15) / 16);
+    } else {
+      return CSA2_ERR_INVALID_ARG;
+    }
+  }
+  return check_launch(launch_upload(host_packed, bytes, n_segs, dev_stage, work, stream));
+}
+
 csa2_status csa2_index_scores(const uint8_t* q_fp8, const uint8_t* k_fp8, int B, int H_I, int D_I,
                               int64_t N, int64_t kv_seq_stride, int q_per_seq,
                               const int32_t* q_pos, int ratio, float* scores,

@@ -216,6 +216,11 @@ cudaError_t launch_sparse_attn_tc(const uint16_t* q_bf16, const uint8_t* kv_fp4,
                                   float* part_lse, int32_t* status, const SwaArgs* swa,
                                   int32_t* idx_copy, cudaStream_t stream, bool pdl);
 
+// csa2_upload: the copy of the packed buffer and the kernel that places its
+// segments (work_units: 16-byte units and rows of all segments, for sizing).
+cudaError_t launch_upload(const void* host_packed, size_t bytes, int n_segs, void* dev_stage,
+                          int64_t work_units, cudaStream_t stream);
+
 int device_sm_count();
 
 // CSA2_OK for cudaSuccess; otherwise keeps cudaGetErrorString(e) for
