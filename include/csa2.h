@@ -388,6 +388,10 @@ typedef struct csa2_group_args {
                               each layer with swa_kv also attends its window (q_pos
                               required, swa_ring >= n_win) */
   int indexer_fmt;         /* csa2_indexer_fmt of qi_fp8 and ki_fp8 */
+  cudaEvent_t q_ready;     /* NULL, or an event the group's attention launches wait for
+                              (cudaStreamWaitEvent before the first one): the layers'
+                              main queries may still be arriving on another stream while
+                              the indexer and top-k run */
 } csa2_group_args;
 
 /*

@@ -58,7 +58,7 @@ class Csa2GroupArgs(ctypes.Structure):
                 ("k", ctypes.c_int), ("pool_size", ctypes.c_int), ("pool_out", _vp),
                 ("softmax_scale", ctypes.c_float), ("pool_block", ctypes.c_int),
                 ("swa_ring", ctypes.c_int64), ("n_win", ctypes.c_int),
-                ("indexer_fmt", ctypes.c_int)]
+                ("indexer_fmt", ctypes.c_int), ("q_ready", _vp)]
 
 
 INDEXER_E4M3, INDEXER_MXFP4 = 0, 1
@@ -451,7 +451,7 @@ class LayerGroup:
                  softmax_scale: Optional[float] = None, want_lse: bool = True,
                  reuse_idx_copy: bool = True, pool_block: int = 0,
                  swa_kv: Optional[Sequence[Optional[torch.Tensor]]] = None, n_win: int = 0,
-                 indexer_fmt: int = INDEXER_E4M3):
+                 indexer_fmt: int = INDEXER_E4M3, q_ready: Optional[torch.cuda.Event] = None):
         L = len(modes)
         self.modes = list(modes)
         self.q = [_bits16(q, f"q_bf16[{l}]") for l, q in enumerate(q_bf16)]
@@ -491,7 +491,9 @@ class LayerGroup:
         self._args = Csa2GroupArgs(_ptr(self.kv), _ptr(self.ki), B, H, H_I, D, D_I, N,
                                    kv_seq_stride, q_per_seq, _ptr(self.q_pos), ratio, k,
                                    pool_size, _ptr(self.pool), softmax_scale, pool_block, ring,
-                                   n_win, indexer_fmt)
+                                   n_win, indexer_fmt,
+                                   q_ready.cuda_event if q_ready is not None else None)
+        self._q_ready = q_ready   # kept alive with the struct that names it
 
     def __call__(self):
         _check(lib.csa2_layer_group(self._layers, len(self.modes), ctypes.byref(self._args),

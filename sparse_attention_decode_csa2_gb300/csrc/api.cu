@@ -421,6 +421,7 @@ csa2_status csa2_layer_group(const csa2_layer* layers, int n_layers, const csa2_
     pf.n = g->N;
     pf.q_per_seq = g->q_per_seq;
   }
+  bool q_waited = false;
   for (int l = 0; l < n_layers && e == cudaSuccess; ++l) {
     const csa2_layer& L = layers[l];
     const int32_t* use = nullptr;
@@ -463,6 +464,11 @@ csa2_status csa2_layer_group(const csa2_layer* layers, int n_layers, const csa2_
     // The attention starts early (programmatic dependent launch): it loads Q
     // and sets up while the kernel before it (this layer's top-k, or the
     // previous layer's merge) finishes.
+    if (g->q_ready && !q_waited) {  // the main queries may arrive on another stream
+      e = cudaStreamWaitEvent(stream, g->q_ready, 0);
+      q_waited = true;
+      if (e != cudaSuccess) break;
+    }
     const SwaArgs swa{L.swa_kv, g->swa_ring, g->n_win, g->q_pos};
     const bool with_swa = g->n_win > 0 && L.swa_kv;
     e = launch_sparse_attn(L.q_bf16, g->kv_fp4, g->B, g->H, g->N, g->kv_seq_stride, g->q_per_seq,
