@@ -10,7 +10,7 @@
  *    1.(4) "CSA2" (indexer scores entries, per-query top-k, each query attends
  *    its selected entries), 1.(4).1 "Cross-Layer KV and Index Reuse",
  *    1.(4).2 "Hierarchical Sparse Indexer", 1.(5).4 "FP4 Main KV Cache",
- *    2.(2).1 "Model settings" (64 query heads x 512).
+ *    3.(2).1 "Model settings" (64 query heads x 512).
  *
  * Conventions for every call:
  *  - All tensor pointers are DEVICE pointers, allocated and owned by the
@@ -275,7 +275,7 @@ csa2_status csa2_hier_pool_index_mxfp4(const uint8_t* q_mx, const uint8_t* k_mx,
 /*
  * csa2_sparse_attn_fp4 -- gathers the selected FP4 entries, dequantises them
  * and runs MQA softmax attention over them (walkthrough 1.(4) "CSA2";
- * 1.(5).4: the cache is dequantised before attention; 2.(2).1: 64 heads x
+ * 1.(5).4: the cache is dequantised before attention; 3.(2).1: 64 heads x
  * 512).  K = V = the dequantised latent, shared by all heads.
  *   q_bf16   bf16 [B][H][D] main queries (16-byte aligned)
  *   kv_fp4   uint8 [S][N][D/2 + D/16] FP4 rows (16-byte aligned)
@@ -295,7 +295,7 @@ csa2_status csa2_sparse_attn_fp4(const uint16_t* q_bf16, const uint8_t* kv_fp4, 
  * csa2_sparse_attn_fp4_swa -- csa2_sparse_attn_fp4 with the query's sliding
  * window of the layer's SWA KV in the same softmax (walkthrough 1.(4): every
  * query attends the selected entries and its layer's own SWA KV; 1.(5).4:
- * SWA KV stays FP8; 2.(2).1: window n_win = 128).
+ * SWA KV stays FP8; 3.(2).1: window n_win = 128).
  *   swa_kv   E4M3 [S][swa_ring][D] one latent per token (plain E4M3, no
  *            scale), per sequence a ring: token t at row t mod swa_ring
  *            (16-byte aligned)

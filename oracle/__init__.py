@@ -239,7 +239,7 @@ def hier_pool_index(q_fp8, k_fp8, N: int, kv_seq_stride: int, q_per_seq: int, po
     return out
 
 
-# --- attention (walkthrough 1.(4), 1.(5).4, 2.(2).1) ---
+# --- attention (walkthrough 1.(4), 1.(5).4, 3.(2).1) ---
 
 def sparse_attn(q_bf16, kv_fp4, N: int, kv_seq_stride: int, q_per_seq: int, idx, scale: float):
     """q_bf16 [B][H][D] (uint16 bits), kv_fp4 [S*stride][9D/16], idx [B][k] -> (out, lse) fp64."""

@@ -25,7 +25,7 @@
  *  [P4d] same page, 1.(5).4 "FP4 Main KV Cache": E2M1 values, one E4M3 scale
  *        per 16 channels, no second-level global scale, largest magnitude
  *        448 x 6 = 2688, quantised after RoPE, dequantised before attention.
- *  [P4e] same page, 2.(2).1 "Model settings": 64 main query heads of 512 dims.
+ *  [P4e] same page, 3.(2).1 "Model settings": 64 main query heads of 512 dims.
  *  [P4f] same page, 1.(5).4: the indexer query and key are FP4 in the OCP
  *        MXFP4 format.
  *

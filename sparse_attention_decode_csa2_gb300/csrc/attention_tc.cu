@@ -1,7 +1,7 @@
 // Sparse MQA attention over the selected FP4 entries on the 5th-generation
 // tensor cores (DeepSeek-V4.1-Flash paper walkthrough, 1.(4) "CSA2": each
 // query attends its selected main-KV entries; 1.(5).4: the FP4 cache is
-// dequantised before attention; 2.(2).1: 64 query heads x 512).  K = V = the
+// dequantised before attention; 3.(2).1: 64 query heads x 512).  K = V = the
 // dequantised 512-channel latent shared by the heads.
 //
 // One CTA = one query x a chunk of its selected slots, in tiles of 128
