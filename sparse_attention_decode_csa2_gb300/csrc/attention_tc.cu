@@ -17,12 +17,12 @@
 // about the same whether it covers 64 or 128 entries, so the tile is as wide
 // as shared memory allows.
 //
-// Pipeline.  There is one V buffer, handed over per pair of 64-channel atoms:
-// O^T(t) M-block p reads atoms 2p, 2p + 1 of V(t); once it completes the
-// dequantisers write those atoms of V(t + 1); S(t + 1) consumes atoms in K
-// order as they arrive.  The tensor pipe thus runs O^T(t) and S(t + 1) back
-// to back and idles only while the softmax of t + 1 runs.  Warp roles (512
-// threads):
+// Pipeline.  There is one V buffer, handed over in two halves of four
+// 64-channel atoms: O^T(t) M-blocks 2h, 2h + 1 read atoms 4h .. 4h + 3 of
+// V(t); once they complete the dequantisers write those atoms of V(t + 1),
+// and S(t + 1) consumes each half as it arrives.  The tensor pipe thus runs
+// O^T(t) and S(t + 1) back to back and idles only while the softmax of t + 1
+// runs.  Warp roles (512 threads):
 //   warps 0-3   softmax: warp q holds heads 16q .. 16q + 15; a paired 16-lane
 //               load gives lane l head 16q + l % 16 and half of the tile's
 //               entries (lanes l and l ^ 16 share a head), so a head's max and
@@ -30,33 +30,33 @@
 //               lazy per-head reference max (it moves only when a logit passes
 //               it by more than 2^8 in the exp2 domain, so P <= 256 stays in
 //               fp16 range and O is rarely rescaled)
-//   warps 4-11  dequantisers: a thread loads one row's half (four atoms of
-//               32 code bytes + 4 scale bytes) into registers a tile ahead;
-//               all eight warps convert one atom pair at a time, E2M1 x E4M3
-//               -> fp16 (exact), into the swizzled V tile
+//   warps 4-11  dequantisers: for half h a lane converts atom 4 h + lane / 8
+//               of rows 16 w + 8 i + lane % 8 (E2M1 x E4M3 -> fp16, exact),
+//               from registers loaded a tile ahead; each load instruction of
+//               a warp reads 128 contiguous bytes of eight rows, each 16-byte
+//               store phase writes eight consecutive rows of one atom
+//               (conflict-free); the next tile's rows are requested after the
+//               tile's handovers
 //   warp 12     TMEM allocation; lane 0 issues every MMA
 //   warp 13     prefetcher: requests the selected rows of tiles 1, 2, ... (and
-//               the SWA window) into L2 up to 16 tiles ahead of the
-//               dequantisers, so that DRAM streams a chunk's rows while earlier
-//               tiles are computed
+//               the SWA window) into L2 with bulk prefetches, up to 16 tiles
+//               ahead of the dequantisers
 //   warps 14-15 join the epilogue
-// (Two measured alternatives were slower: staging rows in shared memory, since
+// (Measured alternatives that were slower: staging rows in shared memory, since
 // the tensor cores read their operands from shared memory and its bandwidth
-// bounds a tile; and one cp.async.bulk copy per 288-byte row, bounded by the
-// copy engine's per-request cost.)
+// bounds a tile; one cp.async.bulk copy per 288-byte row, bounded by the copy
+// engine's per-request cost; one row per lane in each load, bounded by the
+// SM's outstanding-request tracking; S^T at M = 128 with eight softmax warps,
+// whose softmax and MN-major P^T operand cost more than they saved.)
 // The chunk's slot ids are read once at the start: the first kIdxCache into
 // shared memory, the validity of every slot into a bit mask.
 // SWA branch: the CTA of a query's last chunk also attends the query's sliding
 // window (E4M3 rows of the layer's SWA ring) as extra tiles after its selected
 // entries, in the same online softmax.
 // Epilogue: every warp reads one M-block x 32 channels of O^T from tensor
-// memory and writes the output ([head][channel] fp32), or the split partial
-// ([channel][head] fp16, so that a thread's heads are contiguous; the merge
-// kernel transposes).  (Merging the
-// splits of a query inside the kernel, as one thread-block cluster reading
-// its peers' partials through distributed shared memory, was measured no
-// faster than the merge kernel: the remote reads ran at a few bytes per
-// cycle per SM.)
+// memory.  With one split it writes the output ([head][channel] fp32); with
+// several, the query's splits form one thread-block cluster that merges them
+// (staged fp16 blocks exchanged through L2 by bulk copies: see below).
 // Every mbarrier wait is bounded (about 2 s of %globaltimer): a wait that
 // gives up sets the timeout status bit and the CTA drains, frees its tensor
 // memory and exits.
