@@ -68,9 +68,35 @@ __device__ __forceinline__ uint32_t idx_tmem_cols(int NB) {
   return NB <= 16 ? 32u : (NB <= 32 ? 64u : (NB <= 64 ? 128u : (NB <= 128 ? 256u : 512u)));
 }
 
+// A tile's scores from its accumulator columns (thread = entry e of the tile,
+// taddr = its TMEM lane at the buffer's first column): query qq's score is the
+// sum, in column order, of its HI head columns qq * HI .. +HI; 32 columns per
+// tensor-memory round trip.  `srow` = the group's first score row.
+template <int HI>
+__device__ __forceinline__ void score_columns(uint32_t taddr, int nq, int64_t e, int64_t N,
+                                              const int32_t* nv, float* srow) {
+  const int ncols = nq * HI;
+  for (int c0 = 0; c0 < ncols; c0 += 32) {
+    float v[32];
+    tmem_ld16(taddr + c0, v);
+    if (c0 + 16 < ncols) tmem_ld16(taddr + c0 + 16, v + 16);
+    tmem_wait_ld();
+#pragma unroll
+    for (int qn = 0; qn < 32 / HI; ++qn) {
+      const int qq = c0 / HI + qn;
+      if (qq < nq) {
+        float acc = 0.0f;
+#pragma unroll
+        for (int j = 0; j < HI; ++j) acc += v[HI * qn + j];
+        if (e < N) srow[qq * N + e] = (e < nv[qq]) ? acc : -INFINITY;
+      }
+    }
+  }
+}
+
 // One CTA: items [w0, w1) of the call, item w = (group w / T, tile w % T).
 template <int D_I>
-__global__ void __launch_bounds__(kIdxThreads, 1)
+__global__ void __launch_bounds__(kIdxThreads, 3)
 index_tc_kernel(const __grid_constant__ CUtensorMap tmap, const uint8_t* __restrict__ q_fp8,
                 int B, int H_I, int64_t N, int64_t kv_seq_stride, int q_per_seq, int QG, int NB,
                 int64_t T, int64_t W, const int32_t* __restrict__ q_pos, int ratio,
@@ -237,6 +263,22 @@ index_tc_kernel(const __grid_constant__ CUtensorMap tmap, const uint8_t* __restr
         const uint32_t ph = ((uint32_t)n >> 1) & 1u;
         ++n;
         if (alive && !mbar_wait(su32(&ctl.acc_full[ab]), ph, status)) alive = false;
+        if (alive && (H_I == 8 || H_I == 16 || H_I == 32)) {
+          // 8, 16 or 32 heads per query: the group's head columns 32 per
+          // tensor-memory round trip, each query's H_I columns summed in
+          // column order
+          tc_fence_after();
+          if (H_I == 8)
+            score_columns<8>(tmem + lane_base + ab * NB, nq, e, N, nv, scores + q0 * N);
+          else if (H_I == 16)
+            score_columns<16>(tmem + lane_base + ab * NB, nq, e, N, nv, scores + q0 * N);
+          else
+            score_columns<32>(tmem + lane_base + ab * NB, nq, e, N, nv, scores + q0 * N);
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(su32(&ctl.acc_empty[ab]));
+          continue;
+        }
         if (alive) {
           tc_fence_after();
           for (int qq = 0; qq < nq; ++qq) {
