@@ -328,11 +328,12 @@ csa2_status csa2_sparse_attn_fp4_swa(const uint16_t* q_bf16, const uint8_t* kv_f
  *   the device).  Such callers still pass their inputs and outputs, but no
  *   workspace.
  *   Arguments, layouts and results are those of csa2_sparse_attn_fp4 (same
- *   kernels).  The split partials live in a fixed 24 MiB device array inside
- *   the library, held by every GPU that loads the library until the process
- *   exits.  A call whose partials would not fit (more than
- *   csa2_workspace_size(B, 0, k, H, 0) - 256 bytes > 24 MiB) returns
- *   CSA2_ERR_WORKSPACE and launches nothing.  No cudaMalloc, cudaFree or
+ *   kernels).  The split partials (per-split log-sum-exps) live in a fixed
+ *   256 KiB device array inside the library, held by every GPU that loads the
+ *   library until the process exits.  A call whose partials would not fit
+ *   (csa2_workspace_size(B, 0, k, H, 0) - 256 bytes > 256 KiB) returns
+ *   CSA2_ERR_WORKSPACE and launches nothing; with splits never outnumbering
+ *   the SMs, that needs a GPU of more than 1024 SMs.  No cudaMalloc, cudaFree or
  *   allocating library routine is called.
  *   The first call on a device looks up the array's device address
  *   (cudaGetSymbolAddress, once per device, under a lock); make that first

@@ -2,8 +2,9 @@
 // walkthrough, 1.(4) "CSA2": each query attends its selected entries).  The
 // tensor-core kernel (attention_tc.cu) processes one query x one chunk of its
 // selected slots per CTA; when a query's slots are split over several CTAs
-// (a thread-block cluster), each writes its normalised partial output (fp16)
-// and log-sum-exp (fp32), and the cluster merges them in fp32:
+// (a thread-block cluster), each writes its partial log-sum-exp (fp32) to the
+// workspace and hands its normalised partial output (fp16) to the cluster's
+// other CTAs through shared memory; they merge in fp32:
 // out = sum_s exp(lse_s - LSE) o_s with LSE = log sum_s exp(lse_s).
 #include "csa2_internal.cuh"
 
@@ -31,10 +32,10 @@ int choose_splits(int B, int k) {
   return 1;
 }
 
-// fp16 partial outputs, then fp32 partial lse
+// fp32 partial lse [B][nsplit][H] (the partial outputs stay in shared memory)
 size_t partial_bytes(int B, int H, int nsplit) {
   if (nsplit <= 1) return 0;
-  return align_up((size_t)B * nsplit * H * kD * 2, 256) + align_up((size_t)B * nsplit * H * 4, 256);
+  return align_up((size_t)B * nsplit * H * 4, 256);
 }
 
 cudaError_t launch_attn(const uint16_t* q_bf16, const uint8_t* kv_fp4, int B, int H, int64_t N,
@@ -44,16 +45,10 @@ cudaError_t launch_attn(const uint16_t* q_bf16, const uint8_t* kv_fp4, int B, in
                         int32_t* idx_copy) {
   const int nsplit = choose_splits(B, k);
   const int chunk = ((k + nsplit - 1) / nsplit + kSplitTile - 1) / kSplitTile * kSplitTile;
-  __half* part_o = nullptr;
-  float* part_lse = nullptr;
-  if (nsplit > 1) {
-    part_o = reinterpret_cast<__half*>(scratch);
-    part_lse = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(scratch) +
-                                        align_up((size_t)B * nsplit * H * kD * 2, 256));
-  }
+  float* part_lse = nsplit > 1 ? reinterpret_cast<float*>(scratch) : nullptr;
   const float scale_log2 = softmax_scale * 1.4426950408889634f;
   return launch_sparse_attn_tc(q_bf16, kv_fp4, B, H, N, kv_seq_stride, q_per_seq, idx, k, nsplit,
-                               chunk, scale_log2, out, lse, part_o, part_lse, status, swa,
+                               chunk, scale_log2, out, lse, part_lse, status, swa,
                                idx_copy, stream, pdl);
 }
 

@@ -7,16 +7,19 @@
 // owns every device allocation, and latency-critical serving loops that must
 // never hit the allocator (cudaMalloc may synchronise the device).  This entry
 // point runs exactly the same kernels as csa2_sparse_attn_fp4, but its split
-// partials live in a fixed, file-scope device array instead of a caller
-// workspace.  That array is kNoallocScratchBytes (24 MiB) and is held by every
-// GPU that loads the library until the process exits.
+// partials (the per-split log-sum-exp; the partial outputs themselves never
+// leave shared memory) live in a fixed, file-scope device array instead of a
+// caller workspace.  That array is kNoallocScratchBytes (256 KiB: a query's
+// splits never outnumber the SMs, so 64 heads x 4 bytes per SM suffice for
+// any GPU of up to 1024 SMs) and is held by every GPU that loads the library
+// until the process exits.
 #include <mutex>
 
 #include "csa2_internal.cuh"
 
-// Scratch for the split-k partial outputs.  In host code this name is only a
+// Scratch for the split-k partial log-sum-exps.  In host code this name is only a
 // host-side stand-in; kernels receive the device address obtained below.
-static __device__ __align__(256) uint8_t g_csa2_attn_scratch[24u << 20];
+static __device__ __align__(256) uint8_t g_csa2_attn_scratch[256u << 10];
 
 namespace csa2 {
 namespace {

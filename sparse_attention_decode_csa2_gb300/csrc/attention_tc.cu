@@ -56,7 +56,8 @@
 // Epilogue: every warp reads one M-block x 32 channels of O^T from tensor
 // memory.  With one split it writes the output ([head][channel] fp32); with
 // several, the query's splits form one thread-block cluster that merges them
-// (staged fp16 blocks exchanged through L2 by bulk copies: see below).
+// (staged fp16 blocks pushed into their owners' shared memory by bulk copies:
+// see below).
 // Every mbarrier wait is bounded (about 2 s of %globaltimer): a wait that
 // gives up sets the timeout status bit and the CTA drains, frees its tensor
 // memory and exits.
@@ -157,20 +158,21 @@ __device__ __forceinline__ void prefetch_l2(const uint8_t* row, int bytes) {
                : "memory");
 }
 
-// Bulk copies (the SM's copy engine): shared -> global in a bulk group, and
-// global -> shared completing on an mbarrier.  Addresses 16-byte aligned,
-// sizes multiples of 16.
-__device__ __forceinline__ void bulk_store(void* dst, uint32_t src, uint32_t bytes) {
-  asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(dst), "r"(src),
-               "r"(bytes)
-               : "memory");
+// This CTA's shared-memory address `a` as seen in cluster CTA `rank`.
+__device__ __forceinline__ uint32_t peer_smem(uint32_t a, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(rank));
+  return r;
 }
-__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes,
+// Bulk copy of `bytes` from this CTA's shared memory into another CTA's of
+// the cluster, completing on that CTA's mbarrier `bar` (both addresses from
+// peer_smem, 16-byte aligned, bytes a multiple of 16).
+__device__ __forceinline__ void bulk_push(uint32_t dst, uint32_t src, uint32_t bytes,
                                           uint32_t bar) {
   asm volatile(
-      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-          dst),
-      "l"(src), "r"(bytes), "r"(bar)
+      "cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, "
+      "[%3];" ::"r"(dst),
+      "r"(src), "r"(bytes), "r"(bar)
       : "memory");
 }
 
@@ -233,7 +235,7 @@ sparse_attn_tc_kernel(const uint16_t* __restrict__ q_bf16, const uint8_t* __rest
                       int64_t N, int64_t kv_seq_stride, int q_per_seq,
                       const int32_t* __restrict__ idx, int k, int chunk, float scale_log2,
                       float* __restrict__ out, float* __restrict__ lse,
-                      __half* __restrict__ part_o, float* __restrict__ part_lse, int32_t* status,
+                      float* __restrict__ part_lse, int32_t* status,
                       const uint8_t* __restrict__ swa_kv, int64_t swa_ring, int n_win,
                       const int32_t* __restrict__ q_pos, int32_t* __restrict__ idx_copy) {
   using L = TcLayout;
@@ -751,33 +753,27 @@ sparse_attn_tc_kernel(const uint16_t* __restrict__ q_bf16, const uint8_t* __rest
   if (nsplit > 1) {
     // ---- merge of the query's splits (the cluster is the query's nsplit
     //      CTAs, nsplit a power of two): CTA `split` owns the 64-channel
-    //      blocks j = split, split + nsplit, ...  Each CTA stores the blocks
-    //      it does not own (bulk copies through L2, which the measured
-    //      distributed-shared-memory reads were slower than), and after the
-    //      cluster barrier fetches the other splits' copies of its own blocks
-    //      and forms o = sum_s exp(lse_s - lse) o_s, lse the log-sum-exp of
-    //      the lse_s ----
+    //      blocks j = split, split + nsplit, ...  Past a cluster barrier
+    //      (every CTA's MMAs are done with V, whose upper part receives the
+    //      blocks), each CTA pushes the blocks it does not own into their
+    //      owners' shared memory with bulk copies that complete on the
+    //      owner's mbarrier, then forms o = sum_s exp(lse_s - lse) o_s over
+    //      its own blocks, lse the log-sum-exp of the lse_s ----
     const int n_own = 8 / nsplit;
-    if (tid == 0) {
-      uint8_t* dst = reinterpret_cast<uint8_t*>(part_o) + ((int64_t)b * nsplit + split) * 8 * blk_bytes;
-      for (int j = 0; j < 8; ++j)
-        if (j % nsplit != split) bulk_store(dst + j * blk_bytes, sbase + L::v_off + j * blk_bytes, blk_bytes);
-      asm volatile("cp.async.bulk.commit_group;\n\tcp.async.bulk.wait_group 0;" ::: "memory");
-      asm volatile("fence.proxy.async.global;" ::: "memory");
-    }
+    const uint32_t recv_s = sbase + L::v_off + 8 * blk_bytes;  // [source][own block]
     asm volatile(
         "barrier.cluster.arrive.release.aligned;\n\t"
         "barrier.cluster.wait.acquire.aligned;" ::: "memory");
-    const uint32_t recv_s = sbase + L::v_off + 8 * blk_bytes;  // [peer][own block]
     if (tid == 0) {
-      asm volatile("fence.proxy.async.global;" ::: "memory");
       mbar_expect_tx(su32(&ctl.recv), (uint32_t)(nsplit - 1) * n_own * blk_bytes);
-      const uint8_t* src = reinterpret_cast<const uint8_t*>(part_o) + (int64_t)b * nsplit * 8 * blk_bytes;
-      for (int s2 = 0, slot = 0; s2 < nsplit; ++s2) {
-        if (s2 == split) continue;
-        for (int kk = 0; kk < n_own; ++kk, ++slot)
-          bulk_load(recv_s + slot * blk_bytes, src + ((int64_t)s2 * 8 + split + kk * nsplit) * blk_bytes,
-                    blk_bytes, su32(&ctl.recv));
+      for (int j = 0; j < 8; ++j) {
+        const int owner = j % nsplit;
+        if (owner == split) continue;
+        // this split's slot among the owner's sources, block j / nsplit of the owner's
+        const int slot = (split < owner ? split : split - 1) * n_own + j / nsplit;
+        bulk_push(peer_smem(recv_s + (uint32_t)slot * blk_bytes, (uint32_t)owner),
+                  sbase + L::v_off + j * blk_bytes, blk_bytes,
+                  peer_smem(su32(&ctl.recv), (uint32_t)owner));
       }
     }
     // weights exp(lse_s - M) / sum (per split and head), in the free Q region
@@ -806,6 +802,9 @@ sparse_attn_tc_kernel(const uint16_t* __restrict__ q_bf16, const uint8_t* __rest
     }
     __syncthreads();
     const bool got = __all_sync(0xffffffffu, mbar_wait(su32(&ctl.recv), 0u, status));
+    // every block pushed to this CTA has landed; the matching wait below keeps
+    // this CTA's staged blocks alive until every peer's have too
+    asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
     // warp w: channels 32 (w & 1) .. +32 of a block (lane = channel), heads
     // 8 (w >> 1) .. +8; for each head the warp stores one 128-byte line
     const int cc = 32 * (warp & 1) + lane, c8 = warp >> 1;
@@ -839,6 +838,7 @@ sparse_attn_tc_kernel(const uint16_t* __restrict__ q_bf16, const uint8_t* __rest
         for (int i = 0; i < 8; ++i) orow[(int64_t)i * kD] = acc[i];
       }
     }
+    asm volatile("barrier.cluster.wait.aligned;" ::: "memory");
   }
 }
 
@@ -848,7 +848,7 @@ template <int H>
 static cudaError_t launch_tc_t(const uint16_t* q_bf16, const uint8_t* kv_fp4, int B, int64_t N,
                                int64_t kv_seq_stride, int q_per_seq, const int32_t* idx, int k,
                                int nsplit, int chunk, float scale_log2, float* out, float* lse,
-                               __half* part_o, float* part_lse, int32_t* status,
+                               float* part_lse, int32_t* status,
                                const SwaArgs* swa, int32_t* idx_copy, cudaStream_t stream,
                                bool pdl) {
   using L = TcLayout;
@@ -878,7 +878,7 @@ static cudaError_t launch_tc_t(const uint16_t* q_bf16, const uint8_t* kv_fp4, in
   cfg.attrs = attr;
   cfg.numAttrs = na;
   return cudaLaunchKernelEx(&cfg, sparse_attn_tc_kernel<H>, q_bf16, kv_fp4, N, kv_seq_stride,
-                            q_per_seq, idx, k, chunk, scale_log2, out, lse, part_o, part_lse,
+                            q_per_seq, idx, k, chunk, scale_log2, out, lse, part_lse,
                             status, swa ? swa->kv : nullptr, swa ? swa->ring : (int64_t)0,
                             swa ? swa->n_win : 0, swa ? swa->q_pos : nullptr, idx_copy);
 }
@@ -886,21 +886,21 @@ static cudaError_t launch_tc_t(const uint16_t* q_bf16, const uint8_t* kv_fp4, in
 cudaError_t launch_sparse_attn_tc(const uint16_t* q_bf16, const uint8_t* kv_fp4, int B, int H,
                                   int64_t N, int64_t kv_seq_stride, int q_per_seq,
                                   const int32_t* idx, int k, int nsplit, int chunk,
-                                  float scale_log2, float* out, float* lse, __half* part_o,
-                                  float* part_lse, int32_t* status, const SwaArgs* swa,
-                                  int32_t* idx_copy, cudaStream_t stream, bool pdl) {
+                                  float scale_log2, float* out, float* lse, float* part_lse,
+                                  int32_t* status, const SwaArgs* swa, int32_t* idx_copy,
+                                  cudaStream_t stream, bool pdl) {
   switch (H) {
     case 16:
       return launch_tc_t<16>(q_bf16, kv_fp4, B, N, kv_seq_stride, q_per_seq, idx, k, nsplit,
-                             chunk, scale_log2, out, lse, part_o, part_lse, status, swa, idx_copy,
+                             chunk, scale_log2, out, lse, part_lse, status, swa, idx_copy,
                              stream, pdl);
     case 32:
       return launch_tc_t<32>(q_bf16, kv_fp4, B, N, kv_seq_stride, q_per_seq, idx, k, nsplit,
-                             chunk, scale_log2, out, lse, part_o, part_lse, status, swa, idx_copy,
+                             chunk, scale_log2, out, lse, part_lse, status, swa, idx_copy,
                              stream, pdl);
     default:
       return launch_tc_t<64>(q_bf16, kv_fp4, B, N, kv_seq_stride, q_per_seq, idx, k, nsplit,
-                             chunk, scale_log2, out, lse, part_o, part_lse, status, swa, idx_copy,
+                             chunk, scale_log2, out, lse, part_lse, status, swa, idx_copy,
                              stream, pdl);
   }
 }

@@ -206,15 +206,14 @@ cudaError_t launch_sparse_attn(const uint16_t* q_bf16, const uint8_t* kv_fp4, in
 
 // tcgen05 kernel of one sparse-attention call.  With nsplit > 1 (a power of
 // two, at most 8) a query's nsplit CTAs form one thread-block cluster that
-// writes fp16 partials part_o [B][nsplit][8 blocks][64 channels][H] (16-byte
-// chunks of a row swizzled) and partial lse part_lse [B][nsplit][H], then
-// merges them into `out` / `lse`.
+// writes partial lse part_lse [B][nsplit][H], exchanges its fp16 partial
+// outputs through shared memory and merges them into `out` / `lse`.
 cudaError_t launch_sparse_attn_tc(const uint16_t* q_bf16, const uint8_t* kv_fp4, int B, int H,
                                   int64_t N, int64_t kv_seq_stride, int q_per_seq,
                                   const int32_t* idx, int k, int nsplit, int chunk,
-                                  float scale_log2, float* out, float* lse, __half* part_o,
-                                  float* part_lse, int32_t* status, const SwaArgs* swa,
-                                  int32_t* idx_copy, cudaStream_t stream, bool pdl);
+                                  float scale_log2, float* out, float* lse, float* part_lse,
+                                  int32_t* status, const SwaArgs* swa, int32_t* idx_copy,
+                                  cudaStream_t stream, bool pdl);
 
 // csa2_upload: the copy of the packed buffer and the kernel that places its
 // segments (work_units: 16-byte units and rows of all segments, for sizing).

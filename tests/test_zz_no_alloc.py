@@ -41,7 +41,7 @@ def test_noalloc_matches_workspace_entry_point_on_two_calls():
     build.build()
     from sparse_attention_decode_csa2_gb300 import csa2
     lib = csa2.lib
-    B, H, N, k = 4, 64, 5000, 4096       # 8 split chunks per query, merged through scratch
+    B, H, N, k = 4, 64, 5000, 4096       # 8 split chunks per query, their lse through scratch
     assert csa2.workspace_size(B, 0, k, H, 0) > 256
     for seed in (1, 2):                  # two calls in a row, different inputs
         q, kv, idx = _case(seed, B, H, N, k)
@@ -66,12 +66,12 @@ def test_noalloc_rejects_requests_beyond_its_scratch():
     from sparse_attention_decode_csa2_gb300 import build
     build.build()
     from sparse_attention_decode_csa2_gb300 import csa2
-    B, H, k = 40, 64, 16384              # partials would need far more than the fixed array
+    B, H, k = 40, 64, 16384              # split partials of this request vs the fixed array
     q = torch.zeros((B, H, 512), dtype=torch.int16, device="cuda")
     kv = torch.zeros((100, 288), dtype=torch.uint8, device="cuda")
     idx = torch.full((B, k), -1, dtype=torch.int32, device="cuda")
     out = torch.zeros((B, H, 512), device="cuda")
     lse = torch.zeros((B, H), device="cuda")
-    if csa2.workspace_size(B, 0, k, H, 0) - 256 <= (24 << 20):
+    if csa2.workspace_size(B, 0, k, H, 0) - 256 <= (256 << 10):
         pytest.skip("this device's split policy keeps the request small")
     assert _noalloc(csa2.lib, q, kv, idx, 100, out, lse) == 3      # CSA2_ERR_WORKSPACE
