@@ -185,6 +185,8 @@ topk_reg_kernel(const float* __restrict__ scores, int64_t N, int k,
   __shared__ __align__(16) int32_t csum[256];
   __shared__ int32_t tot[kRegWarps + 1];
   __shared__ uint32_t red[4][kRegWarps];
+  __shared__ __align__(8) uint64_t row_bar;  // the row's bulk copy into shared memory
+  extern __shared__ __align__(16) uint32_t row_s[];  // KPT * kRegThreads keys (bulk path)
 
   pdl_trigger();
   pdl_wait();  // scores, n_valid and map come from the kernel before
@@ -217,23 +219,81 @@ topk_reg_kernel(const float* __restrict__ scores, int64_t N, int k,
     return;
   }
 
-  // keys of positions [tid*KPT, tid*KPT + KPT) in registers
+  // keys of positions [tid*KPT, tid*KPT + KPT) in registers.  A 16-byte
+  // aligned row comes into shared memory with bulk copies (the copy engine
+  // fetches it far faster than the threads' own 16-byte loads, each of which
+  // touches 32 rows' worth of lines); thread t then reads its 16-byte chunks
+  // starting at chunk t mod (KPT / 4), so that eight consecutive threads hit
+  // eight different bank groups: key[4 g + e] is position base + 4 ((g + rot)
+  // mod (KPT / 4)) + e
   const int base = tid * KPT;
+  constexpr int kCh = KPT / 4;  // 16-byte chunks per thread
   uint32_t key[KPT];
   const bool vec = ((N & 3) == 0) && ((reinterpret_cast<uintptr_t>(scores) & 15u) == 0);
-#pragma unroll
-  for (int i = 0; i < KPT; i += 4) {
-    const int j = base + i;
-    float v[4];
-    if (vec && j + 3 < n) {
-      const float4 f = *reinterpret_cast<const float4*>(row + j);
-      v[0] = f.x; v[1] = f.y; v[2] = f.z; v[3] = f.w;
-    } else {
-#pragma unroll
-      for (int e = 0; e < 4; ++e) v[e] = (j + e < n) ? row[j + e] : 0.0f;
+  const bool bulk = vec && ((reinterpret_cast<uintptr_t>(row) & 15u) == 0);
+  bool staged_row = false;
+  if (bulk) {
+    const uint32_t bar = static_cast<uint32_t>(__cvta_generic_to_shared(&row_bar));
+    if (tid == 0) {
+      asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(bar));
+      asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
+    __syncthreads();
+    const uint32_t bytes = (uint32_t)((n * 4 + 15) & ~15);  // within the row (N % 4 == 0)
+    if (tid == 0) {
+      asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+                   : "memory");
+      const uint32_t dst = static_cast<uint32_t>(__cvta_generic_to_shared(row_s));
+      for (uint32_t off = 0; off < bytes; off += 16384u) {
+        const uint32_t len = min(16384u, bytes - off);
+        asm volatile(
+            "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+            ::"r"(dst + off), "l"(reinterpret_cast<const uint8_t*>(row) + off), "r"(len), "r"(bar)
+            : "memory");
+      }
+    }
+    // bounded wait (about 2 s); on a timeout the keys are read from global memory
+    const uint64_t t0 = clock64();
+    bool done = false;
+    while (!done) {
+      uint32_t ok;
+      asm volatile(
+          "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+          "selp.u32 %0, 1, 0, p;\n\t}"
+          : "=r"(ok)
+          : "r"(bar), "r"(0u)
+          : "memory");
+      done = ok != 0;
+      if (!done && clock64() - t0 > 4000000000ll) break;
+    }
+    staged_row = __syncthreads_and(done);
+  }
+  const int rot = staged_row ? tid : 0;
+  auto kpos = [&](int i) { return base + 4 * (((i >> 2) + rot) & (kCh - 1)) + (i & 3); };
+  if (staged_row) {
 #pragma unroll
-    for (int e = 0; e < 4; ++e) key[i + e] = float_to_ordered(v[e]);
+    for (int g = 0; g < kCh; ++g) {
+      const uint4 u = *reinterpret_cast<const uint4*>(row_s + base + 4 * ((g + rot) & (kCh - 1)));
+      key[4 * g + 0] = float_to_ordered(__uint_as_float(u.x));
+      key[4 * g + 1] = float_to_ordered(__uint_as_float(u.y));
+      key[4 * g + 2] = float_to_ordered(__uint_as_float(u.z));
+      key[4 * g + 3] = float_to_ordered(__uint_as_float(u.w));
+    }
+  } else {
+#pragma unroll
+    for (int i = 0; i < KPT; i += 4) {
+      const int j = base + i;
+      float v[4];
+      if (vec && j + 3 < n) {
+        const float4 f = *reinterpret_cast<const float4*>(row + j);
+        v[0] = f.x; v[1] = f.y; v[2] = f.z; v[3] = f.w;
+      } else {
+#pragma unroll
+        for (int e = 0; e < 4; ++e) v[e] = (j + e < n) ? row[j + e] : 0.0f;
+      }
+#pragma unroll
+      for (int e = 0; e < 4; ++e) key[i + e] = float_to_ordered(v[e]);
+    }
   }
 
   // OR / AND of the keys, per sign of the score.  Over the whole row they
@@ -245,7 +305,7 @@ topk_reg_kernel(const float* __restrict__ scores, int64_t N, int k,
   uint32_t por = 0u, pand = 0xFFFFFFFFu, nor = 0u, nand = 0xFFFFFFFFu;  // >= 0 / < 0
 #pragma unroll
   for (int i = 0; i < KPT; ++i) {
-    const uint32_t valid = base + i < n ? 0xFFFFFFFFu : 0u;
+    const uint32_t valid = kpos(i) < n ? 0xFFFFFFFFu : 0u;
     const uint32_t pos = valid & (0u - (key[i] >> 31));  // all ones for a valid key >= 0
     const uint32_t neg = valid & ~pos;
     por |= key[i] & pos;
@@ -295,7 +355,7 @@ topk_reg_kernel(const float* __restrict__ scores, int64_t N, int k,
     int32_t* my_hist = hist + warp * 256;  // this warp's private histogram
 #pragma unroll
     for (int i = 0; i < KPT; ++i) {
-      if (base + i < n && (key[i] & mask) == prefix)
+      if (kpos(i) < n && (key[i] & mask) == prefix)
         atomicAdd(&my_hist[(key[i] >> shift) & dmask], 1);
     }
     __syncthreads();
@@ -327,23 +387,24 @@ topk_reg_kernel(const float* __restrict__ scores, int64_t N, int k,
   // first `need` class members in position order.  One scan of the two
   // counts packed in 16-bit halves (n <= 32768) gives both prefixes; the
   // class members taken before this thread are min(eq_before, need).
+  // bit b of the masks: position base + b (the keys' chunk rotation undone)
+  uint64_t g64 = 0u, e64 = 0u;
+#pragma unroll
+  for (int ii = 0; ii < KPT; ++ii) {
+    const uint32_t km = key[ii] & mask;
+    const int b = kpos(ii) - base;
+    const bool valid = base + b < n;
+    g64 |= (uint64_t)(valid && km > prefix) << b;
+    e64 |= (uint64_t)(valid && km == prefix) << b;
+  }
   uint32_t gtm[(KPT + 31) / 32], eqm[(KPT + 31) / 32];
   int gt = 0, eq = 0;
 #pragma unroll
   for (int w = 0; w < (KPT + 31) / 32; ++w) {
-    uint32_t g = 0u, e = 0u;
-#pragma unroll
-    for (int i = 0; i < 32 && 32 * w + i < KPT; ++i) {
-      const int ii = 32 * w + i;
-      const uint32_t km = key[ii] & mask;
-      const bool valid = base + ii < n;
-      g |= (uint32_t)(valid && km > prefix) << i;
-      e |= (uint32_t)(valid && km == prefix) << i;
-    }
-    gtm[w] = g;
-    eqm[w] = e;
-    gt += __popc(g);
-    eq += __popc(e);
+    gtm[w] = (uint32_t)(g64 >> (32 * w));
+    eqm[w] = (uint32_t)(e64 >> (32 * w));
+    gt += __popc(gtm[w]);
+    eq += __popc(eqm[w]);
   }
   int tot_packed;
   const int before = reg_block_scan((gt << 16) | eq, tot, &tot_packed);
@@ -884,8 +945,13 @@ template <int KPT>
 cudaError_t launch_reg(dim3 grid, const float* scores, int64_t N, int k, const int32_t* q_pos,
                        int ratio, const int32_t* n_valid, const int32_t* map, int32_t* idx,
                        int chunk, cudaStream_t stream, bool pdl, const RowPrefetch& pf) {
-  return launch_kernel(topk_reg_kernel<KPT>, grid, dim3(kRegThreads), 0, stream, pdl, scores, N, k,
-                       q_pos, ratio, n_valid, map, idx, chunk, pf);
+  // the row's keys staged in shared memory (bulk copies)
+  const size_t row_bytes = (size_t)KPT * kRegThreads * 4;
+  cudaError_t e = cudaFuncSetAttribute(topk_reg_kernel<KPT>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)row_bytes);
+  if (e != cudaSuccess) return e;
+  return launch_kernel(topk_reg_kernel<KPT>, grid, dim3(kRegThreads), row_bytes, stream, pdl,
+                       scores, N, k, q_pos, ratio, n_valid, map, idx, chunk, pf);
 }
 
 template <int KPT, int CL>
