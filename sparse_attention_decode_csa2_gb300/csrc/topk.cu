@@ -169,6 +169,19 @@ __device__ __forceinline__ int select_digit(const int32_t* csum, int need, int* 
   return 255 - t;
 }
 
+// The low n bits of a W-bit mask (1 <= n <= W <= 64).
+template <int W>
+__device__ __forceinline__ uint64_t lo_bits(int n) {
+  return n >= 64 ? ~0ull : ((1ull << n) - 1ull);
+}
+// A W-bit mask (W a power of two, 8..64) rotated left by r (0 <= r < W).
+template <int W>
+__device__ __forceinline__ uint64_t rot_bits(uint64_t m, int r) {
+  if (r == 0) return m;
+  const uint64_t all = lo_bits<W>(W);
+  return ((m << r) | (m >> (W - r))) & all;
+}
+
 // chunk == 0: CTA b selects row b.  chunk > 0 (map must be null): CTA (c, b)
 // selects among the candidates [c*chunk, (c+1)*chunk) of row b and writes
 // their positions in the row to idx[b][c][0..k) (one level of the long-row
@@ -269,7 +282,18 @@ topk_reg_kernel(const float* __restrict__ scores, int64_t N, int k,
     staged_row = __syncthreads_and(done);
   }
   const int rot = staged_row ? tid : 0;
-  auto kpos = [&](int i) { return base + 4 * (((i >> 2) + rot) & (kCh - 1)) + (i & 3); };
+  // key-order bits <-> position-order bits: a rotation by whole chunks of the
+  // KPT-bit masks (bit 4 g + e of key order is bit 4 ((g + rot) mod kCh) + e
+  // of position order)
+  auto to_pos = [&](uint64_t m) { return rot_bits<KPT>(m, 4 * (rot & (kCh - 1))); };
+  auto to_key = [&](uint64_t m) {
+    return rot_bits<KPT>(m, (KPT - 4 * (rot & (kCh - 1))) & (KPT - 1));
+  };
+  // the valid keys (positions below n), in key order
+  const int nv_here = n - base;
+  const uint64_t vpos = nv_here >= KPT ? lo_bits<KPT>(KPT)
+                                       : (nv_here <= 0 ? 0ull : lo_bits<KPT>(nv_here));
+  const uint64_t vkey = to_key(vpos);
   if (staged_row) {
 #pragma unroll
     for (int g = 0; g < kCh; ++g) {
@@ -305,7 +329,7 @@ topk_reg_kernel(const float* __restrict__ scores, int64_t N, int k,
   uint32_t por = 0u, pand = 0xFFFFFFFFu, nor = 0u, nand = 0xFFFFFFFFu;  // >= 0 / < 0
 #pragma unroll
   for (int i = 0; i < KPT; ++i) {
-    const uint32_t valid = kpos(i) < n ? 0xFFFFFFFFu : 0u;
+    const uint32_t valid = ((vkey >> i) & 1u) ? 0xFFFFFFFFu : 0u;
     const uint32_t pos = valid & (0u - (key[i] >> 31));  // all ones for a valid key >= 0
     const uint32_t neg = valid & ~pos;
     por |= key[i] & pos;
@@ -355,7 +379,7 @@ topk_reg_kernel(const float* __restrict__ scores, int64_t N, int k,
     int32_t* my_hist = hist + warp * 256;  // this warp's private histogram
 #pragma unroll
     for (int i = 0; i < KPT; ++i) {
-      if (kpos(i) < n && (key[i] & mask) == prefix)
+      if (((vkey >> i) & 1u) && (key[i] & mask) == prefix)
         atomicAdd(&my_hist[(key[i] >> shift) & dmask], 1);
     }
     __syncthreads();
@@ -387,16 +411,16 @@ topk_reg_kernel(const float* __restrict__ scores, int64_t N, int k,
   // first `need` class members in position order.  One scan of the two
   // counts packed in 16-bit halves (n <= 32768) gives both prefixes; the
   // class members taken before this thread are min(eq_before, need).
-  // bit b of the masks: position base + b (the keys' chunk rotation undone)
+  // key-order masks, then bit b: position base + b (the chunk rotation undone)
   uint64_t g64 = 0u, e64 = 0u;
 #pragma unroll
   for (int ii = 0; ii < KPT; ++ii) {
     const uint32_t km = key[ii] & mask;
-    const int b = kpos(ii) - base;
-    const bool valid = base + b < n;
-    g64 |= (uint64_t)(valid && km > prefix) << b;
-    e64 |= (uint64_t)(valid && km == prefix) << b;
+    g64 |= (uint64_t)(km > prefix) << ii;
+    e64 |= (uint64_t)(km == prefix) << ii;
   }
+  g64 = to_pos(g64 & vkey);
+  e64 = to_pos(e64 & vkey);
   uint32_t gtm[(KPT + 31) / 32], eqm[(KPT + 31) / 32];
   int gt = 0, eq = 0;
 #pragma unroll
