@@ -35,7 +35,12 @@ namespace {
 
 using namespace tc;
 
-constexpr int kIdxThreads = 192;
+// warps 0, 1 (TMA producer, MMA issuer) + EW epilogue warps; EW = 8 when a
+// tile's accumulator holds 256 head columns per entry (the epilogue, summing
+// them, bounds those shapes), each quadrant of tensor-memory lanes read by
+// two warps that split the group's queries; EW = 4 otherwise
+template <int EW>
+constexpr int idx_threads() { return (2 + EW) * 32; }
 constexpr int kStages = 8;
 constexpr int kTile = 128;
 
@@ -95,8 +100,8 @@ __device__ __forceinline__ void score_columns(uint32_t taddr, int nq, int64_t e,
 }
 
 // One CTA: items [w0, w1) of the call, item w = (group w / T, tile w % T).
-template <int D_I>
-__global__ void __launch_bounds__(kIdxThreads, 3)
+template <int D_I, int EW>
+__global__ void __launch_bounds__(idx_threads<EW>(), EW == 4 ? 3 : 2)
 index_tc_kernel(const __grid_constant__ CUtensorMap tmap, const uint8_t* __restrict__ q_fp8,
                 int B, int H_I, int64_t N, int64_t kv_seq_stride, int q_per_seq, int QG, int NB,
                 int64_t T, int64_t W, const int32_t* __restrict__ q_pos, int ratio,
@@ -127,7 +132,7 @@ index_tc_kernel(const __grid_constant__ CUtensorMap tmap, const uint8_t* __restr
       const int64_t q0 = (g0 + gi) * QG;
       const int nq = (int)min((int64_t)QG, (int64_t)B - q0);
       const uint8_t* qb = q_fp8 + q0 * H_I * D_I;
-      for (int off = et * 128; off < nq * H_I * D_I; off += 128 * 128)
+      for (int off = et * 128; off < nq * H_I * D_I; off += EW * 32 * 128)
         asm volatile("prefetch.global.L2 [%0];" ::"l"(qb + off));
       if (q_pos && et < nq) asm volatile("prefetch.global.L2 [%0];" ::"l"(q_pos + q0 + et));
     }
@@ -146,7 +151,7 @@ index_tc_kernel(const __grid_constant__ CUtensorMap tmap, const uint8_t* __restr
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(su32(&ctl.acc_full[i]), 1);
-      mbar_init(su32(&ctl.acc_empty[i]), 4);
+      mbar_init(su32(&ctl.acc_empty[i]), EW);
     }
     mbar_init(su32(&ctl.meta), 1);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -220,11 +225,11 @@ index_tc_kernel(const __grid_constant__ CUtensorMap tmap, const uint8_t* __restr
     }
   } else {
     // ---- stage the B operands (heads of each group's queries) and the visible lengths ----
-    const int et = tid - 64;  // 0..127
+    const int et = tid - 64;  // 0 .. 32 EW - 1
     for (int gi = 0; gi < ng; ++gi) {
       const int64_t q0 = (g0 + gi) * QG;
       const int nq = (int)min((int64_t)QG, (int64_t)B - q0);
-      for (int i = et; i < NB * D_I / 16; i += 128) {
+      for (int i = et; i < NB * D_I / 16; i += EW * 32) {
         const int nrow = i / (D_I / 16), c = i % (D_I / 16);
         uint4 v = make_uint4(0, 0, 0, 0);
         const int qq = nrow / H_I, h = nrow % H_I;
@@ -235,7 +240,7 @@ index_tc_kernel(const __grid_constant__ CUtensorMap tmap, const uint8_t* __restr
       if (et < 16) ctl.nvis[gi][et] = (et < nq) ? (int)n_visible(q_pos, (int)(q0 + et), ratio, N) : 0;
     }
     proxy_fence();
-    asm volatile("bar.sync 1, 128;" ::: "memory");
+    asm volatile("bar.sync 1, %0;" ::"n"(EW * 32) : "memory");
     if (et == 0) {
       for (int gi = 0; gi < 2; ++gi) {
         int m = 0;
@@ -245,19 +250,28 @@ index_tc_kernel(const __grid_constant__ CUtensorMap tmap, const uint8_t* __restr
       }
       mbar_arrive(su32(&ctl.meta));
     }
-    asm volatile("bar.sync 1, 128;" ::: "memory");
+    asm volatile("bar.sync 1, %0;" ::"n"(EW * 32) : "memory");
 
-    // ---- epilogue: thread = TMEM lane = entry row of the tile ----
+    // ---- epilogue: thread = TMEM lane = entry row of the tile; with eight
+    //      epilogue warps, warps 2-5 take the first half of the group's
+    //      queries and warps 6-9 the second (multiples of four queries) ----
     const int r = (warp & 3) * 32 + lane;
     const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
+    const int cg = (warp - 2) >> 2;  // column group
     bool alive = true;
     int n = 0;
     int64_t g = g0, t = w0 - g0 * T;
     for (int i = 0; i < nitems; ++i, t = (t + 1 == T) ? (++g, 0) : t + 1) {
       const int64_t e = t * kTile + r;
-      const int64_t q0 = g * QG;
-      const int nq = (int)min((int64_t)QG, (int64_t)B - q0);
-      const int32_t* nv = ctl.nvis[g - g0];
+      const int64_t qg0 = g * QG;
+      const int nq_g = (int)min((int64_t)QG, (int64_t)B - qg0);
+      // this warp's queries of the group: [q_lo, q_lo + nq)
+      const int per = EW == 4 ? nq_g : ((nq_g + 1) / 2 + 3) / 4 * 4;
+      const int q_lo = min(nq_g, cg * per);
+      const int nq = min(nq_g, q_lo + per) - q_lo;
+      const int64_t q0 = qg0 + q_lo;
+      const int32_t* nv = ctl.nvis[g - g0] + q_lo;
+      const uint32_t col0 = (uint32_t)(q_lo * H_I);  // this warp's first accumulator column
       if (processed(i, g, t)) {
         const int ab = n & 1;
         const uint32_t ph = ((uint32_t)n >> 1) & 1u;
@@ -269,11 +283,11 @@ index_tc_kernel(const __grid_constant__ CUtensorMap tmap, const uint8_t* __restr
           // column order
           tc_fence_after();
           if (H_I == 8)
-            score_columns<8>(tmem + lane_base + ab * NB, nq, e, N, nv, scores + q0 * N);
+            score_columns<8>(tmem + lane_base + ab * NB + col0, nq, e, N, nv, scores + q0 * N);
           else if (H_I == 16)
-            score_columns<16>(tmem + lane_base + ab * NB, nq, e, N, nv, scores + q0 * N);
+            score_columns<16>(tmem + lane_base + ab * NB + col0, nq, e, N, nv, scores + q0 * N);
           else
-            score_columns<32>(tmem + lane_base + ab * NB, nq, e, N, nv, scores + q0 * N);
+            score_columns<32>(tmem + lane_base + ab * NB + col0, nq, e, N, nv, scores + q0 * N);
           tc_fence_before();
           __syncwarp();
           if (lane == 0) mbar_arrive(su32(&ctl.acc_empty[ab]));
@@ -287,7 +301,7 @@ index_tc_kernel(const __grid_constant__ CUtensorMap tmap, const uint8_t* __restr
             int h = 0;
             for (; h + 16 <= H_I; h += 16) {
               float v[16];
-              tmem_ld16(tmem + lane_base + ab * NB + qq * H_I + h, v);
+              tmem_ld16(tmem + lane_base + ab * NB + col0 + qq * H_I + h, v);
               tmem_wait_ld();
 #pragma unroll
               for (int j = 0; j < 16; ++j) acc += v[j];
@@ -296,10 +310,10 @@ index_tc_kernel(const __grid_constant__ CUtensorMap tmap, const uint8_t* __restr
               float v[16];
               // 16 columns starting at this query's remaining heads (stays inside NB:
               // NB is a multiple of 16 and QG * H_I <= NB)
-              const int cbase = min(qq * H_I + h, NB - 16);
+              const int cbase = min((int)col0 + qq * H_I + h, NB - 16);
               tmem_ld16(tmem + lane_base + ab * NB + cbase, v);
               tmem_wait_ld();
-              const int off = qq * H_I + h - cbase;
+              const int off = (int)col0 + qq * H_I + h - cbase;
 #pragma unroll
               for (int j = 0; j < 16; ++j)
                 if (j >= off && j < off + (H_I - h)) acc += v[j];
@@ -344,7 +358,7 @@ EncodeTiledFn encode_fn() {
   return fn;
 }
 
-template <int D_I>
+template <int D_I, int EW>
 cudaError_t launch_t(const uint8_t* q_fp8, const uint8_t* k_fp8, int B, int H_I, int64_t N,
                      int64_t kv_seq_stride, int q_per_seq, int QG, int NB, const int32_t* q_pos,
                      int ratio, float* scores, int32_t* status, cudaStream_t stream) {
@@ -375,11 +389,11 @@ cudaError_t launch_t(const uint8_t* q_fp8, const uint8_t* k_fp8, int B, int H_I,
   uint32_t smem = L::alloc(NB);
   const uint32_t cap_smem = 232448u / max_ctas - 1024u;  // leaves room for the runtime's reservation
   if (max_ctas < 16 && smem < cap_smem) smem = cap_smem;
-  cudaError_t e = cudaFuncSetAttribute(index_tc_kernel<D_I>,
+  cudaError_t e = cudaFuncSetAttribute(index_tc_kernel<D_I, EW>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   // one wave: as many CTAs as fit at once, but each range within two groups
-  e = cudaFuncSetAttribute(index_tc_kernel<D_I>, cudaFuncAttributePreferredSharedMemoryCarveout,
+  e = cudaFuncSetAttribute(index_tc_kernel<D_I, EW>, cudaFuncAttributePreferredSharedMemoryCarveout,
                            100);
   if (e != cudaSuccess) return e;
   int dev = 0, smem_sm = 0;
@@ -389,11 +403,12 @@ cudaError_t launch_t(const uint8_t* q_fp8, const uint8_t* k_fp8, int B, int H_I,
     return e;
   int per_sm = smem_sm / (int)(smem + 1024);  // the runtime reserves 1 KiB per CTA
   if (per_sm > 4) per_sm = 4;
+  if (per_sm > 12 / EW) per_sm = 12 / EW;  // registers: 3 CTAs of 6 warps or 2 of 10
   if (per_sm < 1) per_sm = 1;
   int64_t C = (int64_t)per_sm * device_sm_count();
   if (C > W) C = W;
   if (C < groups) C = groups;  // W / C <= T: no range spans more than two groups
-  return launch_kernel(index_tc_kernel<D_I>, dim3((unsigned)C), dim3(kIdxThreads), smem, stream,
+  return launch_kernel(index_tc_kernel<D_I, EW>, dim3((unsigned)C), dim3(idx_threads<EW>()), smem, stream,
                        false, map, q_fp8, B, H_I, N, kv_seq_stride, q_per_seq, QG, NB, T, W, q_pos,
                        ratio, scores, status);
 }
@@ -418,19 +433,26 @@ cudaError_t launch_index_scores_tc(const uint8_t* q_fp8, const uint8_t* k_fp8, i
   } else {
     return cudaErrorNotSupported;
   }
+  // eight epilogue warps when a tile's accumulator has 256 head columns per
+  // entry (query groups of 32-head queries: the epilogue bounds those); four
+  // otherwise (measured: with 128 columns the split epilogue was slower)
+  const bool wide = NB >= 256;
+#define CSA2_IDX_LAUNCH(DI)                                                                     \
+  return wide ? launch_t<DI, 8>(q_fp8, k_fp8, B, H_I, N, kv_seq_stride, q_per_seq, QG, NB,    \
+                                q_pos, ratio, scores, status, stream)                          \
+              : launch_t<DI, 4>(q_fp8, k_fp8, B, H_I, N, kv_seq_stride, q_per_seq, QG, NB,    \
+                                q_pos, ratio, scores, status, stream)
   switch (D_I) {
     case 32:
-      return launch_t<32>(q_fp8, k_fp8, B, H_I, N, kv_seq_stride, q_per_seq, QG, NB, q_pos, ratio,
-                          scores, status, stream);
+      CSA2_IDX_LAUNCH(32);
     case 64:
-      return launch_t<64>(q_fp8, k_fp8, B, H_I, N, kv_seq_stride, q_per_seq, QG, NB, q_pos, ratio,
-                          scores, status, stream);
+      CSA2_IDX_LAUNCH(64);
     case 128:
-      return launch_t<128>(q_fp8, k_fp8, B, H_I, N, kv_seq_stride, q_per_seq, QG, NB, q_pos,
-                           ratio, scores, status, stream);
+      CSA2_IDX_LAUNCH(128);
     default:
       return cudaErrorNotSupported;
   }
+#undef CSA2_IDX_LAUNCH
 }
 
 }  // namespace csa2
