@@ -473,9 +473,9 @@ def run_gpu(args, rank, world, local):
         # then (once step i - 1 has read the cache) its packed appended rows,
         # indexer queries and positions; its layer group runs on the compute
         # stream; a download stream copies its outputs out while step i + 1
-        # computes.  Sixteen such steps are one CUDA graph (launching them one
+        # computes.  Thirty-two such steps are one CUDA graph (launching them one
         # call at a time keeps the host busier than the GPU); the graph's
-        # replays follow one another, so one step boundary in sixteen does not
+        # replays follow one another, so one step boundary in thirty-two does not
         # overlap.  Every step still moves all its bytes in and out.
         try:
             sets = []
@@ -507,7 +507,7 @@ def run_gpu(args, rank, world, local):
                 hob = [torch.empty_like(o, device="cpu").pin_memory() for o in lgb.out]
                 sets.append(dict(up_q=upqb, up=upb, lg=lgb, out=lgb.out, host=hob))
             s_up, s_dn = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
-            n_cap = 16
+            n_cap = 32
             evs = [{k_: torch.cuda.Event() for k_ in ("up", "c", "d")} for _ in range(n_cap)]
             for st_ in sets:   # first launches (library set-up) outside the capture
                 st_["lg"]()
@@ -568,8 +568,9 @@ def run_gpu(args, rank, world, local):
                 e2e["value"] = piped_v
                 e2e["issue"] = ("steps in flight together: per step the queries' upload, then the "
                                 "packed rest, on an upload stream, the layer group on the compute "
-                                "stream, the outputs' copy on a download stream; sixteen steps per "
-                                "CUDA graph (graph_value / eager_value: one step at a time)")
+                                "stream, the outputs' copy on a download stream; thirty-two "
+                                "steps per CUDA graph (graph_value / eager_value: one step at a "
+                                "time)")
             del g_p, sets
         except RuntimeError as ex:
             torch.cuda.synchronize()
